@@ -1,0 +1,331 @@
+"""Plain fp64 CPU oracle for Kimi Delta Attention (KDA).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` import this package.  The GPU
+library never imports, loads or calls it, and this package imports nothing
+from the GPU library; the two share no code.  Inputs reach both sides from the
+seeded generators in ``hybrid_linear_attention_delta_gb300.inputs``, which hold
+none of the method's arithmetic.
+
+What is computed, and where it is stated:
+
+* The recurrence (the gated delta rule with per-channel decay, fp32 state per
+  (sequence, head), "a fixed-size matrix-like recurrent state per layer" --
+  "Kimi K3 + vLLM: Inside the Day-0 Production Integration", section "Kimi
+  Delta Attention: When Prefix Caching Meets Recurrent State"; "Kimi K3 on
+  vLLM: Up to 370 Tokens/sec", section "Kimi Delta Attention: a hybrid
+  recurrent + full-attention stack")::
+
+      S_t = (I - b_t k_t k_t^T) Diag(exp g_t) S_{t-1} + b_t k_t v_t^T
+      o_t = S_t^T q_t
+
+  ``recurrence`` evaluates it token by token; ``kda_oracle.c`` is the same
+  sequential loop in C with threads over independent (sequence, head, column
+  block) units, used for large cases and for the CPU baseline.
+
+* The chunked evaluation (``chunked``) is the 64-token-chunk WY/UT form that
+  the GPU prefill uses, written out in fp64 with library primitives (matmul,
+  triangular solve).  It is pinned to the sequential form, not trusted alone.
+
+* Serving semantics of the prefix cache ("Separating Physical Blocks,
+  Scheduler Alignment, and Prefix Matching"; "Interval-Based and
+  Marconi-Style Retention" of the Day-0 integration page): a sequence resumes
+  from a cached state that is copied on write into a private destination slot
+  before extension; snapshots are taken every ``snap_interval`` tokens of the
+  segment; the final (prompt-boundary) state is always kept.  Decode
+  ("a fused CUDA kernel ... for decode", and the speculative-decoding verify
+  path) applies the same step to one or several tokens in place on a pool slot
+  and can record the state after each token for rollback.
+
+Every function here has pins in ``tests/test_oracle_pins.py`` (closed forms,
+invariants, exact-rational brute force, sequential-vs-chunked agreement,
+C-vs-numpy agreement).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libkda_oracle.so")
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_lib = None
+
+
+# ----------------------------------------------------------------------------
+# build / load the C oracle
+# ----------------------------------------------------------------------------
+
+def build(force: bool = False) -> str:
+    """Compile kda_oracle.c into a shared library with the host gcc."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        i32 = ctypes.c_int32
+        lib.kda_oracle_run.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, P, i32, P, P, P, P,
+                                       i32, P, i32, i32, i32]
+        lib.kda_oracle_run.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _f64(x) -> np.ndarray:
+    """Exact upcast to a C-contiguous float64 array (bf16/fp32 -> fp64 is exact)."""
+    if hasattr(x, "detach"):  # a torch tensor
+        x = x.detach().cpu().float().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ----------------------------------------------------------------------------
+# one (sequence, head): sequential and chunked fp64 forms
+# ----------------------------------------------------------------------------
+
+def recurrence(q, k, v, g, beta, S0=None, *, no_delta=False, return_states=False):
+    """Token-by-token fp64 KDA for ONE (sequence, head).
+
+    q, k, g: [L, dk]; v: [L, dv]; beta: [L]; S0: [dk, dv] or None (zero).
+    Returns (o [L, dv], S_L [dk, dv]) and, with ``return_states``, also the
+    state after every token [L, dk, dv].
+
+    Step t (the operator order of the definition: decay first, then the delta
+    correction against the decayed state, then the write; the output reads the
+    state after token t's own update):
+        S' = Diag(exp g_t) S ;  u = beta_t (v_t - S'^T k_t) ;  S = S' + k_t u^T ;
+        o_t = S^T q_t
+    ``no_delta`` is a test hook that drops the correction (u = v_t), which
+    turns the step into plain gated linear attention.
+    """
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(g)
+    beta = _f64(beta).reshape(-1)
+    L, dk = k.shape
+    dv = v.shape[1]
+    S = np.zeros((dk, dv)) if S0 is None else _f64(S0).copy()
+    o = np.zeros((L, dv))
+    states = np.zeros((L, dk, dv)) if return_states else None
+    for t in range(L):
+        S = np.exp(g[t])[:, None] * S
+        u = v[t] if no_delta else beta[t] * (v[t] - S.T @ k[t])
+        S = S + np.outer(k[t], u)
+        o[t] = S.T @ q[t]
+        if return_states:
+            states[t] = S
+    if return_states:
+        return o, S, states
+    return o, S
+
+
+def chunked(q, k, v, g, beta, S0=None, *, C=64, snap_interval=0):
+    """Chunked (WY / UT-transform) fp64 KDA for ONE (sequence, head).
+
+    For each chunk of C' <= C tokens with start state S0 and in-chunk
+    positions r = 1..C':
+        G_r   = sum_{i<=r} g_i                 (per channel)
+        K+    = K * exp(G),  K- = K * exp(-G),  Q+ = Q * exp(G)
+        A     = Diag(beta) * strict_lower(K+ K-^T)
+        T     = (I + A)^{-1} Diag(beta)        (unit lower-triangular solve)
+        W     = T K+ ,  U~ = T V ,  U = U~ - W S0
+        O     = Q+ S0 + lower_incl(Q+ K-^T) U
+        S_end = Diag(exp G_C') S0 + (K * exp(G_C' - G))^T U
+    Row r of U is u_r of the sequential form, so O and S_end equal the
+    token-by-token result up to rounding.  Returns (o, S_L, snapshots) where
+    snapshots are the states after every ``snap_interval`` tokens (which must
+    then be a multiple of C).
+    """
+    import scipy.linalg as sla
+
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(g)
+    beta = _f64(beta).reshape(-1)
+    L, dk = k.shape
+    dv = v.shape[1]
+    if snap_interval and snap_interval % C:
+        raise ValueError("snap_interval must be a multiple of the chunk size")
+    S = np.zeros((dk, dv)) if S0 is None else _f64(S0).copy()
+    o = np.zeros((L, dv))
+    snaps = []
+    for c0 in range(0, L, C):
+        c1 = min(c0 + C, L)
+        n = c1 - c0
+        G = np.cumsum(g[c0:c1], axis=0)
+        Kp = k[c0:c1] * np.exp(G)
+        Km = k[c0:c1] * np.exp(-G)
+        Qp = q[c0:c1] * np.exp(G)
+        b = beta[c0:c1]
+        A = b[:, None] * np.tril(Kp @ Km.T, -1)
+        T = sla.solve_triangular(np.eye(n) + A, np.diag(b), lower=True, unit_diagonal=True)
+        W = T @ Kp
+        U = T @ v[c0:c1] - W @ S
+        o[c0:c1] = Qp @ S + np.tril(Qp @ Km.T) @ U
+        S = np.exp(G[-1])[:, None] * S + (k[c0:c1] * np.exp(G[-1] - G)).T @ U
+        if snap_interval and c1 % snap_interval == 0:
+            snaps.append(S.copy())
+    return o, S, (np.stack(snaps) if snaps else np.zeros((0, dk, dv)))
+
+
+# ----------------------------------------------------------------------------
+# packed varlen batches (the C oracle, or the numpy loop for tiny cases)
+# ----------------------------------------------------------------------------
+
+def snapshot_offsets(cu_seqlens: Sequence[int], snap_interval: int):
+    """Snapshot j of sequence b lives at index off[b] + j; off is the exclusive
+    scan of floor(L_b / snap_interval).  Returns (off [B], total)."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    lens = cu[1:] - cu[:-1]
+    if snap_interval <= 0:
+        return np.zeros(len(lens), dtype=np.int64), 0
+    cnt = lens // snap_interval
+    off = np.concatenate([[0], np.cumsum(cnt)[:-1]]).astype(np.int64)
+    return off, int(cnt.sum())
+
+
+@dataclass
+class Result:
+    out: np.ndarray          # [T, H, dv]
+    final: np.ndarray        # [B, H, dk, dv]
+    snaps: np.ndarray        # [n_snaps, H, dk, dv]
+
+
+def run(q, k, v, g, beta, cu_seqlens, init_states=None, snap_interval=0, *, no_delta=False,
+        units=None, cols=None, nthreads=None, backend="c") -> Result:
+    """KDA over a packed batch.
+
+    q, k, g: [T, H, dk]; v: [T, H, dv]; beta: [T, H]; cu_seqlens: [B+1];
+    init_states: [B, H, dk, dv] or None (zero).  ``units`` optionally restricts
+    the work to a set of (b, h) pairs and ``cols`` to a column range (lo, hi) of
+    the state -- columns evolve independently, so a sampled column block is an
+    exact slice of the full result.  Entries outside the sample are NaN.
+    """
+    q, k, v, g, beta = _f64(q), _f64(k), _f64(v), _f64(g), _f64(beta)
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+    B = len(cu) - 1
+    init = None if init_states is None else _f64(init_states)
+    off, n_snaps = snapshot_offsets(cu, snap_interval)
+    lo, hi = (0, dv) if cols is None else cols
+    mask = None
+    if units is not None:
+        mask = np.zeros(B * H, dtype=np.int32)
+        for (b, h) in units:
+            mask[b * H + h] = 1
+    out = np.full((T, H, dv), np.nan)
+    final = np.full((B, H, dk, dv), np.nan)
+    snaps = np.full((n_snaps, H, dk, dv), np.nan)
+    if backend == "c":
+        lib = _load()
+        rc = lib.kda_oracle_run(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu), B, H, dk,
+                                dv, _ptr(init), int(snap_interval), _ptr(off), _ptr(out),
+                                _ptr(final), _ptr(snaps) if n_snaps else None, int(no_delta),
+                                _ptr(mask), int(lo), int(hi),
+                                int(nthreads or host_cores()))
+        if rc != 0:
+            raise ValueError("kda_oracle_run rejected its arguments")
+        return Result(out, final, snaps)
+    if backend != "numpy":
+        raise ValueError(backend)
+    for b in range(B):
+        for h in range(H):
+            if mask is not None and not mask[b * H + h]:
+                continue
+            t0, t1 = int(cu[b]), int(cu[b + 1])
+            S0 = None if init is None else init[b, h][:, lo:hi]
+            o, S, st = recurrence(q[t0:t1, h], k[t0:t1, h], v[t0:t1, h, lo:hi], g[t0:t1, h],
+                                  beta[t0:t1, h], S0, no_delta=no_delta, return_states=True)
+            out[t0:t1, h, lo:hi] = o
+            final[b, h][:, lo:hi] = S
+            if snap_interval:
+                for j in range((t1 - t0) // snap_interval):
+                    snaps[off[b] + j, h][:, lo:hi] = st[(j + 1) * snap_interval - 1]
+    return Result(out, final, snaps)
+
+
+# ----------------------------------------------------------------------------
+# state-pool semantics of the two library calls
+# ----------------------------------------------------------------------------
+
+def prefill_pool(q, k, v, g, beta, cu_seqlens, init_slots, state_pool, snap_interval=0, **kw):
+    """What ``kda_prefill_varlen`` must produce.
+
+    init_slots: [B, 2] = (src, dst).  Sequence b starts from pool[src] (zero
+    state when src < 0), runs its segment, and its final state is written to
+    pool[dst] (copy-on-write: src itself is not modified unless src == dst).
+    All sources are read before any destination is written.
+    Returns (out [T,H,dv], pool_after [n_slots,H,dk,dv], snaps).
+    """
+    pool = _f64(state_pool)
+    slots = np.asarray(init_slots, dtype=np.int64).reshape(-1, 2)
+    B = slots.shape[0]
+    H, dk, dv = pool.shape[1:]
+    init = np.zeros((B, H, dk, dv))
+    for b in range(B):
+        if slots[b, 0] >= 0:
+            init[b] = pool[slots[b, 0]]
+    res = run(q, k, v, g, beta, cu_seqlens, init, snap_interval, **kw)
+    after = pool.copy()
+    for b in range(B):
+        after[slots[b, 1]] = res.final[b]
+    return res.out, after, res.snaps
+
+
+def decode_pool(q, k, v, g, beta, slot_ids, state_pool, n_tok=1, per_tok_states=False, **kw):
+    """What ``kda_decode`` must produce.
+
+    Sequence n owns tokens [n*n_tok, (n+1)*n_tok) of the [N*n_tok, H, *] inputs
+    and the pool slot slot_ids[n]; the slot is advanced in place to the state
+    after all n_tok tokens.  With ``per_tok_states`` the state after token j is
+    also returned at [n, j] (the rollback points of speculative verify).
+    Returns (out, pool_after, per_tok [N, n_tok, H, dk, dv] or None).
+    """
+    pool = _f64(state_pool)
+    slots = np.asarray(slot_ids, dtype=np.int64).reshape(-1)
+    N = len(slots)
+    H, dk, dv = pool.shape[1:]
+    cu = np.arange(N + 1, dtype=np.int64) * n_tok
+    init = np.stack([pool[s] for s in slots]) if N else np.zeros((0, H, dk, dv))
+    res = run(q, k, v, g, beta, cu, init, 1 if per_tok_states else 0, **kw)
+    after = pool.copy()
+    for n in range(N):
+        after[slots[n]] = res.final[n]
+    per = res.snaps.reshape(N, n_tok, H, dk, dv) if per_tok_states else None
+    return res.out, after, per
+
+
+def rel_l2(x, ref) -> float:
+    """Relative L2 error ||x - ref|| / ||ref|| over the finite entries of ref."""
+    x = _f64(x)
+    ref = _f64(ref)
+    m = np.isfinite(ref)
+    num = np.linalg.norm((x - ref)[m])
+    den = np.linalg.norm(ref[m])
+    return float(num / den) if den > 0 else float(num)
