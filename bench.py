@@ -1,0 +1,466 @@
+#!/usr/bin/env python
+"""KDA prefill tokens/s and decode state GB/s on one GB300, with roofline
+fractions, the fp64 CPU oracle timed beside it, and an end-to-end figure.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one ``kda_prefill_varlen`` call on the single-sequence prefill
+workload (B=1, T=8192, H=32, dk=dv=128, bf16, snapshots every 1024 tokens):
+the device-side plan kernel plus the chunked prefill kernel, which write the
+outputs, the 8 snapshots and the final state.  The same run also times the
+batched decode (256 sequences x 1 token) and the speculative-verify decode
+(64 x 8 tokens with per-token states) and reports them under "decode".
+Inputs are synthetic (seeded, see hybrid_linear_attention_delta_gb300/inputs.py).
+L2 is flushed (a 256 MiB write) between timed steps.  ``--impl reference``
+times the fp64 CPU oracle on a bounded sample of the same workload instead.
+Under torchrun (N > 1) every rank runs an independent replica (the path has
+no exchange step) and the value is the sum of tokens over ranks divided by
+the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s & decode state GB/s on 1 GB300, % of tensor/HBM roofline"
+HEADLINE = "prefill_8k"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["source"] = "fallback"
+    return d
+
+
+def prefill_algorithmic(w, lens, n_snaps, n_resumed, es):
+    """Algorithmic bytes and flops of one prefill call.
+
+    bytes per token-head: q, k, g (dk each), v (dv), beta (1) in, out (dv):
+    (3 dk + 2 dv + 1) * element size = 1282 B for bf16 at dk = dv = 128; plus
+    one dk x dv fp32 state per (sequence, head) for the final state, for each
+    snapshot and for each resumed initial state.
+    flops per token-head at chunk C = 64 (tensor-core products only):
+    5 * 2 C d (K+K-^T, Q+K-^T, T K+, T V, M U) + 3 * 2 d^2 (W S, Q+ S, K^T U)."""
+    T = sum(lens)
+    H, dk, dv = w.H, w.dk, w.dv
+    per_tok = (3 * dk + 2 * dv + 1) * es
+    state = dk * dv * 4
+    B = len(lens)
+    nbytes = T * H * per_tok + H * state * (B + n_snaps + n_resumed)
+    C = 64
+    flops = T * H * (5 * 2 * C * dk + 3 * 2 * dk * dv)
+    return nbytes, flops, T * H * per_tok
+
+
+def decode_algorithmic(w, N, n_tok, per_tok, es):
+    """Bytes of one decode call: each touched state read once and written once
+    (64 KiB each at 128 x 128 fp32), per-token states written when asked, and
+    the token I/O (3 dk + 2 dv + 1 elements per token-head)."""
+    H, dk, dv = w.H, w.dk, w.dv
+    state = dk * dv * 4
+    b = N * H * (2 * state + n_tok * (3 * dk + 2 * dv + 1) * es)
+    if per_tok:
+        b += N * H * n_tok * state
+    return b
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                if self.uuid and parts[0] != self.uuid:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, val in zip(names, parts[4:8]):
+                    if val.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "hybrid_linear_attention_delta_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key, src_files):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("source_hash") != source_hash(src_files):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ GPU arms
+
+def time_calls(fn, steps, warmup, flush, torch):
+    """Per-step CUDA-event times of fn(events) (ms): whole call and main kernel."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn(None)
+    torch.cuda.synchronize()
+    call_ms, kern_ms = [], []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn((k0, k1))
+        e1.record(stream)
+        e1.synchronize()
+        call_ms.append(e0.elapsed_time(e1))
+        kern_ms.append(k0.elapsed_time(k1))
+    return call_ms, kern_ms
+
+
+def bench_prefill(args, torch, kda, inputs, world, rank):
+    w = inputs.WORKLOADS[HEADLINE]
+    b = inputs.make_batch(w, device="cuda")
+    dev = {n: getattr(b, n) for n in ("q", "k", "v", "g", "beta")}
+    cu = b.cu_seqlens.cuda()
+    slots = b.init_slots.cuda()
+    pool = b.pool
+    T, H = dev["q"].shape[:2]
+    out = torch.empty((T, H, w.dv), dtype=dev["q"].dtype, device="cuda")
+    n_snaps = kda.kda_snapshot_count(b.cu_seqlens, w.snap_interval)
+    snaps = torch.empty((n_snaps, H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+    ws = kda.workspace_for(len(b.cu_seqlens) - 1, H, pool.shape[0])
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    launches = []
+
+    def call(events):
+        kda.kda_prefill_varlen(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], cu, slots,
+                               pool, out, w.snap_interval, snaps, workspace=ws, events=events)
+        launches.append(kda.kda_last_launch_count())
+
+    call(None)
+    st, bits = kda.kda_device_status(ws)
+    if st != kda.KDA_OK:
+        raise RuntimeError(f"prefill device check failed: {st} bits={bits}")
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(_uuid(torch))
+    clocks.start()
+    launches.clear()
+    call_ms, kern_ms = time_calls(call, args.steps, args.warmup, flush, torch)
+    timed_launches = sum(launches[-args.steps:])
+    ck = clocks.stop()
+
+    # end to end through the same public call, host (pinned) buffers in and out
+    host = {n: t.cpu().pin_memory() for n, t in dev.items()}
+    host_cu, host_slots = b.cu_seqlens.pin_memory(), b.init_slots.pin_memory()
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + \
+        host_cu.numel() * 4 + host_slots.numel() * 4
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for n in dev:
+            dev[n].copy_(host[n], non_blocking=True)
+        cu.copy_(host_cu, non_blocking=True)
+        slots.copy_(host_slots, non_blocking=True)
+        kda.kda_prefill_varlen(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], cu, slots,
+                               pool, out, w.snap_interval, snaps, workspace=ws)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(max(3, args.steps // 2)):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    st, bits = kda.kda_device_status(ws)
+    if st != kda.KDA_OK:
+        raise RuntimeError(f"prefill device check failed: {st} bits={bits}")
+
+    lens = [T]
+    nbytes, flops, _ = prefill_algorithmic(w, lens, n_snaps, 0, dev["q"].element_size())
+    return dict(w=w, T=T, call_ms=call_ms, kern_ms=kern_ms, clocks=ck, nbytes=nbytes,
+                flops=flops, launches=timed_launches, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
+                n_snaps=n_snaps)
+
+
+def bench_decode(name, args, torch, kda, inputs):
+    w = inputs.WORKLOADS[name]
+    b = inputs.make_batch(w, device="cuda")
+    dev = {n: getattr(b, n) for n in ("q", "k", "v", "g", "beta")}
+    slot_ids = b.slot_ids.cuda()
+    pool = b.pool
+    N = slot_ids.numel()
+    H = w.H
+    out = torch.empty((N * w.n_tok, H, w.dv), dtype=dev["q"].dtype, device="cuda")
+    per = (torch.empty((N, w.n_tok, H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+           if w.per_tok_states else None)
+    ws = kda.workspace_for(N, H, pool.shape[0])
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def call(events):
+        kda.kda_decode(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], slot_ids, pool, out,
+                       w.n_tok, per, workspace=ws, events=events)
+
+    call_ms, kern_ms = time_calls(call, args.steps, args.warmup, flush, torch)
+    st, bits = kda.kda_device_status(ws)
+    if st != kda.KDA_OK:
+        raise RuntimeError(f"decode device check failed: {st} bits={bits}")
+    nbytes = decode_algorithmic(w, N, w.n_tok, w.per_tok_states, dev["q"].element_size())
+    return dict(w=w, N=N, call_ms=call_ms, kern_ms=kern_ms, nbytes=nbytes)
+
+
+def _uuid(torch):
+    try:
+        u = torch.cuda.get_device_properties(0).uuid
+        return "GPU-" + str(u)
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(target_s=12.0, max_heads=None):
+    """Times the fp64 C oracle on whole heads of the headline workload until
+    about ``target_s`` seconds of CPU work; returns a cpu_baseline dict whose
+    value is full-workload-equivalent tokens/s."""
+    import numpy as np
+    import oracle
+    from hybrid_linear_attention_delta_gb300 import inputs
+    w = inputs.WORKLOADS[HEADLINE]
+    b = inputs.make_batch(w, device="cpu")
+    H = w.H
+    cores = oracle.host_cores()
+    arrs = {n: oracle._f64(getattr(b, n)) for n in ("q", "k", "v", "g", "beta")}
+    cu = np.array([0, w.T], dtype=np.int64)
+
+    def run_heads(hs):
+        sub = {n: np.ascontiguousarray(a[:, hs]) for n, a in arrs.items()}
+        t0 = time.perf_counter()
+        oracle.run(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], cu, None,
+                   w.snap_interval, nthreads=cores)
+        return time.perf_counter() - t0
+
+    t1 = run_heads([0])
+    per_head = max(t1, 1e-3)
+    n = int(min(max_heads or H, max(1, target_s / per_head)))
+    hs = list(range(n))
+    t = run_heads(hs) if n > 1 else t1
+    value = w.T * (n / H) / t
+    return {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {H} heads x {w.T} tokens of the headline prefill (C fp64, "
+                      f"{cores} threads over 16-column state blocks), {t:.2f} s; value scaled "
+                      f"to the full {H}-head workload",
+            "seconds": t}
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+
+    import torch
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    import hybrid_linear_attention_delta_gb300 as kda
+    from hybrid_linear_attention_delta_gb300 import inputs
+    kda.lib()   # raises if the CUDA library has not been built
+
+    P = peaks()
+    pre = bench_prefill(args, torch, kda, inputs, world, rank)
+    step_s = statistics.mean(pre["call_ms"]) / 1e3
+    kern_s = statistics.mean(pre["kern_ms"]) / 1e3
+    e2e_s = statistics.mean(pre["e2e_ms"]) / 1e3
+    if world > 1:
+        t = torch.tensor([step_s, e2e_s], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_s, e2e_s = float(t[0]), float(t[1])
+    tokens = pre["T"] * world
+
+    dec = {}
+    if not args.no_decode:
+        for name in ("decode_256x1", "verify_64x8"):
+            r = bench_decode(name, args, torch, kda, inputs)
+            ks = statistics.mean(r["kern_ms"]) / 1e3
+            cs = statistics.mean(r["call_ms"]) / 1e3
+            gbs = r["nbytes"] / ks / 1e9
+            dec[name] = {"workload": r["w"].note, "ms_per_call": cs * 1e3,
+                         "kernel_ms": ks * 1e3, "tokens_per_s": r["N"] * r["w"].n_tok / cs,
+                         "state_GBps": gbs, "algorithmic_bytes": r["nbytes"],
+                         "roofline": {"bound": "hbm", "achieved": gbs, "peak": P["hbm_gbs"],
+                                      "unit": "GB/s", "frac": gbs / P["hbm_gbs"],
+                                      "traffic": ncu_traffic("decode128_" + name,
+                                                             ["kda_decode.cu"]),
+                                      "peak_source": P["source"]}}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.barrier()
+        return 0
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = oracle_sample()
+        cpu.pop("seconds", None)
+
+    algo_gbs = pre["nbytes"] / kern_s / 1e9
+    algo_tflops = pre["flops"] / kern_s / 1e12
+    chunked = "kda_chunked.cu"
+    line = {
+        "metric": METRIC,
+        "value": tokens / step_s,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; q,k L2-normalised, g=-exp(N(-3,1)), beta=sigmoid(N(0,1)))",
+        "config": {"workload": pre["w"].note, "B": 1, "T": pre["T"], "H": pre["w"].H,
+                   "dk": pre["w"].dk, "dv": pre["w"].dv, "snapshots": pre["n_snaps"],
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "l2": "flushed between timed steps (256 MiB write)"},
+        "roofline": {"bound": "hbm", "achieved": algo_gbs, "peak": P["hbm_gbs"], "unit": "GB/s",
+                     "frac": algo_gbs / P["hbm_gbs"],
+                     "traffic": ncu_traffic("prefill_" + HEADLINE, [chunked, "kda_recurrent.cu"]),
+                     "kernel_ms": kern_s * 1e3, "algorithmic_bytes": pre["nbytes"],
+                     "peak_source": P["source"],
+                     "tensor": {"achieved": algo_tflops, "unit": "TFLOP/s",
+                                "peak": P.get("bf16_tflops"),
+                                "frac": algo_tflops / P.get("bf16_tflops", 1900.0),
+                                "algorithmic_flops": pre["flops"]}},
+        "cpu_baseline": cpu,
+        "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": pre["h2d"],
+                "d2h_bytes_per_step": pre["d2h"]},
+        "gpu_launches": pre["launches"],
+        "clocks": pre["clocks"],
+        "decode": dec,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+    return 0
+
+
+def reference_arm(args, world, rank):
+    """The fp64 CPU oracle as it stands, on bounded samples of the workload."""
+    if rank != 0:
+        return 0
+    import oracle
+    per = []
+    info = None
+    for i in range(args.warmup + args.steps):
+        r = oracle_sample(target_s=2.0, max_heads=4)
+        if i >= args.warmup:
+            per.append(r)
+        info = r
+    value = statistics.mean(r["value"] for r in per)
+    ms = statistics.mean(r["seconds"] for r in per) * 1e3
+    cpu = {"value": value, "unit": "tokens/s", "cores": info["cores"], "kind": "oracle",
+           "sample": info["sample"]}
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": "prefill_8k: B=1 T=8192 H=32 dk=dv=128, snapshots every 1024",
+                       "sample": info["sample"]},
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,183 @@
+"""Kimi Delta Attention (KDA) prefill and decode on one GB300 (sm_103a).
+
+This package is a thin binding over ``libkda.so`` (C ABI in include/kda.h):
+the Python functions below carry the same names as the C entry points and do
+argument marshalling only -- every step of the computation runs in the
+library's CUDA kernels.  PyTorch provides device memory and streams.  There is
+no CPU fallback: if ``libkda.so`` has not been built, importing the binding's
+entry points raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from ._build import LIB_PATH, build  # noqa: F401
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_DEVICE_CHECK, \
+    KDA_ERR_TIMEOUT = range(6)
+KDA_F32, KDA_BF16 = 0, 1
+KDA_ALGO_AUTO, KDA_ALGO_RECURRENT, KDA_ALGO_CHUNKED = 0, 1, 2
+
+EXPORTS = ("kda_prefill_varlen", "kda_decode", "kda_workspace_bytes", "kda_snapshot_count",
+           "kda_device_status", "kda_status_string", "kda_last_launch_count")
+
+
+class KdaArgs(ctypes.Structure):
+    """Mirror of ``kda_args`` in include/kda.h."""
+    _fields_ = [("B", ctypes.c_int32), ("T_total", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("n_slots", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("algo", ctypes.c_int32),
+                ("snaps_capacity", ctypes.c_int64), ("stream", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("ev_begin", ctypes.c_void_p), ("ev_end", ctypes.c_void_p)]
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+_lib = None
+
+
+def lib(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libkda.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None or path:
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise ImportError(f"{p} is missing: build the CUDA library first "
+                              "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(p)
+        V, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        A = ctypes.POINTER(KdaArgs)
+        L.kda_prefill_varlen.argtypes = [V, V, V, V, V, V, V, V, V, I32, V, A]
+        L.kda_prefill_varlen.restype = ctypes.c_int
+        L.kda_decode.argtypes = [V, V, V, V, V, V, V, V, I32, V, A]
+        L.kda_decode.restype = ctypes.c_int
+        L.kda_workspace_bytes.argtypes = [A]
+        L.kda_workspace_bytes.restype = ctypes.c_size_t
+        L.kda_snapshot_count.argtypes = [V, I32, I32]
+        L.kda_snapshot_count.restype = I64
+        L.kda_device_status.argtypes = [A, ctypes.POINTER(ctypes.c_uint32)]
+        L.kda_device_status.restype = ctypes.c_int
+        L.kda_status_string.argtypes = [ctypes.c_int]
+        L.kda_status_string.restype = ctypes.c_char_p
+        L.kda_last_launch_count.argtypes = []
+        L.kda_last_launch_count.restype = I32
+        if path:
+            return L
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().kda_status_string(int(status)).decode()
+
+
+# ---------------------------------------------------------------- marshalling
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libkda must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def make_args(*, B, T_total, H, dk, dv, n_slots, dtype, algo=KDA_ALGO_AUTO, snaps_capacity=0,
+              stream=None, workspace=None, events=None) -> KdaArgs:
+    a = KdaArgs(B=B, T_total=T_total, H=H, dk=dk, dv=dv, n_slots=n_slots, dtype=dtype,
+                algo=algo, snaps_capacity=snaps_capacity)
+    a.stream = _stream_ptr(stream)
+    if workspace is not None:
+        a.workspace = workspace.data_ptr()
+        a.workspace_bytes = workspace.numel() * workspace.element_size()
+    if events is not None:
+        a.ev_begin = events[0].cuda_event
+        a.ev_end = events[1].cuda_event
+    return a
+
+
+def workspace_for(B: int, H: int, n_slots: int, device="cuda"):
+    """A zero-filled workspace tensor large enough for (B, H, n_slots)."""
+    import torch
+    a = KdaArgs(B=B, H=H, n_slots=n_slots)
+    n = lib().kda_workspace_bytes(ctypes.byref(a))
+    return torch.zeros(max(int(n), 256), dtype=torch.uint8, device=device)
+
+
+def kda_workspace_bytes(B: int, H: int, n_slots: int) -> int:
+    a = KdaArgs(B=B, H=H, n_slots=n_slots)
+    return int(lib().kda_workspace_bytes(ctypes.byref(a)))
+
+
+def kda_snapshot_count(cu_seqlens_host, snap_interval: int) -> int:
+    import torch
+    cu = torch.as_tensor(cu_seqlens_host, dtype=torch.int32).contiguous().cpu()
+    n = lib().kda_snapshot_count(cu.data_ptr(), cu.numel() - 1, int(snap_interval))
+    if n < 0:
+        raise KdaError(KDA_ERR_INVALID_ARG, "kda_snapshot_count")
+    return int(n)
+
+
+def kda_prefill_varlen(q, k, v, g, beta, cu_seqlens, init_slots, state_pool, out,
+                       snap_interval: int = 0, snaps=None, *, workspace, stream=None,
+                       algo: int = KDA_ALGO_AUTO, events=None) -> None:
+    """Varlen chunked prefill (see kda_prefill_varlen in include/kda.h).
+    All tensors are CUDA tensors; raises KdaError on a nonzero status."""
+    a = make_args(B=cu_seqlens.numel() - 1, T_total=q.shape[0], H=q.shape[1], dk=q.shape[2],
+                  dv=v.shape[2], n_slots=state_pool.shape[0], dtype=_dtype_code(q), algo=algo,
+                  snaps_capacity=0 if snaps is None else snaps.shape[0], stream=stream,
+                  workspace=workspace, events=events)
+    st = lib().kda_prefill_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                  _ptr(cu_seqlens), _ptr(init_slots), _ptr(state_pool), _ptr(out),
+                                  int(snap_interval), _ptr(snaps), ctypes.byref(a))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prefill_varlen")
+
+
+def kda_decode(q, k, v, g, beta, slot_ids, state_pool, out, n_tok: int = 1,
+               per_tok_states=None, *, workspace, stream=None, events=None) -> None:
+    """In-place decode of n_tok tokens per sequence (see kda_decode in include/kda.h)."""
+    a = make_args(B=slot_ids.numel(), T_total=q.shape[0], H=q.shape[1], dk=q.shape[2],
+                  dv=v.shape[2], n_slots=state_pool.shape[0], dtype=_dtype_code(q),
+                  stream=stream, workspace=workspace, events=events)
+    st = lib().kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(slot_ids),
+                          _ptr(state_pool), _ptr(out), int(n_tok), _ptr(per_tok_states),
+                          ctypes.byref(a))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode")
+
+
+def kda_device_status(workspace, stream=None):
+    """(status, error bits) of device-side checks since the last query; clears them."""
+    a = make_args(B=0, T_total=0, H=1, dk=128, dv=128, n_slots=1, dtype=KDA_BF16,
+                  stream=stream, workspace=workspace)
+    bits = ctypes.c_uint32(0)
+    st = lib().kda_device_status(ctypes.byref(a), ctypes.byref(bits))
+    return int(st), int(bits.value)
+
+
+def kda_last_launch_count() -> int:
+    return int(lib().kda_last_launch_count())

@@ -1,0 +1,178 @@
+// kda_api.cu -- the extern "C" entry points of libkda.so (declared in
+// include/kda.h): host-side argument checks, workspace carving, and the
+// stream-ordered launches.  No device memory is allocated here.
+#include <atomic>
+#include <cstring>
+
+#include "kda_internal.cuh"
+
+namespace {
+
+thread_local int32_t g_last_launches = 0;
+std::atomic<uint32_t> g_epoch{0};
+
+uint32_t next_epoch() {
+  uint32_t e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  if (e == 0) e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;  // 0 marks "never claimed"
+  return e;
+}
+
+bool dim_ok(int32_t d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kda_status check_common(const kda_args *a) {
+  if (!a) return KDA_ERR_INVALID_ARG;
+  if (a->dtype != KDA_F32 && a->dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (a->B < 0 || a->T_total < 0 || a->H <= 0 || a->n_slots <= 0) return KDA_ERR_INVALID_ARG;
+  if (!dim_ok(a->dk) || !dim_ok(a->dv)) return KDA_ERR_UNSUPPORTED;
+  if (!a->workspace || (reinterpret_cast<uintptr_t>(a->workspace) & 255u)) return KDA_ERR_INVALID_ARG;
+  if (a->workspace_bytes < kda_workspace_bytes(a)) return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+
+kda_status check_tokens(const void *q, const void *k, const void *v, const void *g,
+                        const void *beta, const void *out, int64_t T) {
+  if (T == 0) return KDA_OK;
+  const void *ps[] = {q, k, v, g, beta, out};
+  for (const void *p : ps)
+    if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+
+kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+void record(void *ev, cudaStream_t s) {
+  if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev), s);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_workspace_bytes(const kda_args *a) {
+  if (!a || a->B < 0 || a->H <= 0 || a->n_slots < 0) return 0;
+  return kda::WorkspaceLayout(a->B, a->H, a->n_slots).total;
+}
+
+int64_t kda_snapshot_count(const int32_t *cu, int32_t B, int32_t snap_interval) {
+  if (B < 0 || snap_interval < 0 || (B > 0 && !cu)) return -1;
+  if (snap_interval == 0) return 0;
+  int64_t n = 0;
+  for (int32_t b = 0; b < B; ++b) {
+    const int64_t len = (int64_t)cu[b + 1] - cu[b];
+    if (len < 0) return -1;
+    n += len / snap_interval;
+  }
+  return n;
+}
+
+kda_status kda_prefill_varlen(const void *q, const void *k, const void *v, const void *g,
+                              const void *beta, const int32_t *cu_seqlens,
+                              const int32_t *init_slots, float *state_pool, void *out,
+                              int32_t snap_interval, float *snaps, const kda_args *a) {
+  g_last_launches = 0;
+  kda_status st = check_common(a);
+  if (st != KDA_OK) return st;
+  if (snap_interval < 0 || (snap_interval > 0) != (snaps != nullptr)) return KDA_ERR_INVALID_ARG;
+  if (snaps && (!aligned16(snaps) || a->snaps_capacity < 0)) return KDA_ERR_INVALID_ARG;
+  if (a->algo < KDA_ALGO_AUTO || a->algo > KDA_ALGO_CHUNKED) return KDA_ERR_INVALID_ARG;
+  if (a->B == 0) return a->T_total == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+  if (!cu_seqlens || !init_slots || !state_pool || !aligned16(state_pool))
+    return KDA_ERR_INVALID_ARG;
+  if ((st = check_tokens(q, k, v, g, beta, out, a->T_total)) != KDA_OK) return st;
+
+  const kda::WorkspaceLayout lay(a->B, a->H, a->n_slots);
+  char *ws = static_cast<char *>(a->workspace);
+  kda::PrefillPlan p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+  p.cu_seqlens = cu_seqlens; p.init_slots = init_slots;
+  p.pool = state_pool; p.out = out; p.snaps = snaps;
+  p.snap_interval = snap_interval;
+  p.snaps_capacity = snaps ? a->snaps_capacity : 0;
+  p.B = a->B; p.T_total = a->T_total; p.H = a->H; p.dk = a->dk; p.dv = a->dv;
+  p.n_slots = a->n_slots; p.dtype = a->dtype;
+  p.err = reinterpret_cast<uint32_t *>(ws);
+  p.meta = reinterpret_cast<kda::SeqMeta *>(ws + lay.meta_off);
+  p.order = reinterpret_cast<int32_t *>(ws + lay.order_off);
+  p.claims = reinterpret_cast<uint32_t *>(ws + lay.claims_off);
+  p.epoch = next_epoch();
+  p.stream = static_cast<cudaStream_t>(a->stream);
+
+  bool chunked = kda::chunked_supported(p);
+  if (a->algo == KDA_ALGO_CHUNKED && !chunked) return KDA_ERR_UNSUPPORTED;
+  if (a->algo == KDA_ALGO_RECURRENT) chunked = false;
+
+  if ((st = from_cuda(kda::launch_meta(p))) != KDA_OK) return st;
+  g_last_launches = 1;
+  record(a->ev_begin, p.stream);
+  st = from_cuda(chunked ? kda::launch_chunked_prefill(p) : kda::launch_recurrent_prefill(p));
+  record(a->ev_end, p.stream);
+  if (st == KDA_OK) g_last_launches = 2;
+  return st;
+}
+
+kda_status kda_decode(const void *q, const void *k, const void *v, const void *g,
+                      const void *beta, const int32_t *slot_ids, float *state_pool, void *out,
+                      int32_t n_tok, float *per_tok_states, const kda_args *a) {
+  g_last_launches = 0;
+  kda_status st = check_common(a);
+  if (st != KDA_OK) return st;
+  if (n_tok < 1 || (int64_t)a->B * n_tok != a->T_total) return KDA_ERR_INVALID_ARG;
+  if (a->B == 0) return KDA_OK;
+  if (!slot_ids || !state_pool || !aligned16(state_pool)) return KDA_ERR_INVALID_ARG;
+  if (per_tok_states && !aligned16(per_tok_states)) return KDA_ERR_INVALID_ARG;
+  if ((st = check_tokens(q, k, v, g, beta, out, a->T_total)) != KDA_OK) return st;
+
+  const kda::WorkspaceLayout lay(a->B, a->H, a->n_slots);
+  char *ws = static_cast<char *>(a->workspace);
+  kda::DecodePlan p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+  p.slot_ids = slot_ids; p.pool = state_pool; p.out = out; p.per_tok = per_tok_states;
+  p.N = a->B; p.n_tok = n_tok; p.H = a->H; p.dk = a->dk; p.dv = a->dv;
+  p.n_slots = a->n_slots; p.dtype = a->dtype;
+  p.err = reinterpret_cast<uint32_t *>(ws);
+  p.claims = reinterpret_cast<uint32_t *>(ws + lay.claims_off);
+  p.epoch = next_epoch();
+  p.stream = static_cast<cudaStream_t>(a->stream);
+  const bool fast = a->dk == 128 && a->dv == 128;
+  record(a->ev_begin, p.stream);
+  st = from_cuda(fast ? kda::launch_decode128(p) : kda::launch_recurrent_decode(p));
+  record(a->ev_end, p.stream);
+  if (st == KDA_OK) g_last_launches = 1;
+  return st;
+}
+
+kda_status kda_device_status(const kda_args *a, uint32_t *detail) {
+  if (detail) *detail = 0;
+  if (!a || !a->workspace) return KDA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(a->stream);
+  uint32_t bits = 0;
+  if (cudaMemcpyAsync(&bits, a->workspace, sizeof(bits), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+  if (bits) {
+    if (cudaMemsetAsync(a->workspace, 0, sizeof(bits), s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+  }
+  if (detail) *detail = bits;
+  if (bits & kda::ERR_TIMEOUT) return KDA_ERR_TIMEOUT;
+  return bits ? KDA_ERR_DEVICE_CHECK : KDA_OK;
+}
+
+const char *kda_status_string(kda_status s) {
+  switch (s) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+    case KDA_ERR_DEVICE_CHECK: return "KDA_ERR_DEVICE_CHECK";
+    case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+  }
+  return "KDA_ERR_UNKNOWN";
+}
+
+int32_t kda_last_launch_count(void) { return g_last_launches; }
+
+}  // extern "C"

@@ -1,0 +1,115 @@
+// kda_internal.cuh -- shared definitions of the libkda.so CUDA sources.
+//
+// Workspace layout (caller-owned device memory, zero-filled once after
+// allocation, see include/kda.h):
+//   [0, 256)                 header: uint32 error bits (sticky)
+//   [256, +align(B*32))      SeqMeta[B]   per-sequence plan written by the metadata kernel
+//   [.., +align(B*4))        int32 order[B]: sequences, longest first
+//   [.., +align(n_slots*H*4*4)) uint32 claims: epoch stamps that detect two
+//                            sequences of one call writing the same state
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+enum ErrBits : uint32_t {
+  ERR_BAD_SLOT = 1u,
+  ERR_DUP_SLOT = 2u,
+  ERR_BAD_CU = 4u,
+  ERR_SNAP_CAPACITY = 8u,
+  ERR_TIMEOUT = 16u,
+};
+
+struct SeqMeta {
+  int32_t tok0;      // first packed token row
+  int32_t len;       // tokens in this segment
+  int32_t src;       // initial state slot, -1 = zero
+  int32_t dst;       // final state slot
+  int64_t snap_off;  // index of this sequence's first snapshot
+  int32_t ok;        // 0: skip every write of this sequence (a device check failed)
+  int32_t pad;
+};
+static_assert(sizeof(SeqMeta) == 32, "SeqMeta is 32 bytes");
+
+constexpr int kClaimsPerState = 4;  // one claim word per (slot, head, column block)
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WorkspaceLayout {
+  size_t meta_off, order_off, claims_off, total;
+  __host__ __device__ WorkspaceLayout(int64_t B, int64_t H, int64_t n_slots) {
+    meta_off = 256;
+    order_off = meta_off + align256((size_t)B * sizeof(SeqMeta));
+    claims_off = order_off + align256((size_t)B * sizeof(int32_t));
+    total = claims_off + align256((size_t)n_slots * H * kClaimsPerState * sizeof(uint32_t));
+  }
+};
+
+// ---------------------------------------------------------------- element io
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ void raise_error(uint32_t *err, uint32_t bits) {
+  atomicOr(err, bits);
+}
+
+// Claims (slot, head, block) for this call; returns false when another CTA of
+// the same call already claimed it (two sequences would write one state).
+__device__ __forceinline__ bool claim_state(uint32_t *claims, int64_t index, uint32_t epoch) {
+  return atomicExch(claims + index, epoch) != epoch;
+}
+
+// ---------------------------------------------------------------- launchers
+struct PrefillPlan {
+  const void *q, *k, *v, *g, *beta;
+  const int32_t *cu_seqlens, *init_slots;
+  float *pool;
+  void *out;
+  float *snaps;
+  int32_t snap_interval;
+  int64_t snaps_capacity;
+  int32_t B, T_total, H, dk, dv, n_slots, dtype;
+  uint32_t *err;
+  SeqMeta *meta;
+  int32_t *order;
+  uint32_t *claims;
+  uint32_t epoch;
+  cudaStream_t stream;
+};
+
+struct DecodePlan {
+  const void *q, *k, *v, *g, *beta;
+  const int32_t *slot_ids;
+  float *pool;
+  void *out;
+  float *per_tok;
+  int32_t N, n_tok, H, dk, dv, n_slots, dtype;
+  uint32_t *err;
+  uint32_t *claims;
+  uint32_t epoch;
+  cudaStream_t stream;
+};
+
+cudaError_t launch_meta(const PrefillPlan &p);
+cudaError_t launch_recurrent_prefill(const PrefillPlan &p);
+cudaError_t launch_recurrent_decode(const DecodePlan &p);
+cudaError_t launch_decode128(const DecodePlan &p);
+// Returns cudaErrorNotSupported when the chunked tensor-core kernel does not
+// apply to these shapes.
+bool chunked_supported(const PrefillPlan &p);
+cudaError_t launch_chunked_prefill(const PrefillPlan &p);
+
+}  // namespace kda

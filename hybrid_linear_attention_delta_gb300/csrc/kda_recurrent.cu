@@ -1,0 +1,213 @@
+// kda_recurrent.cu -- token-by-token KDA on CUDA cores, fp32 state and math.
+//
+// The recurrence (gated delta rule with per-channel decay, "Kimi K3 on vLLM:
+// Up to 370 Tokens/sec", section "Kimi Delta Attention: a hybrid recurrent +
+// full-attention stack"):
+//     S' = Diag(exp g_t) S ;  u = beta_t (v_t - S'^T k_t) ;  S = S' + k_t u^T ;
+//     o_t = S^T q_t = S'^T q_t + u (k_t . q_t)
+//
+// Columns of S evolve independently, so each thread owns one column j of one
+// (sequence, head) state and keeps its dk entries in registers for the whole
+// segment: every reduction over the key channels is thread-local and the
+// only shared traffic is the broadcast of q, k, exp(g) per token.  A CTA is
+// one warp covering 32 columns (fewer when dv < 32); the state is read once
+// and written once.  This kernel is the exact-fp32 path (fp32 inputs, shapes
+// other than dk = dv = 128) and serves decode for those shapes too.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kTile = 8;  // tokens staged in shared memory at a time
+
+struct RecArgs {
+  const void *q, *k, *v, *g, *beta;
+  float *pool;
+  void *out;
+  float *snaps;
+  int64_t snaps_capacity;
+  int32_t snap_interval;
+  int32_t H, dv, n_slots;
+  // prefill: per-sequence plan; decode: slot ids (tok0 = n * n_tok)
+  const SeqMeta *meta;
+  const int32_t *order;
+  const int32_t *slot_ids;
+  int32_t n_tok;
+  uint32_t *err;
+  uint32_t *claims;
+  uint32_t epoch;
+};
+
+// R lanes share one column (R = 2 for dk = 128 keeps the column in 64
+// registers per lane); lane (c, r) holds rows i = R*ii + r of column c.
+template <typename Tin, int DK, int R, bool DECODE>
+__global__ void __launch_bounds__(32) recurrent_kernel(RecArgs a) {
+  constexpr int DKR = DK / R;
+  const int lane = threadIdx.x;
+  const int ncol = blockDim.x / R;
+  const int c = lane / R, r = lane % R;
+  const int h = blockIdx.y;
+  const int j = blockIdx.z * ncol + c;
+  const int H = a.H, dv = a.dv;
+  const unsigned mask = 0xffffffffu >> (32 - blockDim.x);
+
+  int64_t tok0, len, snap_off;
+  int src, dst;
+  if (DECODE) {
+    const int n = blockIdx.x;
+    const int slot = a.slot_ids[n];
+    int ok = 1;
+    if (slot < 0 || slot >= a.n_slots) {
+      ok = 0;
+      if (lane == 0) raise_error(a.err, ERR_BAD_SLOT);
+    } else if (lane == 0) {
+      const int64_t idx = ((int64_t)slot * H + h) * kClaimsPerState + blockIdx.z;
+      if (!claim_state(a.claims, idx, a.epoch)) {
+        raise_error(a.err, ERR_DUP_SLOT);
+        ok = 0;
+      }
+    }
+    ok = __shfl_sync(mask, ok, 0);
+    if (!ok) return;
+    tok0 = (int64_t)n * a.n_tok;
+    len = a.n_tok;
+    src = dst = slot;
+    snap_off = (int64_t)n * a.n_tok;
+  } else {
+    const SeqMeta m = a.meta[a.order[blockIdx.x]];
+    if (!m.ok) return;
+    tok0 = m.tok0;
+    len = m.len;
+    src = m.src;
+    dst = m.dst;
+    snap_off = m.snap_off;
+  }
+
+  const int64_t state_elems = (int64_t)DK * dv;
+  float S[DKR];
+  if (src >= 0) {
+    const float *s0 = a.pool + ((int64_t)src * H + h) * state_elems + (int64_t)r * dv + j;
+#pragma unroll
+    for (int ii = 0; ii < DKR; ++ii) S[ii] = s0[(int64_t)ii * R * dv];
+  } else {
+#pragma unroll
+    for (int ii = 0; ii < DKR; ++ii) S[ii] = 0.f;
+  }
+
+  __shared__ float sk[kTile][DK], sq[kTile][DK], sa[kTile][DK];
+  __shared__ float sv[kTile][32], sb[kTile], skq[kTile];
+
+  const Tin *q = (const Tin *)a.q, *k = (const Tin *)a.k, *g = (const Tin *)a.g;
+  const Tin *v = (const Tin *)a.v, *beta = (const Tin *)a.beta;
+  Tin *out = (Tin *)a.out;
+  const int nthr = blockDim.x;
+
+  for (int64_t t0 = 0; t0 < len; t0 += kTile) {
+    const int nt = (int)((len - t0) < kTile ? (len - t0) : kTile);
+    __syncwarp(mask);
+    for (int tt = 0; tt < nt; ++tt) {
+      const int64_t row = (tok0 + t0 + tt) * H + h;
+      float kq = 0.f;
+      for (int i = lane; i < DK; i += nthr) {
+        const float kk = to_f32(k[row * DK + i]);
+        const float qq = to_f32(q[row * DK + i]);
+        sk[tt][i] = kk;
+        sq[tt][i] = qq;
+        sa[tt][i] = expf(to_f32(g[row * DK + i]));
+        kq = fmaf(kk, qq, kq);
+      }
+      for (int off = nthr / 2; off > 0; off >>= 1) kq += __shfl_xor_sync(mask, kq, off, nthr);
+      if (r == 0) sv[tt][c] = to_f32(v[row * dv + j]);
+      if (lane == 0) {
+        sb[tt] = to_f32(beta[row]);
+        skq[tt] = kq;
+      }
+    }
+    __syncwarp(mask);
+    for (int tt = 0; tt < nt; ++tt) {
+      float x = 0.f, y = 0.f;
+#pragma unroll
+      for (int ii = 0; ii < DKR; ++ii) {
+        const int i = ii * R + r;
+        const float s = S[ii] * sa[tt][i];
+        S[ii] = s;
+        x = fmaf(sk[tt][i], s, x);
+        y = fmaf(sq[tt][i], s, y);
+      }
+#pragma unroll
+      for (int off = 1; off < R; off <<= 1) {
+        x += __shfl_xor_sync(mask, x, off);
+        y += __shfl_xor_sync(mask, y, off);
+      }
+      const float u = sb[tt] * (sv[tt][c] - x);
+#pragma unroll
+      for (int ii = 0; ii < DKR; ++ii) S[ii] = fmaf(sk[tt][ii * R + r], u, S[ii]);
+      const int64_t t = tok0 + t0 + tt;
+      if (r == 0) out[(t * H + h) * dv + j] = from_f32<Tin>(fmaf(u, skq[tt], y));
+      const int64_t done = t0 + tt + 1;
+      if (a.snaps && a.snap_interval > 0 && done % a.snap_interval == 0) {
+        const int64_t s = snap_off + done / a.snap_interval - 1;
+        if (s < a.snaps_capacity) {
+          float *d = a.snaps + (s * H + h) * state_elems + (int64_t)r * dv + j;
+#pragma unroll
+          for (int ii = 0; ii < DKR; ++ii) d[(int64_t)ii * R * dv] = S[ii];
+        } else if (lane == 0) {
+          raise_error(a.err, ERR_SNAP_CAPACITY);
+        }
+      }
+    }
+  }
+  float *sd = a.pool + ((int64_t)dst * H + h) * state_elems + (int64_t)r * dv + j;
+#pragma unroll
+  for (int ii = 0; ii < DKR; ++ii) sd[(int64_t)ii * R * dv] = S[ii];
+}
+
+template <bool DECODE>
+cudaError_t launch(const RecArgs &a, int dk, int dv, int nseq, int dtype, cudaStream_t st) {
+  if (nseq == 0) return cudaSuccess;
+  const int R = dk == 128 ? 2 : 1;
+  const int ncol = (dv < 32 / R) ? dv : 32 / R;
+  dim3 grid(nseq, a.H, dv / ncol), block(ncol * R);
+#define KDA_REC_CASE(DK, RR)                                                         \
+  case DK:                                                                           \
+    if (dtype == KDA_BF16)                                                           \
+      recurrent_kernel<__nv_bfloat16, DK, RR, DECODE><<<grid, block, 0, st>>>(a);    \
+    else                                                                             \
+      recurrent_kernel<float, DK, RR, DECODE><<<grid, block, 0, st>>>(a);            \
+    break;
+  switch (dk) {
+    KDA_REC_CASE(16, 1)
+    KDA_REC_CASE(32, 1)
+    KDA_REC_CASE(64, 1)
+    KDA_REC_CASE(128, 2)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef KDA_REC_CASE
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent_prefill(const PrefillPlan &p) {
+  RecArgs a = {};
+  a.q = p.q; a.k = p.k; a.v = p.v; a.g = p.g; a.beta = p.beta;
+  a.pool = p.pool; a.out = p.out; a.snaps = p.snaps; a.snaps_capacity = p.snaps_capacity;
+  a.snap_interval = p.snap_interval; a.H = p.H; a.dv = p.dv; a.n_slots = p.n_slots;
+  a.meta = p.meta; a.order = p.order; a.err = p.err; a.claims = p.claims; a.epoch = p.epoch;
+  return launch<false>(a, p.dk, p.dv, p.B, p.dtype, p.stream);
+}
+
+cudaError_t launch_recurrent_decode(const DecodePlan &p) {
+  RecArgs a = {};
+  a.q = p.q; a.k = p.k; a.v = p.v; a.g = p.g; a.beta = p.beta;
+  a.pool = p.pool; a.out = p.out; a.snaps = p.per_tok;
+  a.snaps_capacity = (int64_t)p.N * p.n_tok;
+  a.snap_interval = p.per_tok ? 1 : 0;
+  a.H = p.H; a.dv = p.dv; a.n_slots = p.n_slots;
+  a.slot_ids = p.slot_ids; a.n_tok = p.n_tok;
+  a.err = p.err; a.claims = p.claims; a.epoch = p.epoch;
+  return launch<true>(a, p.dk, p.dv, p.N, p.dtype, p.stream);
+}
+
+}  // namespace kda

@@ -1,0 +1,177 @@
+/*
+ * kda.h -- C ABI of libkda.so: Kimi Delta Attention (KDA) prefill and decode
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * KDA is the gated delta rule with a per-channel decay.  For every (sequence,
+ * head) it carries a matrix state S in R^{dk x dv}, held in fp32, and for each
+ * token t with query q_t, key k_t (dk), value v_t (dv), log-decay g_t (dk) and
+ * write strength beta_t (scalar) it computes
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp g_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t
+ *
+ * ("Kimi K3 on vLLM: Up to 370 Tokens/sec", section "Kimi Delta Attention: a
+ * hybrid recurrent + full-attention stack": a linear-attention mechanism with a
+ * fixed-size recurrent state; "Kimi K3 + vLLM: Inside the Day-0 Production
+ * Integration", section "Kimi Delta Attention: When Prefix Caching Meets
+ * Recurrent State": a fixed-size matrix-like recurrent state per layer).
+ * g is used as given (exp g is the decay; no activation is applied) and there
+ * is no in-kernel normalisation or 1/sqrt(dk) scaling of q or k.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer argument of the compute calls is caller-owned DEVICE memory
+ *   (cu_seqlens, init_slots and slot_ids included).  The library allocates no
+ *   device memory in these calls; scratch lives in the caller's workspace.
+ * - All arrays are dense, row-major, contiguous, with 16-byte aligned base
+ *   pointers.  q, k, v, g, beta and out share the element type a->dtype.
+ *   Token-major layouts: q, k, g: [T][H][dk]; v, out: [T][H][dv]; beta: [T][H].
+ *   States: state_pool [n_slots][H][dk][dv] fp32, row i of a state is the
+ *   key channel i.
+ * - The calls are asynchronous and stream-ordered on a->stream (a
+ *   cudaStream_t; NULL is the legacy default stream).
+ * - Errors that the host can see (null pointers, bad sizes, unsupported
+ *   shapes, a too-small workspace) return immediately without launching
+ *   anything.  Errors that only the device can see (a slot id out of range, a
+ *   duplicate destination slot, non-monotone cu_seqlens, too small a snapshot
+ *   buffer) are recorded in a sticky error word in the workspace, the
+ *   offending sequence's writes are skipped (nothing outside the caller's
+ *   buffers is touched), and kda_device_status() reports and clears them.
+ * - Results are deterministic: no floating-point atomics, no order-dependent
+ *   reductions.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1,   /* a host-visible argument is wrong; nothing launched */
+  KDA_ERR_UNSUPPORTED = 2,   /* valid but not supported (shape, dtype, algo) */
+  KDA_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch, sync) */
+  KDA_ERR_DEVICE_CHECK = 4,  /* a device-side argument check failed (see kda_device_status) */
+  KDA_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Which prefill algorithm to run.  AUTO picks the tensor-core chunked kernel
+ * for bf16 with dk = dv = 128 and snap_interval % 64 == 0, else the
+ * token-recurrent CUDA-core kernel (exact fp32 recurrence, any supported
+ * shape).  The other two force one of them (CHUNKED returns
+ * KDA_ERR_UNSUPPORTED where it does not apply). */
+typedef enum { KDA_ALGO_AUTO = 0, KDA_ALGO_RECURRENT = 1, KDA_ALGO_CHUNKED = 2 } kda_algo;
+
+typedef struct {
+  int32_t B;              /* prefill: sequences in the packed batch; decode: N sequences */
+  int32_t T_total;        /* prefill: cu_seqlens[B]; decode: N * n_tok */
+  int32_t H;              /* heads */
+  int32_t dk, dv;         /* key / value head dims: each one of 16, 32, 64, 128 */
+  int32_t n_slots;        /* state_pool slots */
+  int32_t dtype;          /* kda_dtype of q, k, v, g, beta, out */
+  int32_t algo;           /* kda_algo (prefill only) */
+  int64_t snaps_capacity; /* prefill: snapshots the snaps buffer holds */
+  void *stream;           /* cudaStream_t */
+  void *workspace;        /* device scratch: >= kda_workspace_bytes(this), 256-byte aligned,
+                             ZERO-FILLED ONCE after allocation; reusable across calls that
+                             are ordered on one stream; never shared by concurrent calls */
+  size_t workspace_bytes;
+  void *ev_begin;         /* optional cudaEvent_t recorded on stream just before the main
+                             compute kernel of the call (NULL: none); for timing */
+  void *ev_end;           /* optional cudaEvent_t recorded just after it */
+} kda_args;
+
+/*
+ * Varlen chunked prefill with copy-on-write resume and state snapshots.
+ *
+ * Serving semantics follow the hybrid prefix cache of the Day-0 integration
+ * page: "Separating Physical Blocks, Scheduler Alignment, and Prefix Matching"
+ * (a cached state is copied into a private destination before extension;
+ * valid states are registered at fine prefix boundaries) and "Interval-Based
+ * and Marconi-Style Retention" (checkpoints at a fixed token interval, the
+ * prompt boundary always kept).
+ *
+ * q, k, g    [T_total][H][dk]   dtype        packed tokens of B sequences
+ * v          [T_total][H][dv]   dtype
+ * beta       [T_total][H]       dtype
+ * cu_seqlens [B+1]              int32        cu[0] = 0, non-decreasing, cu[B] = T_total;
+ *                                            sequence b owns tokens [cu[b], cu[b+1])
+ * init_slots [B][2]             int32        {src, dst}: sequence b starts from
+ *                                            state_pool[src] (src = -1: zero state) and its
+ *                                            final state is written to state_pool[dst].
+ *                                            src is only read (unless src == dst, which
+ *                                            extends in place).  dst slots must be distinct
+ *                                            and no src may be another sequence's dst.
+ * state_pool [n_slots][H][dk][dv] fp32       read at src, written at dst; all other slots
+ *                                            are left bit-identical
+ * out        [T_total][H][dv]   dtype        o_t (round-to-nearest-even for bf16)
+ * snap_interval                              0, or a positive interval: snapshot j of
+ *                                            sequence b is its state after (j+1)*interval
+ *                                            tokens of this segment (segment-relative)
+ * snaps      [n_snaps][H][dk][dv] fp32       snapshots, sequence-major then position:
+ *                                            sequence b's start at the exclusive scan of
+ *                                            floor(L_b / interval); NULL iff interval == 0;
+ *                                            n_snaps = kda_snapshot_count(...)
+ *                                            <= a->snaps_capacity
+ * Callers align segment starts to the interval (a scheduler invariant) so that
+ * segment-relative snapshots fall on absolute prefix boundaries.
+ */
+kda_status kda_prefill_varlen(const void *q, const void *k, const void *v, const void *g,
+                              const void *beta, const int32_t *cu_seqlens,
+                              const int32_t *init_slots, float *state_pool, void *out,
+                              int32_t snap_interval, float *snaps, const kda_args *a);
+
+/*
+ * Single- and multi-token decode in place on the state pool (the fused decode
+ * step of "Kimi K3 on vLLM: Up to 370 Tokens/sec", section "Kimi Delta
+ * Attention: a hybrid recurrent + full-attention stack", and the multi-token
+ * verify pass used under speculative decoding).
+ *
+ * q, k, g    [N*n_tok][H][dk]   dtype        sequence n owns rows [n*n_tok, (n+1)*n_tok)
+ * v, out     [N*n_tok][H][dv]   dtype
+ * beta       [N*n_tok][H]       dtype
+ * slot_ids   [N]                int32        distinct slots in [0, n_slots)
+ * state_pool [n_slots][H][dk][dv] fp32       slot_ids[n] advanced in place by n_tok tokens
+ * n_tok      >= 1
+ * per_tok_states [N][n_tok][H][dk][dv] fp32 or NULL: the state after each token, for
+ *                                            rollback of rejected draft tokens (copy
+ *                                            per_tok_states[n][a-1] into the slot)
+ * a->B = N, a->T_total = N * n_tok.
+ */
+kda_status kda_decode(const void *q, const void *k, const void *v, const void *g,
+                      const void *beta, const int32_t *slot_ids, float *state_pool, void *out,
+                      int32_t n_tok, float *per_tok_states, const kda_args *a);
+
+/* Workspace bytes the calls need for these sizes (uses B, H, n_slots). */
+size_t kda_workspace_bytes(const kda_args *a);
+
+/* Number of snapshots a prefill writes: sum over b of floor(L_b / snap_interval),
+ * from a HOST copy of cu_seqlens.  Returns -1 on a bad argument. */
+int64_t kda_snapshot_count(const int32_t *cu_seqlens_host, int32_t B, int32_t snap_interval);
+
+/* Synchronises a->stream, then returns KDA_OK, KDA_ERR_DEVICE_CHECK or
+ * KDA_ERR_TIMEOUT for any device-side error recorded in a->workspace since the
+ * last call to this function, and clears the record.  If detail is not NULL
+ * it receives the raw error bits (1 slot out of range, 2 duplicate slot or a
+ * source that is another sequence's destination, 4 bad cu_seqlens, 8 snapshot
+ * buffer too small, 16 wait timeout). */
+kda_status kda_device_status(const kda_args *a, uint32_t *detail);
+
+/* Human-readable name of a status code (static string). */
+const char *kda_status_string(kda_status s);
+
+/* Kernel launches issued by the last successful compute call on this host
+ * thread (for launch accounting). */
+int32_t kda_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */
