@@ -172,6 +172,8 @@ def time_calls(fn, steps, warmup, flush, torch):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(stream)   # torch creates the CUDA events lazily; the library re-records them
+        k1.record(stream)
         e0.record(stream)
         fn((k0, k1))
         e1.record(stream)

@@ -35,7 +35,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode128_kernel(DecodePlan p) {
   const int n = blockIdx.x / H, h = blockIdx.x % H;
 
   __shared__ int s_slot;
-  __shared__ float sa[kD], sk[kD], sq[kD], sv[kD], su[kD], sy[kD];
+  // su is read as float4: every staging array is 16-byte aligned
+  __shared__ __align__(16) float sa[kD];
+  __shared__ __align__(16) float sk[kD];
+  __shared__ __align__(16) float sq[kD];
+  __shared__ __align__(16) float sv[kD];
+  __shared__ __align__(16) float su[kD];
+  __shared__ __align__(16) float sy[kD];
   __shared__ __align__(16) float redx[kThreads / 32][kD];
   __shared__ __align__(16) float redy[kThreads / 32][kD];
   __shared__ float skq[4], sbeta;
