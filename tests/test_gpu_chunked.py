@@ -1,0 +1,209 @@
+"""GPU parity of the tcgen05 chunked prefill against the fp64 oracle (through
+the C ABI), plus its layout rules: snapshot placement, copy-on-write resume,
+untouched slots, split invariance and run-to-run determinism (bit-exact)."""
+
+import numpy as np
+import pytest
+import torch
+
+import hybrid_linear_attention_delta_gb300 as kda
+import oracle
+from hybrid_linear_attention_delta_gb300 import inputs
+from kda_cases import (TOL, assert_untouched, gpu_prefill, oracle_prefill, rel, touched_slots,
+                       worst_unit)
+
+pytestmark = pytest.mark.gpu
+CH = kda.KDA_ALGO_CHUNKED
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    kda.build()
+    kda.lib()
+
+
+def _case(lens, H, n_slots, slots, dv=128, index=92):
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lens), 0).to(torch.int32)
+    tt = inputs.token_tensors(int(cu[-1]), H, 128, dv, torch.bfloat16, index)
+    pool = inputs.pool_states(n_slots, H, 128, dv, index)
+    return inputs.Batch(cu_seqlens=cu, init_slots=torch.tensor(slots, dtype=torch.int32),
+                        pool=pool, **tt)
+
+
+def _check(b, snap, out, pool, snaps, tol=TOL["bf16"]):
+    ro, rpool, rsn = oracle_prefill(b, snap)
+    H = b.q.shape[1]
+    e_out = rel(out, ro)
+    e_state = max(rel(pool[s], rpool[s]) for s in touched_slots(b))
+    assert e_out <= tol, f"out rel L2 {e_out:.2e}"
+    assert e_state <= tol, f"state rel L2 {e_state:.2e}"
+    assert worst_unit(out, ro, b.cu_seqlens.numpy(), H) <= 2 * tol
+    if snap:
+        e_sn = rel(snaps, rsn)
+        assert e_sn <= tol, f"snapshot rel L2 {e_sn:.2e}"
+    return e_out, e_state
+
+
+@pytest.mark.parametrize("lens", [[64], [1], [63, 65], [200, 130, 7], [129, 0, 256]])
+def test_chunked_ragged_varlen(lens):
+    """Ragged tails and empty sequences; the narrow (64-column) dv blocks."""
+    B = len(lens)
+    slots = [[-1, b] for b in range(B)]
+    b = _case(lens, 3, B + 2, slots)
+    out, pool, snaps, (st, bits) = gpu_prefill(b, 64, algo=CH)
+    assert st == kda.KDA_OK and bits == 0
+    _check(b, 64, out, pool, snaps)
+
+
+def test_chunked_resume_cow_wide_blocks():
+    """Copy-on-write resume from cached slots with B*H >= 148 (128-column dv
+    blocks): sources stay bit-identical, untouched slots stay bit-identical."""
+    lens = [70, 130, 64, 1, 200, 33, 128, 90]
+    slots = [[3, 20], [-1, 21], [5, 22], [-1, 23], [7, 24], [9, 9], [-1, 26], [11, 27]]
+    b = _case(lens, 20, 30, slots)
+    before = b.pool.clone()
+    out, pool, snaps, (st, bits) = gpu_prefill(b, 64, algo=CH)
+    assert st == kda.KDA_OK and bits == 0
+    _check(b, 64, out, pool, snaps)
+    assert_untouched(pool, before, touched_slots(b))
+    for src in (3, 5, 7, 11):
+        assert torch.equal(pool[src].cpu(), before[src])
+
+
+def test_chunked_dv64_heads():
+    lens = [150, 64]
+    b = _case(lens, 4, 4, [[1, 2], [-1, 3]], dv=64)
+    out, pool, snaps, (st, bits) = gpu_prefill(b, 128, algo=CH)
+    assert st == kda.KDA_OK and bits == 0
+    _check(b, 128, out, pool, snaps)
+
+
+def test_chunked_matches_recurrent_path():
+    lens = [300, 77]
+    b = _case(lens, 4, 4, [[0, 2], [-1, 3]])
+    o1, p1, s1, _ = gpu_prefill(b, 64, algo=CH)
+    o2, p2, s2, _ = gpu_prefill(b, 64, algo=kda.KDA_ALGO_RECURRENT)
+    assert rel(o1, o2.float().cpu().numpy()) <= TOL["bf16"]
+    assert rel(s1, s2.cpu().numpy()) <= TOL["bf16"]
+    assert rel(p1[2:4], p2[2:4].cpu().numpy()) <= TOL["bf16"]
+
+
+def test_chunked_snapshot_equals_prefix_final_state():
+    """Snapshot j is bit-identical to the final state of a prefill of the
+    first (j+1)*interval tokens (same kernel path, same chunking)."""
+    L, I = 320, 64
+    b = _case([L], 2, 2, [[-1, 0]])
+    _, _, snaps, _ = gpu_prefill(b, I, algo=CH)
+    for j in range(L // I):
+        n = (j + 1) * I
+        bj = inputs.Batch(q=b.q[:n], k=b.k[:n], v=b.v[:n], g=b.g[:n], beta=b.beta[:n],
+                          cu_seqlens=torch.tensor([0, n], dtype=torch.int32),
+                          init_slots=b.init_slots, pool=b.pool)
+        _, pj, _, _ = gpu_prefill(bj, 0, algo=CH)
+        assert torch.equal(snaps[j].cpu(), pj[0].cpu()), f"snapshot {j}"
+
+
+def test_chunked_resume_chain_is_exact_on_chunk_boundaries():
+    """prefill(L1) -> slot, then prefill(L2) from that slot equals prefill(L1+L2)
+    bit for bit when L1 is a multiple of the chunk (the state round-trips
+    through the fp32 pool exactly)."""
+    L1, L2 = 128, 100
+    b = _case([L1 + L2], 2, 3, [[-1, 0]])
+    o_all, p_all, _, _ = gpu_prefill(b, 0, algo=CH)
+    b1 = inputs.Batch(q=b.q[:L1], k=b.k[:L1], v=b.v[:L1], g=b.g[:L1], beta=b.beta[:L1],
+                      cu_seqlens=torch.tensor([0, L1], dtype=torch.int32),
+                      init_slots=torch.tensor([[-1, 1]], dtype=torch.int32), pool=b.pool)
+    o1, p1, _, _ = gpu_prefill(b1, 0, algo=CH)
+    b2 = inputs.Batch(q=b.q[L1:], k=b.k[L1:], v=b.v[L1:], g=b.g[L1:], beta=b.beta[L1:],
+                      cu_seqlens=torch.tensor([0, L2], dtype=torch.int32),
+                      init_slots=torch.tensor([[1, 2]], dtype=torch.int32),
+                      pool=p1.cpu())
+    o2, p2, _, _ = gpu_prefill(b2, 0, algo=CH)
+    assert torch.equal(torch.cat([o1, o2]).cpu(), o_all.cpu())
+    assert torch.equal(p2[2].cpu(), p_all[0].cpu())
+
+
+def test_chunked_deterministic():
+    b = _case([500, 64], 3, 4, [[2, 0], [-1, 1]])
+    o1, p1, s1, _ = gpu_prefill(b, 64, algo=CH)
+    o2, p2, s2, _ = gpu_prefill(b, 64, algo=CH)
+    assert torch.equal(o1.cpu(), o2.cpu()) and torch.equal(p1.cpu(), p2.cpu())
+    assert torch.equal(s1.cpu(), s2.cpu())
+
+
+def test_auto_selects_chunked_for_bf16_128():
+    b = _case([100], 2, 1, [[-1, 0]])
+    o_auto, _, _, _ = gpu_prefill(b, 0)
+    o_ch, _, _, _ = gpu_prefill(b, 0, algo=CH)
+    assert torch.equal(o_auto.cpu(), o_ch.cpu())
+
+
+# ------------------------------------------------------------ full-size workloads
+
+def test_prefill_8k_full():
+    """B=1, T=8192, H=32, dk=dv=128, snapshots every 1024: every output, the
+    8 snapshots and the final state against the oracle (all heads)."""
+    w = inputs.WORKLOADS["prefill_8k"]
+    b = inputs.make_batch(w)
+    out, pool, snaps, (st, bits) = gpu_prefill(b, w.snap_interval)
+    assert st == kda.KDA_OK and bits == 0
+    assert snaps.shape[0] == 8
+    e_out, e_state = _check(b, w.snap_interval, out, pool, snaps)
+    print(f"prefill_8k: out {e_out:.2e} state {e_state:.2e}")
+
+
+def test_varlen_resume_full_sampled():
+    """16 sequences, L ~ U[512, 32768], 8 resumed from a 1024-slot pool, snapshots
+    every 256: the run is full size; the oracle recomputes a sample of
+    (sequence, head) pairs -- the longest, the shortest and two resumed ones --
+    exactly (each unit is independent)."""
+    w = inputs.WORKLOADS["varlen_resume"]
+    b = inputs.make_batch(w)
+    before = b.pool.clone()
+    out, pool, snaps, (st, bits) = gpu_prefill(b, w.snap_interval)
+    assert st == kda.KDA_OK and bits == 0
+    lens = (b.cu_seqlens[1:] - b.cu_seqlens[:-1]).tolist()
+    resumed = [i for i in range(w.B) if int(b.init_slots[i, 0]) >= 0]
+    seqs = sorted({int(np.argmax(lens)), int(np.argmin(lens)), resumed[0], resumed[-1]})
+    cu = b.cu_seqlens.numpy()
+    off, _ = oracle.snapshot_offsets(cu, w.snap_interval)
+    for s in seqs:
+        for h in (0, 17):
+            t0, t1 = int(cu[s]), int(cu[s + 1])
+            sub = {n: getattr(b, n)[t0:t1, h:h + 1] for n in ("q", "k", "v", "g", "beta")}
+            src, dst = int(b.init_slots[s, 0]), int(b.init_slots[s, 1])
+            init = None if src < 0 else b.pool[src, h][None, None]
+            res = oracle.run(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], [0, t1 - t0],
+                             init, w.snap_interval)
+            assert oracle.rel_l2(out[t0:t1, h].float().cpu().numpy(), res.out[:, 0]) \
+                <= TOL["bf16"], (s, h)
+            assert oracle.rel_l2(pool[dst, h].cpu().numpy(), res.final[0, 0]) <= TOL["bf16"]
+            n = lens[s] // w.snap_interval
+            sn = snaps[off[s]:off[s] + n, h].cpu().numpy()
+            assert oracle.rel_l2(sn, res.snaps[:, 0]) <= TOL["bf16"], (s, h)
+    assert_untouched(pool, before, touched_slots(b))
+    for s in resumed:
+        src = int(b.init_slots[s, 0])
+        assert torch.equal(pool[src].cpu(), before[src])
+
+
+@pytest.mark.slow
+def test_prefill_1m_full_sampled():
+    """B=1, T=2^20, H=16, snapshots every 32768 (inputs drawn on the GPU): the
+    oracle recomputes head 5, state columns 32..47, over all 2^20 tokens --
+    outputs, all 32 snapshots and the final state of those columns."""
+    w = inputs.WORKLOADS["prefill_1m"]
+    b = inputs.make_batch(w, device="cuda")
+    out, pool, snaps, (st, bits) = gpu_prefill(b, w.snap_interval)
+    assert st == kda.KDA_OK and bits == 0
+    assert snaps.shape[0] == 32
+    h, lo, hi = 5, 32, 48
+    sub = {n: getattr(b, n)[:, h:h + 1].cpu() for n in ("q", "k", "v", "g", "beta")}
+    res = oracle.run(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], [0, w.T], None,
+                     w.snap_interval, cols=(lo, hi))
+    assert oracle.rel_l2(out[:, h, lo:hi].float().cpu().numpy(), res.out[:, 0, lo:hi]) <= TOL["bf16"]
+    assert oracle.rel_l2(snaps[:, h, :, lo:hi].cpu().numpy(), res.snaps[:, 0, :, lo:hi]) <= TOL["bf16"]
+    assert oracle.rel_l2(pool[0, h, :, lo:hi].cpu().numpy(), res.final[0, 0, :, lo:hi]) <= TOL["bf16"]
