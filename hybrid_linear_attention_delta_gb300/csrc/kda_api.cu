@@ -73,8 +73,12 @@ kda_status kda_prefill_varlen(const void *q, const void *k, const void *v, const
   g_last_launches = 0;
   kda_status st = check_common(a);
   if (st != KDA_OK) return st;
-  if (snap_interval < 0 || (snap_interval > 0) != (snaps != nullptr)) return KDA_ERR_INVALID_ARG;
-  if (snaps && (!aligned16(snaps) || a->snaps_capacity < 0)) return KDA_ERR_INVALID_ARG;
+  // snaps may be NULL with an interval only when its capacity is 0 (a batch
+  // whose sequences are all shorter than the interval)
+  if (snap_interval < 0 || a->snaps_capacity < 0) return KDA_ERR_INVALID_ARG;
+  if (snap_interval == 0 && snaps) return KDA_ERR_INVALID_ARG;
+  if (snap_interval > 0 && !snaps && a->snaps_capacity > 0) return KDA_ERR_INVALID_ARG;
+  if (snaps && !aligned16(snaps)) return KDA_ERR_INVALID_ARG;
   if (a->algo < KDA_ALGO_AUTO || a->algo > KDA_ALGO_CHUNKED) return KDA_ERR_INVALID_ARG;
   if (a->B == 0) return a->T_total == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
   if (!cu_seqlens || !init_slots || !state_pool || !aligned16(state_pool))

@@ -116,7 +116,8 @@ typedef struct {
  *                                            tokens of this segment (segment-relative)
  * snaps      [n_snaps][H][dk][dv] fp32       snapshots, sequence-major then position:
  *                                            sequence b's start at the exclusive scan of
- *                                            floor(L_b / interval); NULL iff interval == 0;
+ *                                            floor(L_b / interval); NULL when interval == 0
+ *                                            (or when a->snaps_capacity == 0);
  *                                            n_snaps = kda_snapshot_count(...)
  *                                            <= a->snaps_capacity
  * Callers align segment starts to the interval (a scheduler invariant) so that

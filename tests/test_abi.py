@@ -85,8 +85,8 @@ def test_host_visible_errors_return_without_launch(lib):
     st = lib.kda_prefill_varlen(fake, fake, fake, fake, fake, fake, fake, fake, fake, 0, None,
                                 ctypes.byref(a))
     assert st == kda.KDA_ERR_INVALID_ARG
-    # snap interval without a snapshot buffer
-    a = _args(workspace=V(1 << 20), workspace_bytes=1 << 20)
+    # snap interval with a nonzero capacity but no snapshot buffer
+    a = _args(workspace=V(1 << 20), workspace_bytes=1 << 20, snaps_capacity=5)
     st = lib.kda_prefill_varlen(fake, fake, fake, fake, fake, fake, fake, fake, fake, 64, None,
                                 ctypes.byref(a))
     assert st == kda.KDA_ERR_INVALID_ARG
