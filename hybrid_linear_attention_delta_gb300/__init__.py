@@ -69,6 +69,8 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_last_launch_count.argtypes = []
         L.kda_last_launch_count.restype = I32
+        L.kda_decode_noalloc.argtypes = [V, V, V, V, V, V, V, V, I32, V, V, A]
+        L.kda_decode_noalloc.restype = ctypes.c_int
         if path:
             return L
         _lib = L
@@ -168,6 +170,22 @@ def kda_decode(q, k, v, g, beta, slot_ids, state_pool, out, n_tok: int = 1,
                           ctypes.byref(a))
     if st != KDA_OK:
         raise KdaError(st, "kda_decode")
+
+
+def kda_decode_noalloc(q, k, v, g, beta, slot_ids, state_pool, out, n_tok: int = 1,
+                       per_tok_states=None, err_bits=None, *, stream=None) -> None:
+    """kda_decode for dk = dv = 128 without a workspace: for callers that may
+    not allocate device memory (see kda_decode_noalloc in include/kda.h).
+    err_bits: optional int32/uint32 CUDA tensor of one element that collects
+    the device-side check bits."""
+    a = make_args(B=slot_ids.numel(), T_total=q.shape[0], H=q.shape[1], dk=q.shape[2],
+                  dv=v.shape[2], n_slots=state_pool.shape[0], dtype=_dtype_code(q),
+                  stream=stream)
+    st = lib().kda_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                  _ptr(slot_ids), _ptr(state_pool), _ptr(out), int(n_tok),
+                                  _ptr(per_tok_states), _ptr(err_bits), ctypes.byref(a))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_noalloc")
 
 
 def kda_device_status(workspace, stream=None):

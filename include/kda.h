@@ -149,6 +149,39 @@ kda_status kda_decode(const void *q, const void *k, const void *v, const void *g
                       const void *beta, const int32_t *slot_ids, float *state_pool, void *out,
                       int32_t n_tok, float *per_tok_states, const kda_args *a);
 
+/*
+ * kda_decode without a workspace, for callers that may not allocate device
+ * memory: code inside a framework that owns every device buffer through its
+ * own pool and hands a plugin only the step's tensors, or code on a latency
+ * path where cudaMalloc is not allowed because it can synchronise the whole
+ * device.  (The pages describe no such entry point; it exists for those
+ * callers only.)
+ *
+ * Same arguments and results as kda_decode, restricted to dk = dv = 128;
+ * a->workspace and a->workspace_bytes are ignored.  The scratch the decode
+ * kernel needs (its duplicate-slot claim table) is a fixed array inside
+ * libkda.so: every GPU that loads the library holds it (2 MiB + 256 bytes)
+ * until the process exits, and it covers n_slots * H <= 131072 states; larger
+ * pools are refused with KDA_ERR_INVALID_ARG before anything is launched.
+ * This call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine).
+ *
+ * err_bits: NULL, or a caller-owned device uint32 that the kernel ORs the
+ * device-side check bits into (same bits as kda_device_status reports); the
+ * caller clears it.
+ *
+ * The first call on each device looks up the array's device address on the
+ * current device (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  Every call shares the one array and leaves its contents
+ * behind (claims are stamped per call, so nothing needs clearing); calls that
+ * overlap on the GPU race on it and may miss a duplicate slot, so order them
+ * on one stream.
+ */
+kda_status kda_decode_noalloc(const void *q, const void *k, const void *v, const void *g,
+                              const void *beta, const int32_t *slot_ids, float *state_pool,
+                              void *out, int32_t n_tok, float *per_tok_states, uint32_t *err_bits,
+                              const kda_args *a);
+
 /* Workspace bytes the calls need for these sizes (uses B, H, n_slots). */
 size_t kda_workspace_bytes(const kda_args *a);
 
