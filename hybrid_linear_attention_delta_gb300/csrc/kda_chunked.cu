@@ -29,7 +29,7 @@
 //   MMA1  [K+; Q+] K-^T                 M=128 N=64  K=128  -> A, Q+K-^T (TMEM)
 //   solve T = (I + A)^{-1} Diag(beta)    fp32, 16x16 blocks, CUDA cores
 //   MMA2  [T; M] K+ and [T; M] V        -> W, U~ (TMEM)
-//   MMA3  U~ -= W S0'  ;  O = Q+ S0'
+//   MMA3  U~ -= W S0'  (O = Q+ S0' was issued before the solve)
 //   MMA4  K_end^T U    ;  O += M U
 //   out   o rows -> global bf16; S = Diag(e^{G_C}) S + K_end^T U (registers),
 //         snapshot / final state -> global fp32
@@ -67,9 +67,15 @@ struct Layout {
   static constexpr uint32_t kBars = 0;                 // tma[2], mma
   static constexpr uint32_t kSlot = 24;                // TMEM base address
   static constexpr uint32_t kBeta = 64;                // f32[64]
-  static constexpr uint32_t kEgc = kBeta + 256;        // f32[128] e^{G_C}
-  static constexpr uint32_t kPart = kEgc + 512;        // f32[2][128] half-chunk decay sums
-  static constexpr uint32_t kBytes = kMisc + kPart + 1024;
+  static constexpr uint32_t kTot = kBeta + 256;        // f32[128] G_C (chunk decay)
+  static constexpr uint32_t kAnc = kTot + 512;         // f32[128] a (anchor decay)
+  static constexpr uint32_t kBytes = kMisc + kAnc + 512;
+  // prep scratch: per 4-row group decay sums f32[16][128], inside the W buffer
+  static constexpr uint32_t kGpart = kW;
+  // solve scratch (fp32, swizzled 64x64): L in the W buffer, X^T in the U
+  // buffer, diagonal blocks of X and Y^T in the g slot (K- is dead by then)
+  static constexpr uint32_t kXd = kG;                   // f32[4][16][16] (stage-relative)
+  static constexpr uint32_t kYt = kG + 4096;            // f32[3][16][20]
   static_assert(kStage % 1024 == 0, "stage alignment");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
@@ -93,57 +99,86 @@ __device__ __forceinline__ bool cta_wait(uint32_t bar, uint32_t parity) {
   return !__syncthreads_or(!ok);
 }
 
-__device__ __forceinline__ float bf(const uint8_t *base, uint32_t off) {
-  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(base + off));
-}
 __device__ __forceinline__ void st_bf(uint8_t *base, uint32_t off, float x) {
   *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(x);
 }
 
-// Fp32 64x64 unit-lower-triangular system L = I + A with A stored rotated
-// (element (r, i) at r*64 + ((i + r) & 63), conflict-free row writes).
-__device__ __forceinline__ float Lrot(const float *L, int r, int i) {
-  return L[r * 64 + ((i + r) & 63)];
+// 64x64 fp32 matrices in shared memory: row r holds 16 float4 chunks, chunk c
+// stored at position c ^ (r & 15).  A warp writing one row per lane, or
+// reading the same chunk of 16 different rows, touches distinct banks, and any
+// 4 aligned consecutive entries of a row are one float4.
+__device__ __forceinline__ int fidx(int r, int i) {
+  return r * 64 + ((((i >> 2) ^ (r & 15)) << 2) | (i & 3));
+}
+__device__ __forceinline__ float4 ld4(const float *M, int r, int i) {
+  return *reinterpret_cast<const float4 *>(M + fidx(r, i));
+}
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
+  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
 }
 
-// X = (I + A)^{-1} by 16x16 blocks: diagonal blocks by forward substitution,
-// then the three bands below the diagonal, X_ab = -X_aa sum_{b<=c<a} A_ac X_cb.
-__device__ __forceinline__ void solve_unit_lower(const float *L, float *X, float *Y, int tid) {
-  if (tid < 64) {
-    const int base = (tid >> 4) * 16, jj = tid & 15;
-    float x[16];
+// T = (I + A)^{-1} Diag(beta) for the 64x64 strictly lower A held in L
+// (fidx layout, fp32, zero on and above the diagonal).  X = (I + A)^{-1} is
+// built by 16x16 blocks:
+//  * the four diagonal blocks X_aa by forward substitution, column by column;
+//    four lanes share a column, each owning four consecutive rows, and
+//    combine the partial sums of a step with two shuffles;
+//  * the blocks below the diagonal level by level (a - b = 1, 2, 3):
+//        Y_b = sum_{b<=c<a} A_ac X_cb ,   X_ab = -X_aa Y_b ,
+//    one output element per thread and pass, each a 16-term float4 dot
+//    product per block (A rows from L, X columns from X^T, X_aa rows from
+//    Xd, Y columns from Y^T).
+// T is written as bf16 into rows 0..63 of the K-major [T; M] operand; its
+// blocks above the diagonal stay zero from the start of the kernel.
+__device__ __forceinline__ void solve_T(const float *L, float *XT, float *Xd, float *YT,
+                                        const float *beta, uint8_t *tm, int tid) {
+  {
+    const int p = tid >> 2, sub = tid & 3, a = p >> 4, jj = p & 15, base = 16 * a;
+    float xo[4];  // x[4 sub + t] of column jj of X_aa
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float acc = (r == jj) ? 1.f : 0.f;
+    for (int t = 0; t < 4; ++t) xo[t] = (4 * sub + t == jj) ? 1.f : 0.f;
 #pragma unroll
-      for (int i = 0; i < r; ++i) acc = fmaf(-Lrot(L, base + r, base + i), x[i], acc);
-      x[r] = acc;
+    for (int r = 1; r < 16; ++r) {
+      // L is zero on and above the diagonal, so rows i >= r contribute nothing
+      float part = dot4(ld4(L, base + r, base + 4 * sub), make_float4(xo[0], xo[1], xo[2], xo[3]),
+                        0.f);
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      if (sub == (r >> 2) && r > jj) xo[r & 3] = -part;
     }
+    *reinterpret_cast<float4 *>(XT + fidx(base + jj, base + 4 * sub)) =
+        make_float4(xo[0], xo[1], xo[2], xo[3]);
+    const float bj = beta[base + jj];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) X[(base + r) * 64 + base + jj] = x[r];
+    for (int t = 0; t < 4; ++t) {
+      Xd[a * 256 + (4 * sub + t) * 16 + jj] = xo[t];
+      st_bf(tm, sw128_offset(base + 4 * sub + t, base + jj), xo[t] * bj);
+    }
   }
   __syncthreads();
 #pragma unroll 1
   for (int d = 1; d < 4; ++d) {
-    const int nblk = 4 - d;
-    for (int e = tid; e < nblk * 256; e += kThreads) {
-      const int b = e >> 8, r = (e >> 4) & 15, j = e & 15, a = b + d;
+    const int nout = (4 - d) * 256;
+    for (int e = tid; e < nout; e += kThreads) {  // Y_b[k][j] -> Y^T
+      const int b = e >> 8, k = (e >> 4) & 15, j = e & 15, a = b + d;
       float acc = 0.f;
       for (int c = b; c < a; ++c) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-          acc = fmaf(Lrot(L, 16 * a + r, 16 * c + k), X[(16 * c + k) * 64 + 16 * b + j], acc);
+        for (int q = 0; q < 4; ++q)
+          acc = dot4(ld4(L, 16 * a + k, 16 * c + 4 * q), ld4(XT, 16 * b + j, 16 * c + 4 * q), acc);
       }
-      Y[e] = acc;
+      YT[b * 320 + j * 20 + k] = acc;
     }
     __syncthreads();
-    for (int e = tid; e < nblk * 256; e += kThreads) {
+    for (int e = tid; e < nout; e += kThreads) {  // X_ab[r][j] = -sum_k X_aa[r][k] Y_b[k][j]
       const int b = e >> 8, r = (e >> 4) & 15, j = e & 15, a = b + d;
+      const float4 *xr = reinterpret_cast<const float4 *>(Xd + a * 256 + r * 16);
+      const float4 *yc = reinterpret_cast<const float4 *>(YT + b * 320 + j * 20);
       float acc = 0.f;
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        acc = fmaf(X[(16 * a + r) * 64 + 16 * a + k], Y[b * 256 + k * 16 + j], acc);
-      X[(16 * a + r) * 64 + 16 * b + j] = -acc;
+      for (int q = 0; q < 4; ++q) acc = dot4(xr[q], yc[q], acc);
+      XT[fidx(16 * b + j, 16 * a + r)] = -acc;
+      st_bf(tm, sw128_offset(16 * a + r, 16 * b + j), -acc * beta[16 * b + j]);
     }
     __syncthreads();
   }
@@ -178,8 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_tma0 = sbase + Ly::kMisc + Ly::kBars;
   const uint32_t bar_mma = bar_tma0 + 16;
   float *s_beta = reinterpret_cast<float *>(misc + Ly::kBeta);
-  float *s_egc = reinterpret_cast<float *>(misc + Ly::kEgc);
-  float *s_part = reinterpret_cast<float *>(misc + Ly::kPart);
+  float *s_tot = reinterpret_cast<float *>(misc + Ly::kTot);
+  float *s_anc = reinterpret_cast<float *>(misc + Ly::kAnc);
+  float *s_gpart = reinterpret_cast<float *>(smem + Ly::kGpart);
 
   if (tid == 0) {
     mbar_init(bar_tma0, 1);
@@ -192,6 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_g);
   }
   if (warp == 0) tmem_alloc(sbase + Ly::kMisc + Ly::kSlot, kTmemCols);
+  // [T; M] starts at zero: the blocks of T above its diagonal are never written
+  for (int e = tid; e < 16384 / 16; e += kThreads) st_shared_v4(sbase + Ly::kTM + 16 * e, 0, 0, 0, 0);
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc + Ly::kSlot);
@@ -257,23 +295,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t0 = m.tok0 + n * kC;
     const int cl = min(kC, m.len - n * kC);
 
-    if (n + 1 < nchunks) {
+    if (!cta_wait(bar_tma0 + 8 * st, (n >> 1) & 1)) { aborted = true; break; }
+    tma_pending[st] = false;
+    if (n + 1 < nchunks) {  // the other stage was released at the end of chunk n-1
       if (tid == 0) issue_tma(n + 1);
       tma_pending[(n + 1) & 1] = true;
       tma_parity[(n + 1) & 1] = ((n + 1) >> 1) & 1;
     }
-    if (!cta_wait(bar_tma0 + 8 * st, (n >> 1) & 1)) { aborted = true; break; }
-    tma_pending[st] = false;
 
     // ------------------------------------------------------------ prep
-    const int ch = tid & 127, hf = tid >> 7;
-    const uint32_t kq_half = (ch >> 6) * 16384, g_half = (ch >> 6) * 8192;
-    const int cc = ch & 63;
+    // thread: channels [8 cq, 8 cq + 8) x rows [4 rg, 4 rg + 4), 16-byte accesses
+    const int cq = tid & 15, rg = tid >> 4;
+    const uint32_t okq = (cq >> 3) * 16384, og = Ly::kG + (cq >> 3) * 8192;
+    const uint32_t oke = Ly::kKE + (cq >> 3) * 8192;
+    float gl[4][8];  // in-group inclusive cumulative decay
     {
-      float s = 0.f;
-      for (int r = 32 * hf; r < 32 * hf + 32 && r < cl; ++r)
-        s += bf(stage, Ly::kG + g_half + sw128_offset(r, cc));
-      s_part[hf * 128 + ch] = s;
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int r = 4 * rg + rr;
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (r < cl) w = ld_shared_v4(sb + og + sw128_chunk(r, cq & 7));
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          gl[rr][2 * j] = (rr ? gl[rr - 1][2 * j] : 0.f) + bf16lo(wv[j]);
+          gl[rr][2 * j + 1] = (rr ? gl[rr - 1][2 * j + 1] : 0.f) + bf16hi(wv[j]);
+        }
+      }
+      float4 *gp = reinterpret_cast<float4 *>(s_gpart + rg * 128 + 8 * cq);
+      gp[0] = make_float4(gl[3][0], gl[3][1], gl[3][2], gl[3][3]);
+      gp[1] = make_float4(gl[3][4], gl[3][5], gl[3][6], gl[3][7]);
       if (tid < 64)
         s_beta[tid] = tid < cl ? __bfloat162float(a.beta[(int64_t)(t0 + tid) * H + h]) : 0.f;
       if (cl < kC) {  // ragged tail: zero the v rows past the sequence end
@@ -284,44 +335,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncthreads();
-    {
-      const float p0 = s_part[ch], p1 = s_part[128 + ch];
-      const float cke = expf(p1);  // e^{G_C - a}
-      if (hf == 0) s_egc[ch] = expf(p0 + p1);
-      float x = 0.f;
-      for (int it = 0; it < 32; ++it) {
-        const int r = hf ? 32 + it : 31 - it;
-        const uint32_t okq = kq_half + sw128_offset(r, cc);
-        const uint32_t og = Ly::kG + g_half + sw128_offset(r, cc);
-        const uint32_t oke = Ly::kKE + g_half + sw128_offset(r, cc);
-        float gr = 0.f;
-        if (r < cl) gr = bf(stage, og);
-        if (hf) x += gr;  // x = G_r - a
-        if (r < cl) {
-          const float kv = bf(stage, okq), qv = bf(stage, Ly::kQ + okq);
-          const float e1 = __expf(x), e2 = __expf(-x);
-          st_bf(stage, okq, kv * e1);
-          st_bf(stage, Ly::kQ + okq, qv * e1);
-          st_bf(stage, og, kv * e2);
-          st_bf(smem, oke, kv * e2 * cke);
-        } else {
-          st_bf(stage, okq, 0.f);
-          st_bf(stage, Ly::kQ + okq, 0.f);
-          st_bf(stage, og, 0.f);
-          st_bf(smem, oke, 0.f);
-        }
-        if (!hf) x -= gr;
-      }
-      // S0' = Diag(e^{a}) S as the bf16 operand (MN-major: row = channel c)
-      const float ea = expf(s_part[c]);
+    if (tid < 128) {  // per channel: exclusive prefix over the 16 row groups (in place)
+      float run = 0.f;
 #pragma unroll
-      for (int j = 0; j < NH / 8; ++j) {
-        const int col = col0 + 8 * j;
-        st_shared_v4(sbase + Ly::kS0 + (col >> 6) * 16384 + sw128_chunk(c, (col & 63) >> 3),
-                     pack_bf16x2(ea * S[8 * j], ea * S[8 * j + 1]),
-                     pack_bf16x2(ea * S[8 * j + 2], ea * S[8 * j + 3]),
-                     pack_bf16x2(ea * S[8 * j + 4], ea * S[8 * j + 5]),
-                     pack_bf16x2(ea * S[8 * j + 6], ea * S[8 * j + 7]));
+      for (int g2 = 0; g2 < 16; ++g2) {
+        const float p = s_gpart[g2 * 128 + tid];
+        s_gpart[g2 * 128 + tid] = run;
+        run += p;
+        if (g2 == 7) s_anc[tid] = run;  // a: decay through row 31
+      }
+      s_tot[tid] = run;                  // G_C: decay through the chunk
+    }
+    __syncthreads();
+    {
+      float pre[8], anc[8], tot[8];
+      {
+        const float4 *pp = reinterpret_cast<const float4 *>(s_gpart + rg * 128 + 8 * cq);
+        const float4 *pa = reinterpret_cast<const float4 *>(s_anc + 8 * cq);
+        const float4 *pt = reinterpret_cast<const float4 *>(s_tot + 8 * cq);
+        const float4 p0 = pp[0], p1 = pp[1], a0 = pa[0], a1 = pa[1], t0v = pt[0], t1v = pt[1];
+        pre[0] = p0.x; pre[1] = p0.y; pre[2] = p0.z; pre[3] = p0.w;
+        pre[4] = p1.x; pre[5] = p1.y; pre[6] = p1.z; pre[7] = p1.w;
+        anc[0] = a0.x; anc[1] = a0.y; anc[2] = a0.z; anc[3] = a0.w;
+        anc[4] = a1.x; anc[5] = a1.y; anc[6] = a1.z; anc[7] = a1.w;
+        tot[0] = t0v.x; tot[1] = t0v.y; tot[2] = t0v.z; tot[3] = t0v.w;
+        tot[4] = t1v.x; tot[5] = t1v.y; tot[6] = t1v.z; tot[7] = t1v.w;
+      }
+      float cke[8];  // e^{G_C - a}
+#pragma unroll
+      for (int j = 0; j < 8; ++j) cke[j] = __expf(tot[j] - anc[j]);
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int r = 4 * rg + rr;
+        const uint32_t ck = sw128_chunk(r, cq & 7);
+        uint32_t kp[4] = {0, 0, 0, 0}, qp[4] = {0, 0, 0, 0}, km[4] = {0, 0, 0, 0},
+                 ke[4] = {0, 0, 0, 0};
+        if (r < cl) {
+          const uint4 kw = ld_shared_v4(sb + okq + ck);
+          const uint4 qw = ld_shared_v4(sb + Ly::kQ + okq + ck);
+          const uint32_t kv[4] = {kw.x, kw.y, kw.z, kw.w}, qv[4] = {qw.x, qw.y, qw.z, qw.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float x0 = pre[2 * j] + gl[rr][2 * j] - anc[2 * j];  // G_r - a
+            const float x1 = pre[2 * j + 1] + gl[rr][2 * j + 1] - anc[2 * j + 1];
+            const float e0 = __expf(x0), e1 = __expf(x1);
+            const float f0 = __expf(-x0), f1 = __expf(-x1);
+            const float k0 = bf16lo(kv[j]), k1 = bf16hi(kv[j]);
+            const float q0 = bf16lo(qv[j]), q1 = bf16hi(qv[j]);
+            kp[j] = pack_bf16x2(k0 * e0, k1 * e1);
+            qp[j] = pack_bf16x2(q0 * e0, q1 * e1);
+            km[j] = pack_bf16x2(k0 * f0, k1 * f1);
+            ke[j] = pack_bf16x2(k0 * f0 * cke[2 * j], k1 * f1 * cke[2 * j + 1]);
+          }
+        }
+        st_shared_v4(sb + okq + ck, kp[0], kp[1], kp[2], kp[3]);
+        st_shared_v4(sb + Ly::kQ + okq + ck, qp[0], qp[1], qp[2], qp[3]);
+        st_shared_v4(sb + og + ck, km[0], km[1], km[2], km[3]);
+        st_shared_v4(sbase + oke + ck, ke[0], ke[1], ke[2], ke[3]);
       }
     }
     fence_async_smem();
@@ -339,6 +409,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(bar_mma);
     }
     mma_pending = true;
+    {  // S0' = Diag(e^{a}) S as the bf16 operand (MN-major: row = channel c), under MMA1
+      const float ea = expf(s_anc[c]);
+#pragma unroll
+      for (int j = 0; j < NH / 8; ++j) {
+        const int col = col0 + 8 * j;
+        st_shared_v4(sbase + Ly::kS0 + (col >> 6) * 16384 + sw128_chunk(c, (col & 63) >> 3),
+                     pack_bf16x2(ea * S[8 * j], ea * S[8 * j + 1]),
+                     pack_bf16x2(ea * S[8 * j + 2], ea * S[8 * j + 3]),
+                     pack_bf16x2(ea * S[8 * j + 4], ea * S[8 * j + 5]),
+                     pack_bf16x2(ea * S[8 * j + 6], ea * S[8 * j + 7]));
+      }
+      fence_async_smem();
+    }
     if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
     mma_phase ^= 1;
     mma_pending = false;
@@ -346,18 +429,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // A (rows 0..63) into the fp32 system; M (rows 64..127) into [T; M]
     float *Lm = reinterpret_cast<float *>(smem + Ly::kW);
-    float *Xm = reinterpret_cast<float *>(smem + Ly::kU);
-    float *Ym = reinterpret_cast<float *>(stage + Ly::kG);
     {
       float v[32];
       tmem_ld32(lane_base + 256 + colhalf * 32, v);
       const int rr = quarter * 32 + lane;
-      if (quarter < 2) {
+      if (quarter < 2) {  // L = Diag(beta) strict_lower(K+ K-^T), zero elsewhere
         const float br = s_beta[rr];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int i = colhalf * 32 + j;
-          Lm[rr * 64 + ((i + rr) & 63)] = (i < rr) ? br * v[j] : 0.f;
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const int i = colhalf * 32 + q4 * 4;
+          *reinterpret_cast<float4 *>(Lm + fidx(rr, i)) =
+              make_float4(i < rr ? br * v[q4 * 4] : 0.f, i + 1 < rr ? br * v[q4 * 4 + 1] : 0.f,
+                          i + 2 < rr ? br * v[q4 * 4 + 2] : 0.f,
+                          i + 3 < rr ? br * v[q4 * 4 + 3] : 0.f);
         }
       } else {
         const int r = rr - 64;
@@ -378,23 +462,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
 
-    // ------------------------------------------------------------ solve
-    solve_unit_lower(Lm, Xm, Ym, tid);
-    {
-      const int r = tid >> 2, q4 = tid & 3;
+    // O = Q+ S0' runs on the tensor cores while the CUDA cores solve for T
+    // (the commit after MMA2 covers it)
+    if (tid == 0) {
+      tc_fence_after();
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float t8[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int col = q4 * 16 + half * 8 + j;
-          t8[j] = (col <= r) ? Xm[r * 64 + col] * s_beta[col] : 0.f;
-        }
-        st_shared_v4(sbase + Ly::kTM + sw128_chunk(r, q4 * 2 + half), pack_bf16x2(t8[0], t8[1]),
-                     pack_bf16x2(t8[2], t8[3]), pack_bf16x2(t8[4], t8[5]),
-                     pack_bf16x2(t8[6], t8[7]));
-      }
+      for (int kk = 0; kk < 8; ++kk)
+        mma_bf16(tmem + 384,
+                 sw128_desc(sb + Ly::kQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                 sw128_desc(sbase + Ly::kS0 + kk * 2048, 16384, 1024), idesc_v, kk > 0);
     }
+
+    // ------------------------------------------------------------ solve
+    solve_T(Lm, reinterpret_cast<float *>(smem + Ly::kU),
+            reinterpret_cast<float *>(stage + Ly::kXd),
+            reinterpret_cast<float *>(stage + Ly::kYt), s_beta, smem + Ly::kTM, tid);
     fence_async_smem();
     __syncthreads();
 
@@ -442,9 +524,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t bd = sw128_desc(sbase + Ly::kS0 + kk * 2048, 16384, 1024);
         mma_bf16(tmem + 128, sw128_desc(sbase + Ly::kW + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
                  bd, idesc_vneg, 1);
-        mma_bf16(tmem + 384,
-                 sw128_desc(sb + Ly::kQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024), bd,
-                 idesc_v, kk > 0);
       }
       mma_commit(bar_mma);
     }
@@ -514,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     {
-      const float egc = s_egc[c];
+      const float egc = expf(s_tot[c]);
 #pragma unroll
       for (int p = 0; p < NH / 32; ++p) {
         float v[32];
