@@ -25,13 +25,14 @@
 // the block's columns).  Per chunk:
 //   TMA   q, k, v, g tiles (128-byte swizzled) into one of two stages
 //         (the next chunk's tiles load while this one computes)
-//   prep  cumulative decay per channel, K+, Q+, K- (in place), K_end, S0'
+//   prep  cumulative decay per channel, K+, Q+, K- (in place), S0'
 //   MMA1  [K+; Q+] K-^T                 M=128 N=64  K=128  -> A, Q+K-^T (TMEM)
 //   solve T = (I + A)^{-1} Diag(beta)    fp32, 16x16 blocks, CUDA cores
 //   MMA2  [T; M] K+ and [T; M] V        -> W, U~ (TMEM)
 //   MMA3  U~ -= W S0'  (O = Q+ S0' was issued before the solve)
-//   MMA4  K_end^T U    ;  O += M U
-//   out   o rows -> global bf16; S = Diag(e^{G_C}) S + K_end^T U (registers),
+//   MMA4  K-^T U       ;  O += M U
+//   out   o rows -> global bf16; S = Diag(e^{G_C}) S + Diag(e^{G_C - a}) K-^T U
+//         (= K_end^T U with K_end = K e^{G_C - G}) in registers;
 //         snapshot / final state -> global fp32
 // All MMAs are M = 128 (rows 64..127 of the 64-row operands are ignored).
 #include <cuda.h>
@@ -61,8 +62,8 @@ struct Layout {
   static constexpr uint32_t kTM = 2 * kStage;          // [T; M]: 128 rows x 64 tokens
   static constexpr uint32_t kW = kTM + 16384;          // W halves; fp32 L during the solve
   static constexpr uint32_t kU = kW + 16384;           // U halves; fp32 X during the solve
-  static constexpr uint32_t kKE = kU + 16384;          // K_end halves
-  static constexpr uint32_t kS0 = kKE + 16384;         // S0' halves (128 rows each)
+  static constexpr uint32_t kScr = kU + 16384;         // solve scratch (16 KiB)
+  static constexpr uint32_t kS0 = kScr + 16384;        // S0' halves (128 rows each)
   static constexpr uint32_t kMisc = kS0 + (DV / 64) * 16384;
   static constexpr uint32_t kBars = 0;                 // tma[2], mma
   static constexpr uint32_t kSlot = 24;                // TMEM base address
@@ -72,10 +73,10 @@ struct Layout {
   static constexpr uint32_t kBytes = kMisc + kAnc + 512;
   // prep scratch: per 4-row group decay sums f32[16][128], inside the W buffer
   static constexpr uint32_t kGpart = kW;
-  // solve scratch (fp32, swizzled 64x64): L in the W buffer, X^T in the U
-  // buffer, diagonal blocks of X and Y^T in the g slot (K- is dead by then)
-  static constexpr uint32_t kXd = kG;                   // f32[4][16][16] (stage-relative)
-  static constexpr uint32_t kYt = kG + 4096;            // f32[3][16][20]
+  // solve scratch (fp32): L (swizzled 64x64) in the W buffer, X^T in the U
+  // buffer, diagonal blocks of X and Y^T in kScr
+  static constexpr uint32_t kXd = kScr;                 // f32[4][16][16]
+  static constexpr uint32_t kYt = kScr + 4096;          // f32[3][16][20]
   static_assert(kStage % 1024 == 0, "stage alignment");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
@@ -117,6 +118,43 @@ __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
   return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
 }
 
+// One level of the block solve: the 4 - D blocks X_ab with a - b = D, from
+// the blocks of earlier levels.  Each thread owns 4 - D output elements (one
+// per block) and computes them side by side.
+template <int D>
+__device__ __forceinline__ void solve_level(const float *L, float *XT, const float *Xd, float *YT,
+                                            const float *beta, uint8_t *tm, int tid) {
+  constexpr int NB = 4 - D;
+  const int k = tid >> 4, j = tid & 15;  // row k (of Y) / r (of X), column j
+  float acc[NB][2];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {  // Y_b[k][j] = sum_{b<=c<b+D} A[16(b+D)+k][16c+.] X[16c+.][16b+j]
+    acc[b][0] = acc[b][1] = 0.f;
+#pragma unroll
+    for (int cc = 0; cc < D; ++cc) {
+      const int c = b + cc, ar = 16 * (b + D) + k, xr = 16 * b + j;
+      acc[b][0] = dot4(ld4(L, ar, 16 * c), ld4(XT, xr, 16 * c), acc[b][0]);
+      acc[b][1] = dot4(ld4(L, ar, 16 * c + 4), ld4(XT, xr, 16 * c + 4), acc[b][1]);
+      acc[b][0] = dot4(ld4(L, ar, 16 * c + 8), ld4(XT, xr, 16 * c + 8), acc[b][0]);
+      acc[b][1] = dot4(ld4(L, ar, 16 * c + 12), ld4(XT, xr, 16 * c + 12), acc[b][1]);
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < NB; ++b) YT[b * 320 + j * 20 + k] = acc[b][0] + acc[b][1];
+  __syncthreads();
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {  // X_ab[r][j] = -sum_k X_aa[r][k] Y_b[k][j]
+    const int a = b + D, r = k;
+    const float4 *xr = reinterpret_cast<const float4 *>(Xd + a * 256 + r * 16);
+    const float4 *yc = reinterpret_cast<const float4 *>(YT + b * 320 + j * 20);
+    const float v = -(dot4(xr[0], yc[0], dot4(xr[1], yc[1], 0.f)) +
+                      dot4(xr[2], yc[2], dot4(xr[3], yc[3], 0.f)));
+    XT[fidx(16 * b + j, 16 * a + r)] = v;
+    st_bf(tm, sw128_offset(16 * a + r, 16 * b + j), v * beta[16 * b + j]);
+  }
+  __syncthreads();
+}
+
 // T = (I + A)^{-1} Diag(beta) for the 64x64 strictly lower A held in L
 // (fidx layout, fp32, zero on and above the diagonal).  X = (I + A)^{-1} is
 // built by 16x16 blocks:
@@ -132,56 +170,36 @@ __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
 // blocks above the diagonal stay zero from the start of the kernel.
 __device__ __forceinline__ void solve_T(const float *L, float *XT, float *Xd, float *YT,
                                         const float *beta, uint8_t *tm, int tid) {
-  {
-    const int p = tid >> 2, sub = tid & 3, a = p >> 4, jj = p & 15, base = 16 * a;
-    float xo[4];  // x[4 sub + t] of column jj of X_aa
+  if (tid < 64) {  // one column of one diagonal block per thread
+    const int a = tid >> 4, jj = tid & 15, base = 16 * a;
+    float x[16];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) xo[t] = (4 * sub + t == jj) ? 1.f : 0.f;
+    for (int i = 0; i < 16; ++i) x[i] = (i == jj) ? 1.f : 0.f;
 #pragma unroll
     for (int r = 1; r < 16; ++r) {
-      // L is zero on and above the diagonal, so rows i >= r contribute nothing
-      float part = dot4(ld4(L, base + r, base + 4 * sub), make_float4(xo[0], xo[1], xo[2], xo[3]),
-                        0.f);
-      part += __shfl_xor_sync(0xffffffffu, part, 1);
-      part += __shfl_xor_sync(0xffffffffu, part, 2);
-      if (sub == (r >> 2) && r > jj) xo[r & 3] = -part;
+      // L is zero on and above the diagonal, so entries i >= r contribute nothing
+      const float p0 = dot4(ld4(L, base + r, base + 0), make_float4(x[0], x[1], x[2], x[3]), 0.f);
+      const float p1 = dot4(ld4(L, base + r, base + 4), make_float4(x[4], x[5], x[6], x[7]), 0.f);
+      const float p2 = dot4(ld4(L, base + r, base + 8), make_float4(x[8], x[9], x[10], x[11]), 0.f);
+      const float p3 =
+          dot4(ld4(L, base + r, base + 12), make_float4(x[12], x[13], x[14], x[15]), 0.f);
+      if (r > jj) x[r] = -((p0 + p1) + (p2 + p3));
     }
-    *reinterpret_cast<float4 *>(XT + fidx(base + jj, base + 4 * sub)) =
-        make_float4(xo[0], xo[1], xo[2], xo[3]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<float4 *>(XT + fidx(base + jj, base + 4 * q)) =
+          make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
     const float bj = beta[base + jj];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      Xd[a * 256 + (4 * sub + t) * 16 + jj] = xo[t];
-      st_bf(tm, sw128_offset(base + 4 * sub + t, base + jj), xo[t] * bj);
+    for (int i = 0; i < 16; ++i) {
+      Xd[a * 256 + i * 16 + jj] = x[i];
+      st_bf(tm, sw128_offset(base + i, base + jj), x[i] * bj);
     }
   }
   __syncthreads();
-#pragma unroll 1
-  for (int d = 1; d < 4; ++d) {
-    const int nout = (4 - d) * 256;
-    for (int e = tid; e < nout; e += kThreads) {  // Y_b[k][j] -> Y^T
-      const int b = e >> 8, k = (e >> 4) & 15, j = e & 15, a = b + d;
-      float acc = 0.f;
-      for (int c = b; c < a; ++c) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          acc = dot4(ld4(L, 16 * a + k, 16 * c + 4 * q), ld4(XT, 16 * b + j, 16 * c + 4 * q), acc);
-      }
-      YT[b * 320 + j * 20 + k] = acc;
-    }
-    __syncthreads();
-    for (int e = tid; e < nout; e += kThreads) {  // X_ab[r][j] = -sum_k X_aa[r][k] Y_b[k][j]
-      const int b = e >> 8, r = (e >> 4) & 15, j = e & 15, a = b + d;
-      const float4 *xr = reinterpret_cast<const float4 *>(Xd + a * 256 + r * 16);
-      const float4 *yc = reinterpret_cast<const float4 *>(YT + b * 320 + j * 20);
-      float acc = 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) acc = dot4(xr[q], yc[q], acc);
-      XT[fidx(16 * b + j, 16 * a + r)] = -acc;
-      st_bf(tm, sw128_offset(16 * a + r, 16 * b + j), -acc * beta[16 * b + j]);
-    }
-    __syncthreads();
-  }
+  solve_level<1>(L, XT, Xd, YT, beta, tm, tid);
+  solve_level<2>(L, XT, Xd, YT, beta, tm, tid);
+  solve_level<3>(L, XT, Xd, YT, beta, tm, tid);
 }
 
 template <int DV>
@@ -307,7 +325,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // thread: channels [8 cq, 8 cq + 8) x rows [4 rg, 4 rg + 4), 16-byte accesses
     const int cq = tid & 15, rg = tid >> 4;
     const uint32_t okq = (cq >> 3) * 16384, og = Ly::kG + (cq >> 3) * 8192;
-    const uint32_t oke = Ly::kKE + (cq >> 3) * 8192;
     float gl[4][8];  // in-group inclusive cumulative decay
     {
 #pragma unroll
@@ -361,23 +378,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tot[0] = t0v.x; tot[1] = t0v.y; tot[2] = t0v.z; tot[3] = t0v.w;
         tot[4] = t1v.x; tot[5] = t1v.y; tot[6] = t1v.z; tot[7] = t1v.w;
       }
-      float cke[8];  // e^{G_C - a}
 #pragma unroll
-      for (int j = 0; j < 8; ++j) cke[j] = __expf(tot[j] - anc[j]);
+      for (int j = 0; j < 8; ++j) pre[j] -= anc[j];  // G_r - a = pre + gl - a
 #pragma unroll
       for (int rr = 0; rr < 4; ++rr) {
         const int r = 4 * rg + rr;
         const uint32_t ck = sw128_chunk(r, cq & 7);
-        uint32_t kp[4] = {0, 0, 0, 0}, qp[4] = {0, 0, 0, 0}, km[4] = {0, 0, 0, 0},
-                 ke[4] = {0, 0, 0, 0};
+        uint32_t kp[4] = {0, 0, 0, 0}, qp[4] = {0, 0, 0, 0}, km[4] = {0, 0, 0, 0};
         if (r < cl) {
           const uint4 kw = ld_shared_v4(sb + okq + ck);
           const uint4 qw = ld_shared_v4(sb + Ly::kQ + okq + ck);
           const uint32_t kv[4] = {kw.x, kw.y, kw.z, kw.w}, qv[4] = {qw.x, qw.y, qw.z, qw.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const float x0 = pre[2 * j] + gl[rr][2 * j] - anc[2 * j];  // G_r - a
-            const float x1 = pre[2 * j + 1] + gl[rr][2 * j + 1] - anc[2 * j + 1];
+            const float x0 = pre[2 * j] + gl[rr][2 * j];  // G_r - a
+            const float x1 = pre[2 * j + 1] + gl[rr][2 * j + 1];
             const float e0 = __expf(x0), e1 = __expf(x1);
             const float f0 = __expf(-x0), f1 = __expf(-x1);
             const float k0 = bf16lo(kv[j]), k1 = bf16hi(kv[j]);
@@ -385,13 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             kp[j] = pack_bf16x2(k0 * e0, k1 * e1);
             qp[j] = pack_bf16x2(q0 * e0, q1 * e1);
             km[j] = pack_bf16x2(k0 * f0, k1 * f1);
-            ke[j] = pack_bf16x2(k0 * f0 * cke[2 * j], k1 * f1 * cke[2 * j + 1]);
           }
         }
         st_shared_v4(sb + okq + ck, kp[0], kp[1], kp[2], kp[3]);
         st_shared_v4(sb + Ly::kQ + okq + ck, qp[0], qp[1], qp[2], qp[3]);
         st_shared_v4(sb + og + ck, km[0], km[1], km[2], km[3]);
-        st_shared_v4(sbase + oke + ck, ke[0], ke[1], ke[2], ke[3]);
       }
     }
     fence_async_smem();
@@ -475,8 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------------------------ solve
     solve_T(Lm, reinterpret_cast<float *>(smem + Ly::kU),
-            reinterpret_cast<float *>(stage + Ly::kXd),
-            reinterpret_cast<float *>(stage + Ly::kYt), s_beta, smem + Ly::kTM, tid);
+            reinterpret_cast<float *>(smem + Ly::kXd),
+            reinterpret_cast<float *>(smem + Ly::kYt), s_beta, smem + Ly::kTM, tid);
     fence_async_smem();
     __syncthreads();
 
@@ -560,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t bd = sw128_desc(sbase + Ly::kU + kk * 2048, 8192, 1024);
-        mma_bf16(tmem + 256, sw128_desc(sbase + Ly::kKE + kk * 2048, 8192, 1024), bd, idesc_ke,
+        mma_bf16(tmem + 256, sw128_desc(sb + Ly::kG + kk * 2048, 8192, 1024), bd, idesc_ke,
                  kk > 0);
         mma_bf16(tmem + 384, sw128_desc(sbase + Ly::kTM + 8192 + kk * 32, 16, 1024), bd, idesc_v,
                  1);
@@ -593,13 +606,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     {
-      const float egc = expf(s_tot[c]);
+      // S = Diag(e^{G_C}) S + Diag(e^{G_C - a}) (K-^T U)   (K_end = K- e^{G_C - a})
+      const float egc = expf(s_tot[c]), cke = expf(s_tot[c] - s_anc[c]);
 #pragma unroll
       for (int p = 0; p < NH / 32; ++p) {
         float v[32];
         tmem_ld32(lane_base + 256 + col0 + p * 32, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) S[p * 32 + j] = fmaf(egc, S[p * 32 + j], v[j]);
+        for (int j = 0; j < 32; ++j) S[p * 32 + j] = fmaf(egc, S[p * 32 + j], cke * v[j]);
       }
       const int64_t done = (int64_t)n * kC + cl;
       if (a.snap_interval > 0 && done % a.snap_interval == 0) {
