@@ -19,7 +19,8 @@ from ._build import LIB_PATH, build  # noqa: F401
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_DEVICE_CHECK, \
     KDA_ERR_TIMEOUT = range(6)
 KDA_F32, KDA_BF16 = 0, 1
-KDA_ALGO_AUTO, KDA_ALGO_RECURRENT, KDA_ALGO_CHUNKED = 0, 1, 2
+KDA_ALGO_AUTO, KDA_ALGO_RECURRENT, KDA_ALGO_CHUNKED, KDA_ALGO_CHUNKED_PER_STATE, \
+    KDA_ALGO_CHUNKED_COOP = range(5)
 
 EXPORTS = ("kda_prefill_varlen", "kda_decode", "kda_workspace_bytes", "kda_snapshot_count",
            "kda_device_status", "kda_status_string", "kda_last_launch_count")

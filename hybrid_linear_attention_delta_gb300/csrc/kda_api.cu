@@ -79,7 +79,7 @@ kda_status kda_prefill_varlen(const void *q, const void *k, const void *v, const
   if (snap_interval == 0 && snaps) return KDA_ERR_INVALID_ARG;
   if (snap_interval > 0 && !snaps && a->snaps_capacity > 0) return KDA_ERR_INVALID_ARG;
   if (snaps && !aligned16(snaps)) return KDA_ERR_INVALID_ARG;
-  if (a->algo < KDA_ALGO_AUTO || a->algo > KDA_ALGO_CHUNKED) return KDA_ERR_INVALID_ARG;
+  if (a->algo < KDA_ALGO_AUTO || a->algo > KDA_ALGO_CHUNKED_COOP) return KDA_ERR_INVALID_ARG;
   if (a->B == 0) return a->T_total == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
   if (!cu_seqlens || !init_slots || !state_pool || !aligned16(state_pool))
     return KDA_ERR_INVALID_ARG;
@@ -102,15 +102,26 @@ kda_status kda_prefill_varlen(const void *q, const void *k, const void *v, const
   p.claims = reinterpret_cast<uint32_t *>(ws + lay.claims_off);
   p.epoch = next_epoch();
   p.stream = static_cast<cudaStream_t>(a->stream);
+  if (lay.coop_units > 0) {
+    p.coop_hdr = reinterpret_cast<uint32_t *>(ws + lay.coop_off);
+    p.coop_flags = reinterpret_cast<unsigned long long *>(ws + lay.coop_flags_off);
+    p.coop_ring = reinterpret_cast<uint8_t *>(ws + lay.coop_ring_off);
+  }
 
   bool chunked = kda::chunked_supported(p);
-  if (a->algo == KDA_ALGO_CHUNKED && !chunked) return KDA_ERR_UNSUPPORTED;
+  int mode = kda::kChunkAuto;
+  if (a->algo == KDA_ALGO_CHUNKED_PER_STATE) mode = kda::kChunkPerState;
+  if (a->algo == KDA_ALGO_CHUNKED_COOP) {
+    if (!kda::coop_supported(p)) return KDA_ERR_UNSUPPORTED;
+    mode = kda::kChunkCoop;
+  }
+  if (a->algo >= KDA_ALGO_CHUNKED && !chunked) return KDA_ERR_UNSUPPORTED;
   if (a->algo == KDA_ALGO_RECURRENT) chunked = false;
 
   if ((st = from_cuda(kda::launch_meta(p))) != KDA_OK) return st;
   g_last_launches = 1;
   record(a->ev_begin, p.stream);
-  st = from_cuda(chunked ? kda::launch_chunked_prefill(p) : kda::launch_recurrent_prefill(p));
+  st = from_cuda(chunked ? kda::launch_chunked_prefill(p, mode) : kda::launch_recurrent_prefill(p));
   record(a->ev_end, p.stream);
   if (st == KDA_OK) g_last_launches = 2;
   return st;

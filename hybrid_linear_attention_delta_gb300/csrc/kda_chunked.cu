@@ -202,6 +202,172 @@ __device__ __forceinline__ void solve_T(const float *L, float *XT, float *Xd, fl
   solve_level<3>(L, XT, Xd, YT, beta, tm, tid);
 }
 
+// ------------------------------------------------------------------ chunk phases
+// The steps of one chunk that do not depend on its start state, shared by the
+// single-CTA kernel and the producer role of the cooperative kernel.  Ly is
+// the shared-memory layout; VCOLS the v columns staged per chunk.
+
+// Decay-scaled operands of one chunk, in place in its stage: K+ over k, Q+
+// over q, K- over g; per channel the anchor a (s_anc) and the chunk decay G_C
+// (s_tot); beta (s_beta, zero past the end); v rows past a ragged end zeroed.
+// Thread: channels [8 cq, 8 cq + 8) x rows [4 rg, 4 rg + 4), 16-byte accesses.
+// Ends with the operand writes fenced for the tensor cores and a barrier.
+template <class Ly, int VCOLS>
+__device__ __forceinline__ void prep_chunk(uint32_t sb, int cl, const __nv_bfloat16 *beta_t0,
+                                           int H, float *s_gpart, float *s_beta, float *s_tot,
+                                           float *s_anc, int tid) {
+  const int cq = tid & 15, rg = tid >> 4;
+  const uint32_t okq = (cq >> 3) * 16384, og = Ly::kG + (cq >> 3) * 8192;
+  float gl[4][8];  // in-group inclusive cumulative decay
+#pragma unroll
+  for (int rr = 0; rr < 4; ++rr) {
+    const int r = 4 * rg + rr;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (r < cl) w = ld_shared_v4(sb + og + sw128_chunk(r, cq & 7));
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      gl[rr][2 * j] = (rr ? gl[rr - 1][2 * j] : 0.f) + bf16lo(wv[j]);
+      gl[rr][2 * j + 1] = (rr ? gl[rr - 1][2 * j + 1] : 0.f) + bf16hi(wv[j]);
+    }
+  }
+  float4 *gp = reinterpret_cast<float4 *>(s_gpart + rg * 128 + 8 * cq);
+  gp[0] = make_float4(gl[3][0], gl[3][1], gl[3][2], gl[3][3]);
+  gp[1] = make_float4(gl[3][4], gl[3][5], gl[3][6], gl[3][7]);
+  if (tid < 64) s_beta[tid] = tid < cl ? __bfloat162float(beta_t0[(int64_t)tid * H]) : 0.f;
+  if (cl < kC) {  // ragged tail: zero the v rows past the sequence end
+    for (int e = tid; e < (kC - cl) * (VCOLS / 8); e += kThreads) {
+      const int r = cl + e / (VCOLS / 8), chk = e % (VCOLS / 8);
+      st_shared_v4(sb + Ly::kV + (chk >> 3) * 8192 + sw128_chunk(r, chk & 7), 0, 0, 0, 0);
+    }
+  }
+  __syncthreads();
+  if (tid < 128) {  // per channel: exclusive prefix over the 16 row groups (in place)
+    float run = 0.f;
+#pragma unroll
+    for (int g2 = 0; g2 < 16; ++g2) {
+      const float p = s_gpart[g2 * 128 + tid];
+      s_gpart[g2 * 128 + tid] = run;
+      run += p;
+      if (g2 == 7) s_anc[tid] = run;  // a: decay through row 31
+    }
+    s_tot[tid] = run;                  // G_C: decay through the chunk
+  }
+  __syncthreads();
+  float pre[8];  // G before this thread's rows, minus the anchor
+  {
+    const float4 *pp = reinterpret_cast<const float4 *>(s_gpart + rg * 128 + 8 * cq);
+    const float4 *pa = reinterpret_cast<const float4 *>(s_anc + 8 * cq);
+    const float4 p0 = pp[0], p1 = pp[1], a0 = pa[0], a1 = pa[1];
+    pre[0] = p0.x - a0.x; pre[1] = p0.y - a0.y; pre[2] = p0.z - a0.z; pre[3] = p0.w - a0.w;
+    pre[4] = p1.x - a1.x; pre[5] = p1.y - a1.y; pre[6] = p1.z - a1.z; pre[7] = p1.w - a1.w;
+  }
+#pragma unroll
+  for (int rr = 0; rr < 4; ++rr) {
+    const int r = 4 * rg + rr;
+    const uint32_t ck = sw128_chunk(r, cq & 7);
+    uint32_t kp[4] = {0, 0, 0, 0}, qp[4] = {0, 0, 0, 0}, km[4] = {0, 0, 0, 0};
+    if (r < cl) {
+      const uint4 kw = ld_shared_v4(sb + okq + ck);
+      const uint4 qw = ld_shared_v4(sb + Ly::kQ + okq + ck);
+      const uint32_t kv[4] = {kw.x, kw.y, kw.z, kw.w}, qv[4] = {qw.x, qw.y, qw.z, qw.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float x0 = pre[2 * j] + gl[rr][2 * j];  // G_r - a
+        const float x1 = pre[2 * j + 1] + gl[rr][2 * j + 1];
+        const float e0 = __expf(x0), e1 = __expf(x1);
+        const float f0 = __expf(-x0), f1 = __expf(-x1);
+        const float k0 = bf16lo(kv[j]), k1 = bf16hi(kv[j]);
+        const float q0 = bf16lo(qv[j]), q1 = bf16hi(qv[j]);
+        kp[j] = pack_bf16x2(k0 * e0, k1 * e1);
+        qp[j] = pack_bf16x2(q0 * e0, q1 * e1);
+        km[j] = pack_bf16x2(k0 * f0, k1 * f1);
+      }
+    }
+    st_shared_v4(sb + okq + ck, kp[0], kp[1], kp[2], kp[3]);
+    st_shared_v4(sb + Ly::kQ + okq + ck, qp[0], qp[1], qp[2], qp[3]);
+    st_shared_v4(sb + og + ck, km[0], km[1], km[2], km[3]);
+  }
+  fence_async_smem();
+  __syncthreads();
+}
+
+// MMA1: [K+; Q+] K-^T -> d (64 columns: rows 0..63 A-raw, rows 64..127 Q+K-^T).
+template <class Ly>
+__device__ __forceinline__ void issue_mma1(uint32_t d, uint32_t sb) {
+  tc_fence_after();
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_bf16(d, sw128_desc(sb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+             sw128_desc(sb + Ly::kG + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+             idesc_bf16(128, 64, 0, 0), kk > 0);
+}
+
+// A (rows 0..63 of the MMA1 result at taddr) into the fp32 system L (fidx
+// layout, Diag(beta) strict_lower, zero elsewhere); M = lower_incl(Q+ K-^T)
+// (rows 64..127) as bf16 into rows 64..127 of [T; M] at tm.
+__device__ __forceinline__ void extract_am(uint32_t taddr, int quarter, int colhalf, int lane,
+                                           const float *s_beta, float *Lm, uint32_t tm) {
+  float v[32];
+  tmem_ld32(taddr + colhalf * 32, v);
+  const int rr = quarter * 32 + lane;
+  if (quarter < 2) {
+    const float br = s_beta[rr];
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4) {
+      const int i = colhalf * 32 + q4 * 4;
+      *reinterpret_cast<float4 *>(Lm + fidx(rr, i)) =
+          make_float4(i < rr ? br * v[q4 * 4] : 0.f, i + 1 < rr ? br * v[q4 * 4 + 1] : 0.f,
+                      i + 2 < rr ? br * v[q4 * 4 + 2] : 0.f, i + 3 < rr ? br * v[q4 * 4 + 3] : 0.f);
+    }
+  } else {
+    const int r = rr - 64;
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      float w8[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = colhalf * 32 + q4 * 8 + j;
+        w8[j] = (i <= r) ? v[q4 * 8 + j] : 0.f;
+      }
+      st_shared_v4(tm + sw128_chunk(64 + r, colhalf * 4 + q4), pack_bf16x2(w8[0], w8[1]),
+                   pack_bf16x2(w8[2], w8[3]), pack_bf16x2(w8[4], w8[5]), pack_bf16x2(w8[6], w8[7]));
+    }
+  }
+}
+
+// MMA2: [T; M] K+ -> tmem[0, 128) and [T; M] V -> tmem[128, 128 + VCOLS).
+template <class Ly, int VCOLS>
+__device__ __forceinline__ void issue_mma2(uint32_t tmem, uint32_t tm, uint32_t sb) {
+  tc_fence_after();
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    const uint64_t ad = sw128_desc(tm + kk * 32, 16, 1024);
+    mma_bf16(tmem + 0, ad, sw128_desc(sb + kk * 2048, 16384, 1024), idesc_bf16(128, 128, 0, 1),
+             kk > 0);
+    mma_bf16(tmem + 128, ad, sw128_desc(sb + Ly::kV + kk * 2048, 8192, 1024),
+             idesc_bf16(128, VCOLS, 0, 1), kk > 0);
+  }
+}
+
+// W (rows 0..63 of tmem[0, 128)) as bf16 [token][channel] (K-major W, or the
+// MN-major view with K = token).
+__device__ __forceinline__ void extract_w(uint32_t lane_base, int quarter, int colhalf, int lane,
+                                          uint32_t w) {
+  if (quarter >= 2) return;
+  const int r = quarter * 32 + lane;
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    float v[32];
+    tmem_ld32(lane_base + colhalf * 64 + p * 32, v);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4)
+      st_shared_v4(w + colhalf * 8192 + sw128_chunk(r, p * 4 + q4),
+                   pack_bf16x2(v[q4 * 8], v[q4 * 8 + 1]), pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]),
+                   pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]), pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]));
+  }
+}
+
 template <int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -299,8 +465,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0 && nchunks > 0) issue_tma(0);
   tma_pending[0] = nchunks > 0;
 
-  const uint32_t idesc_am = idesc_bf16(128, 64, 0, 0);
-  const uint32_t idesc_w = idesc_bf16(128, 128, 0, 1);
   const uint32_t idesc_v = idesc_bf16(128, DV, 0, 1);
   const uint32_t idesc_vneg = idesc_bf16(128, DV, 0, 1, 1);
   const uint32_t idesc_ke = idesc_bf16(128, DV, 1, 1);
@@ -322,103 +486,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------ prep
-    // thread: channels [8 cq, 8 cq + 8) x rows [4 rg, 4 rg + 4), 16-byte accesses
-    const int cq = tid & 15, rg = tid >> 4;
-    const uint32_t okq = (cq >> 3) * 16384, og = Ly::kG + (cq >> 3) * 8192;
-    float gl[4][8];  // in-group inclusive cumulative decay
-    {
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const int r = 4 * rg + rr;
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (r < cl) w = ld_shared_v4(sb + og + sw128_chunk(r, cq & 7));
-        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          gl[rr][2 * j] = (rr ? gl[rr - 1][2 * j] : 0.f) + bf16lo(wv[j]);
-          gl[rr][2 * j + 1] = (rr ? gl[rr - 1][2 * j + 1] : 0.f) + bf16hi(wv[j]);
-        }
-      }
-      float4 *gp = reinterpret_cast<float4 *>(s_gpart + rg * 128 + 8 * cq);
-      gp[0] = make_float4(gl[3][0], gl[3][1], gl[3][2], gl[3][3]);
-      gp[1] = make_float4(gl[3][4], gl[3][5], gl[3][6], gl[3][7]);
-      if (tid < 64)
-        s_beta[tid] = tid < cl ? __bfloat162float(a.beta[(int64_t)(t0 + tid) * H + h]) : 0.f;
-      if (cl < kC) {  // ragged tail: zero the v rows past the sequence end
-        for (int e = tid; e < (kC - cl) * (DV / 8); e += kThreads) {
-          const int r = cl + e / (DV / 8), chk = e % (DV / 8);
-          st_shared_v4(sb + Ly::kV + (chk >> 3) * 8192 + sw128_chunk(r, chk & 7), 0, 0, 0, 0);
-        }
-      }
-    }
-    __syncthreads();
-    if (tid < 128) {  // per channel: exclusive prefix over the 16 row groups (in place)
-      float run = 0.f;
-#pragma unroll
-      for (int g2 = 0; g2 < 16; ++g2) {
-        const float p = s_gpart[g2 * 128 + tid];
-        s_gpart[g2 * 128 + tid] = run;
-        run += p;
-        if (g2 == 7) s_anc[tid] = run;  // a: decay through row 31
-      }
-      s_tot[tid] = run;                  // G_C: decay through the chunk
-    }
-    __syncthreads();
-    {
-      float pre[8], anc[8], tot[8];
-      {
-        const float4 *pp = reinterpret_cast<const float4 *>(s_gpart + rg * 128 + 8 * cq);
-        const float4 *pa = reinterpret_cast<const float4 *>(s_anc + 8 * cq);
-        const float4 *pt = reinterpret_cast<const float4 *>(s_tot + 8 * cq);
-        const float4 p0 = pp[0], p1 = pp[1], a0 = pa[0], a1 = pa[1], t0v = pt[0], t1v = pt[1];
-        pre[0] = p0.x; pre[1] = p0.y; pre[2] = p0.z; pre[3] = p0.w;
-        pre[4] = p1.x; pre[5] = p1.y; pre[6] = p1.z; pre[7] = p1.w;
-        anc[0] = a0.x; anc[1] = a0.y; anc[2] = a0.z; anc[3] = a0.w;
-        anc[4] = a1.x; anc[5] = a1.y; anc[6] = a1.z; anc[7] = a1.w;
-        tot[0] = t0v.x; tot[1] = t0v.y; tot[2] = t0v.z; tot[3] = t0v.w;
-        tot[4] = t1v.x; tot[5] = t1v.y; tot[6] = t1v.z; tot[7] = t1v.w;
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) pre[j] -= anc[j];  // G_r - a = pre + gl - a
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const int r = 4 * rg + rr;
-        const uint32_t ck = sw128_chunk(r, cq & 7);
-        uint32_t kp[4] = {0, 0, 0, 0}, qp[4] = {0, 0, 0, 0}, km[4] = {0, 0, 0, 0};
-        if (r < cl) {
-          const uint4 kw = ld_shared_v4(sb + okq + ck);
-          const uint4 qw = ld_shared_v4(sb + Ly::kQ + okq + ck);
-          const uint32_t kv[4] = {kw.x, kw.y, kw.z, kw.w}, qv[4] = {qw.x, qw.y, qw.z, qw.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float x0 = pre[2 * j] + gl[rr][2 * j];  // G_r - a
-            const float x1 = pre[2 * j + 1] + gl[rr][2 * j + 1];
-            const float e0 = __expf(x0), e1 = __expf(x1);
-            const float f0 = __expf(-x0), f1 = __expf(-x1);
-            const float k0 = bf16lo(kv[j]), k1 = bf16hi(kv[j]);
-            const float q0 = bf16lo(qv[j]), q1 = bf16hi(qv[j]);
-            kp[j] = pack_bf16x2(k0 * e0, k1 * e1);
-            qp[j] = pack_bf16x2(q0 * e0, q1 * e1);
-            km[j] = pack_bf16x2(k0 * f0, k1 * f1);
-          }
-        }
-        st_shared_v4(sb + okq + ck, kp[0], kp[1], kp[2], kp[3]);
-        st_shared_v4(sb + Ly::kQ + okq + ck, qp[0], qp[1], qp[2], qp[3]);
-        st_shared_v4(sb + og + ck, km[0], km[1], km[2], km[3]);
-      }
-    }
-    fence_async_smem();
-    __syncthreads();
+    prep_chunk<Ly, DV>(sb, cl, a.beta + (int64_t)t0 * H + h, H, s_gpart, s_beta, s_tot, s_anc,
+                       tid);
 
     // ------------------------------------------------------------ MMA1
     if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = sw128_desc(sb + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-        const uint64_t bd = sw128_desc(sb + Ly::kG + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-        mma_bf16(tmem + 256, ad, bd, idesc_am, kk > 0);
-      }
+      issue_mma1<Ly>(tmem + 256, sb);
       mma_commit(bar_mma);
     }
     mma_pending = true;
@@ -442,36 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // A (rows 0..63) into the fp32 system; M (rows 64..127) into [T; M]
     float *Lm = reinterpret_cast<float *>(smem + Ly::kW);
-    {
-      float v[32];
-      tmem_ld32(lane_base + 256 + colhalf * 32, v);
-      const int rr = quarter * 32 + lane;
-      if (quarter < 2) {  // L = Diag(beta) strict_lower(K+ K-^T), zero elsewhere
-        const float br = s_beta[rr];
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const int i = colhalf * 32 + q4 * 4;
-          *reinterpret_cast<float4 *>(Lm + fidx(rr, i)) =
-              make_float4(i < rr ? br * v[q4 * 4] : 0.f, i + 1 < rr ? br * v[q4 * 4 + 1] : 0.f,
-                          i + 2 < rr ? br * v[q4 * 4 + 2] : 0.f,
-                          i + 3 < rr ? br * v[q4 * 4 + 3] : 0.f);
-        }
-      } else {
-        const int r = rr - 64;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          float w8[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int i = colhalf * 32 + q4 * 8 + j;
-            w8[j] = (i <= r) ? v[q4 * 8 + j] : 0.f;
-          }
-          st_shared_v4(sbase + Ly::kTM + sw128_chunk(64 + r, colhalf * 4 + q4),
-                       pack_bf16x2(w8[0], w8[1]), pack_bf16x2(w8[2], w8[3]),
-                       pack_bf16x2(w8[4], w8[5]), pack_bf16x2(w8[6], w8[7]));
-        }
-      }
-    }
+    extract_am(lane_base + 256, quarter, colhalf, lane, s_beta, Lm, sbase + Ly::kTM);
     tc_fence_before();
     __syncthreads();
 
@@ -495,13 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------------------------ MMA2
     if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ad = sw128_desc(sbase + Ly::kTM + kk * 32, 16, 1024);
-        mma_bf16(tmem + 0, ad, sw128_desc(sb + kk * 2048, 16384, 1024), idesc_w, kk > 0);
-        mma_bf16(tmem + 128, ad, sw128_desc(sb + Ly::kV + kk * 2048, 8192, 1024), idesc_v, kk > 0);
-      }
+      issue_mma2<Ly, DV>(tmem, sbase + Ly::kTM, sb);
       mma_commit(bar_mma);
     }
     mma_pending = true;
@@ -511,20 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
 
     // W (rows 0..63) -> bf16 K-major operand
-    if (quarter < 2) {
-      const int r = quarter * 32 + lane;
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        float v[32];
-        tmem_ld32(lane_base + colhalf * 64 + p * 32, v);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          st_shared_v4(sbase + Ly::kW + colhalf * 8192 + sw128_chunk(r, p * 4 + q4),
-                       pack_bf16x2(v[q4 * 8], v[q4 * 8 + 1]), pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]),
-                       pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]),
-                       pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]));
-      }
-    }
+    extract_w(lane_base, quarter, colhalf, lane, sbase + Ly::kW);
     tc_fence_before();
     fence_async_smem();
     __syncthreads();
@@ -651,6 +676,472 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------------------ cooperative mode
+// For batches with few (sequence, head) pairs, one CTA per pair carries that
+// pair's state ("chain" CTA) while every other CTA of a cooperative grid
+// prepares chunks ("producer" CTAs): the part of a chunk that does not depend
+// on its start state.  Producers take chunks in ticket order (chunk index
+// major, so all pairs advance together) and hand each to its pair's chain CTA
+// as a package in a ring of kCoopRing slots in global memory (small enough to
+// stay in L2).  Ready / consumed flags hold the call's epoch in their upper
+// 32 bits and the chunk number + 1 below; every wait is bounded and an abort
+// word stops all CTAs after a timeout.
+//
+// With P = K-^T W and Q~ = Q+ - M W (computed by the producer), and
+// S' = Diag(e^{a}) S (bf16 operand), the single-CTA kernel's update becomes
+//     S_next = Diag(e^{G_C}) S + Diag(e^{G_C - a}) (K-^T U~ - P S')
+//     O      = Q~ S' + M U~
+// (U = U~ - W S' expanded), so the state's critical path per chunk is one
+// MMA group of the chain CTA.
+
+// package layout (bytes); each operand in the shared-memory layout the chain
+// CTA feeds to its MMAs, so packages are copied verbatim
+constexpr uint32_t kPkP = 0;        // P [128 i][128 j] bf16, K-major, 2 halves x 16 KiB
+constexpr uint32_t kPkKm = 32768;   // K- [64 tok][128 ch] bf16, 2 halves x 8 KiB
+constexpr uint32_t kPkU = 49152;    // U~ [64 tok][128 dv] bf16, 2 halves x 8 KiB
+constexpr uint32_t kPkQ = 65536;    // Q~ [64 tok][128 ch] bf16, K-major, 2 halves x 8 KiB
+constexpr uint32_t kPkM = 81920;    // M [64 tok][64 tok] bf16, K-major, 8 KiB
+constexpr uint32_t kPkDec = 90112;  // f32 e^{G_C}[128], e^{G_C - a}[128], e^{a}[128]
+static_assert(kPkDec + 1536 <= kCoopPkgBytes && kCoopPkgBytes % 1024 == 0, "package layout");
+// chain CTA shared memory: two package stages, S' (2 halves x 16 KiB), misc
+constexpr uint32_t kChS = 2 * (uint32_t)kCoopPkgBytes;
+constexpr uint32_t kChMisc = kChS + 32768;
+constexpr uint32_t kChBytes = kChMisc + 64;
+constexpr uint32_t kCoopSmem =
+    Layout<128>::kBytes > kChBytes ? Layout<128>::kBytes : kChBytes;
+
+struct CoopArgs {
+  ChunkArgs c;
+  uint8_t *ring;                       // [units][kCoopRing][kCoopPkgBytes]
+  unsigned long long *ready, *consumed;  // [units][kCoopRing]
+  uint32_t *hdr;                       // [0] ticket, [1] abort, [2] max chunks per sequence
+  int units;                           // (sequence, head) pairs = chain CTAs
+  uint32_t epoch;
+};
+
+__device__ __forceinline__ unsigned long long coop_tag(uint32_t epoch, int n) {
+  return ((unsigned long long)epoch << 32) | (unsigned long long)(n + 1);
+}
+
+// Thread 0: bounded wait until *p >= want (about a second); false on timeout
+// or when another CTA aborted.
+__device__ bool coop_flag_wait(const unsigned long long *p, unsigned long long want,
+                               const uint32_t *abort_flag) {
+  for (uint32_t i = 0; i < (1u << 22); ++i) {
+    if (ld_acquire_u64(p) >= want) return true;
+    if (*reinterpret_cast<const volatile uint32_t *>(abort_flag)) return false;
+    __nanosleep(i < 64 ? 32 : 256);
+  }
+  return false;
+}
+
+__device__ __forceinline__ void coop_abort(const CoopArgs &a) {
+  atomicExch(a.hdr + 1, 1u);
+  raise_error(a.c.err, ERR_TIMEOUT);
+}
+
+__device__ __forceinline__ uint4 pack8(const float *v) {
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
+}
+
+// Producer role: prepares chunks of any pair, in ticket order.
+__device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
+                              const CUtensorMap *tm_v, const CUtensorMap *tm_g,
+                              const CoopArgs &a) {
+  using Ly = Layout<128>;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, colhalf = warp >> 2;
+  const uint32_t sbase = smem_u32(smem);
+  const int H = a.c.H, units = a.units;
+  uint8_t *misc = smem + Ly::kMisc;
+  const uint32_t bar_tma0 = sbase + Ly::kMisc + Ly::kBars, bar_mma = bar_tma0 + 16;
+  float *s_beta = reinterpret_cast<float *>(misc + Ly::kBeta);
+  float *s_tot = reinterpret_cast<float *>(misc + Ly::kTot);
+  float *s_anc = reinterpret_cast<float *>(misc + Ly::kAnc);
+  float *s_gpart = reinterpret_cast<float *>(smem + Ly::kGpart);
+  volatile int *s_item = reinterpret_cast<volatile int *>(misc + 32);
+
+  if (tid == 0) {
+    mbar_init(bar_tma0, 1);
+    mbar_init(bar_tma0 + 8, 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(sbase + Ly::kMisc + Ly::kSlot, kTmemCols);
+  for (int e = tid; e < 16384 / 16; e += kThreads) st_shared_v4(sbase + Ly::kTM + 16 * e, 0, 0, 0, 0);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc + Ly::kSlot);
+  const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+  const int total = (int)a.hdr[2] * units;
+
+  auto take = [&]() -> int {  // thread 0: next ticket that names a real chunk, or -1
+    for (;;) {
+      if (*reinterpret_cast<volatile uint32_t *>(a.hdr + 1)) return -1;
+      const int t = (int)atomicAdd(a.hdr, 1u);
+      if (t >= total) return -1;
+      const SeqMeta m = a.c.meta[a.c.order[(t % units) / H]];
+      if (m.ok && (t / units) * kC < m.len) return t;
+    }
+  };
+  auto issue = [&](int t, int st) {  // thread 0: TMA loads of chunk t into stage st
+    const int u = t % units, h = u % H;
+    const SeqMeta m = a.c.meta[a.c.order[u / H]];
+    const uint32_t sb = sbase + st * Ly::kStage, bar = bar_tma0 + 8 * st;
+    const int y = m.tok0 + (t / units) * kC;
+    mbar_expect_tx(bar, 8 * 8192);
+    tma_load_2d(sb, tm_k, h * kDK, y, bar);
+    tma_load_2d(sb + 16384, tm_k, h * kDK + 64, y, bar);
+    tma_load_2d(sb + Ly::kQ, tm_q, h * kDK, y, bar);
+    tma_load_2d(sb + Ly::kQ + 16384, tm_q, h * kDK + 64, y, bar);
+    tma_load_2d(sb + Ly::kV, tm_v, h * 128, y, bar);
+    tma_load_2d(sb + Ly::kV + 8192, tm_v, h * 128 + 64, y, bar);
+    tma_load_2d(sb + Ly::kG, tm_g, h * kDK, y, bar);
+    tma_load_2d(sb + Ly::kG + 8192, tm_g, h * kDK + 64, y, bar);
+  };
+
+  if (tid == 0) {
+    const int t = take();
+    s_item[0] = t;
+    if (t >= 0) issue(t, 0);
+  }
+  __syncthreads();
+  int cur = s_item[0];
+  uint32_t uses[2] = {0, 0}, mma_phase = 0;
+  bool tma_pending[2] = {cur >= 0, false}, mma_pending = false, aborted = false;
+  for (int it = 0; cur >= 0; ++it) {
+    const int st = it & 1;
+    if (tid == 0) {  // the other stage was released at the end of the previous chunk
+      const int t = take();
+      s_item[1] = t;
+      if (t >= 0) issue(t, st ^ 1);
+    }
+    __syncthreads();
+    const int next = s_item[1];
+    if (next >= 0) tma_pending[st ^ 1] = true;
+    if (!cta_wait(bar_tma0 + 8 * st, uses[st] & 1)) { aborted = true; break; }
+    ++uses[st];
+    tma_pending[st] = false;
+
+    const int n = cur / units, u = cur % units, h = u % H;
+    const SeqMeta m = a.c.meta[a.c.order[u / H]];
+    const int t0 = m.tok0 + n * kC, cl = min(kC, m.len - n * kC);
+    uint8_t *stage = smem + st * Ly::kStage;
+    const uint32_t sb = sbase + st * Ly::kStage;
+
+    prep_chunk<Ly, 128>(sb, cl, a.c.beta + (int64_t)t0 * H + h, H, s_gpart, s_beta, s_tot, s_anc,
+                        tid);
+    if (tid == 0) {
+      issue_mma1<Ly>(tmem + 256, sb);
+      mma_commit(bar_mma);
+    }
+    mma_pending = true;
+    if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
+    mma_phase ^= 1;
+    mma_pending = false;
+    tc_fence_after();
+    float *Lm = reinterpret_cast<float *>(smem + Ly::kW);
+    extract_am(lane_base + 256, quarter, colhalf, lane, s_beta, Lm, sbase + Ly::kTM);
+    tc_fence_before();
+    __syncthreads();
+    solve_T(Lm, reinterpret_cast<float *>(smem + Ly::kU),
+            reinterpret_cast<float *>(smem + Ly::kXd),
+            reinterpret_cast<float *>(smem + Ly::kYt), s_beta, smem + Ly::kTM, tid);
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      issue_mma2<Ly, 128>(tmem, sbase + Ly::kTM, sb);
+      mma_commit(bar_mma);
+    }
+    mma_pending = true;
+    if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
+    mma_phase ^= 1;
+    mma_pending = false;
+    tc_fence_after();
+    extract_w(lane_base, quarter, colhalf, lane, sbase + Ly::kW);
+    tc_fence_before();
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {  // P = K-^T W -> tmem[256, 384); M W -> tmem[384, 512)
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t bd = sw128_desc(sbase + Ly::kW + kk * 2048, 8192, 1024);
+        mma_bf16(tmem + 256, sw128_desc(sb + Ly::kG + kk * 2048, 8192, 1024), bd,
+                 idesc_bf16(128, 128, 1, 1), kk > 0);
+        mma_bf16(tmem + 384, sw128_desc(sbase + Ly::kTM + 8192 + kk * 32, 16, 1024), bd,
+                 idesc_bf16(128, 128, 0, 1), kk > 0);
+      }
+      mma_commit(bar_mma);
+    }
+    mma_pending = true;
+
+    // while they run: take the ring slot, copy the parts that are ready
+    const int slot = n % kCoopRing;
+    uint8_t *pk = a.ring + ((size_t)u * kCoopRing + slot) * kCoopPkgBytes;
+    {
+      int ok = 1;
+      if (tid == 0 && n >= kCoopRing)
+        ok = coop_flag_wait(a.consumed + u * kCoopRing + slot, coop_tag(a.epoch, n - kCoopRing),
+                            a.hdr + 1);
+      if (__syncthreads_or(!ok)) { aborted = true; break; }
+    }
+    for (int e = tid; e < 1024; e += kThreads)  // K- (the g slot)
+      *reinterpret_cast<uint4 *>(pk + kPkKm + 16 * e) =
+          *reinterpret_cast<const uint4 *>(stage + Ly::kG + 16 * e);
+    for (int e = tid; e < 512; e += kThreads)  // M (rows 64..127 of [T; M])
+      *reinterpret_cast<uint4 *>(pk + kPkM + 16 * e) =
+          *reinterpret_cast<const uint4 *>(smem + Ly::kTM + 8192 + 16 * e);
+    if (tid < 128) {
+      float *dec = reinterpret_cast<float *>(pk + kPkDec);
+      dec[tid] = expf(s_tot[tid]);
+      dec[128 + tid] = expf(s_tot[tid] - s_anc[tid]);
+      dec[256 + tid] = expf(s_anc[tid]);
+    }
+    if (quarter < 2) {  // U~ (rows 0..63 of tmem[128, 256)) as bf16 [token][dv]
+      const int r = quarter * 32 + lane;
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        float v[32];
+        tmem_ld32(lane_base + 128 + colhalf * 64 + p * 32, v);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          *reinterpret_cast<uint4 *>(pk + kPkU + colhalf * 8192 + sw128_chunk(r, p * 4 + q4)) =
+              pack8(v + 8 * q4);
+      }
+    }
+    if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
+    mma_phase ^= 1;
+    mma_pending = false;
+    tc_fence_after();
+    {  // P: row i (all 128), K-half colhalf
+      const int i = quarter * 32 + lane;
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        float v[32];
+        tmem_ld32(lane_base + 256 + colhalf * 64 + p * 32, v);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          *reinterpret_cast<uint4 *>(pk + kPkP + colhalf * 16384 + sw128_chunk(i, p * 4 + q4)) =
+              pack8(v + 8 * q4);
+      }
+    }
+    if (quarter < 2) {  // Q~ = Q+ - M W (rows 0..63)
+      const int r = quarter * 32 + lane;
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        float v[32];
+        tmem_ld32(lane_base + 384 + colhalf * 64 + p * 32, v);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint4 qw = ld_shared_v4(sb + Ly::kQ + colhalf * 16384 + sw128_chunk(r, p * 4 + q4));
+          const uint32_t qv[4] = {qw.x, qw.y, qw.z, qw.w};
+          float d[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            d[2 * j] = bf16lo(qv[j]) - v[8 * q4 + 2 * j];
+            d[2 * j + 1] = bf16hi(qv[j]) - v[8 * q4 + 2 * j + 1];
+          }
+          *reinterpret_cast<uint4 *>(pk + kPkQ + colhalf * 8192 + sw128_chunk(r, p * 4 + q4)) =
+              pack8(d);
+        }
+      }
+    }
+    tc_fence_before();
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) st_release_u64(a.ready + u * kCoopRing + slot, coop_tag(a.epoch, n));
+    cur = next;
+  }
+  if (aborted) {
+    if (tid == 0) coop_abort(a);
+    for (int s = 0; s < 2; ++s)
+      if (tma_pending[s]) mbar_wait(bar_tma0 + 8 * s, uses[s] & 1);
+    if (mma_pending) mbar_wait(bar_mma, mma_phase);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Chain role: carries the state of pair u through its packages.
+__device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, colhalf = warp >> 2;
+  const uint32_t sbase = smem_u32(smem);
+  const int H = a.c.H, h = u % H, dv = a.c.dv;
+  const SeqMeta m = a.c.meta[a.c.order[u / H]];
+  uint8_t *misc = smem + kChMisc;
+  const uint32_t bar_s = sbase + kChMisc, bar_o = bar_s + 8;
+  if (tid == 0) {
+    mbar_init(bar_s, 1);
+    mbar_init(bar_o, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(sbase + kChMisc + 16, 256);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc + 16);
+  const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+  const int c = quarter * 32 + lane, col0 = colhalf * 64;
+
+  float S[64];
+  if (m.ok && m.src >= 0) {
+    const float4 *s0 =
+        reinterpret_cast<const float4 *>(a.c.pool + (((int64_t)m.src * H + h) * kDK + c) * dv + col0);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float4 t = s0[j];
+      S[4 * j] = t.x; S[4 * j + 1] = t.y; S[4 * j + 2] = t.z; S[4 * j + 3] = t.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 64; ++j) S[j] = 0.f;
+  }
+  const int N = m.ok ? (m.len + kC - 1) / kC : 0;
+  const unsigned long long *ready = a.ready + u * kCoopRing;
+  unsigned long long *consumed = a.consumed + u * kCoopRing;
+  const uint8_t *ring_u = a.ring + (size_t)u * kCoopRing * kCoopPkgBytes;
+
+  // wait for package n and start copying it into stage n & 1 (all threads)
+  auto fetch = [&](int n) -> bool {
+    int ok = 1;
+    if (tid == 0) ok = coop_flag_wait(ready + n % kCoopRing, coop_tag(a.epoch, n), a.hdr + 1);
+    if (__syncthreads_or(!ok)) return false;
+    const uint8_t *src = ring_u + (size_t)(n % kCoopRing) * kCoopPkgBytes;
+    const uint32_t dst = sbase + (n & 1) * (uint32_t)kCoopPkgBytes;
+    for (int e = tid; e < (int)(kCoopPkgBytes / 16); e += kThreads) cp_async16(dst + 16 * e, src + 16 * e);
+    cp_async_commit();
+    return true;
+  };
+
+  bool aborted = false, pend_s = false, pend_o = false;
+  uint32_t ph_s = 0, ph_o = 0;
+  if (N > 0 && !fetch(0)) aborted = true;
+  for (int n = 0; n < N && !aborted; ++n) {
+    const int st = n & 1;
+    const int cl = min(kC, m.len - n * kC);
+    if (n + 1 < N) {
+      if (!fetch(n + 1)) { aborted = true; break; }
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) st_release_u64(consumed + n % kCoopRing, coop_tag(a.epoch, n));
+    const uint32_t sp = sbase + st * (uint32_t)kCoopPkgBytes;
+    const float *dec = reinterpret_cast<const float *>(smem + st * kCoopPkgBytes + kPkDec);
+    const float egc = dec[c], cke = dec[128 + c], ea = dec[256 + c];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // S' = Diag(e^{a}) S (MN-major: row = channel c)
+      float w8[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) w8[t] = ea * S[8 * j + t];
+      const int col = col0 + 8 * j;
+      const uint4 pw = pack8(w8);
+      st_shared_v4(sbase + kChS + (col >> 6) * 16384 + sw128_chunk(c, (col & 63) >> 3), pw.x, pw.y,
+                   pw.z, pw.w);
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)  // K-^T U~
+        mma_bf16(tmem, sw128_desc(sp + kPkKm + kk * 2048, 8192, 1024),
+                 sw128_desc(sp + kPkU + kk * 2048, 8192, 1024), idesc_bf16(128, 128, 1, 1), kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // -= P S'
+        mma_bf16(tmem, sw128_desc(sp + kPkP + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                 sw128_desc(sbase + kChS + kk * 2048, 16384, 1024), idesc_bf16(128, 128, 0, 1, 1), 1);
+      mma_commit(bar_s);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // O = Q~ S'
+        mma_bf16(tmem + 128, sw128_desc(sp + kPkQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                 sw128_desc(sbase + kChS + kk * 2048, 16384, 1024), idesc_bf16(128, 128, 0, 1),
+                 kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)  // O += M U~
+        mma_bf16(tmem + 128, sw128_desc(sp + kPkM + kk * 32, 16, 1024),
+                 sw128_desc(sp + kPkU + kk * 2048, 8192, 1024), idesc_bf16(128, 128, 0, 1), 1);
+      mma_commit(bar_o);
+    }
+    pend_s = pend_o = true;
+    if (!cta_wait(bar_s, ph_s)) { aborted = true; break; }
+    ph_s ^= 1;
+    pend_s = false;
+    tc_fence_after();
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      float v[32];
+      tmem_ld32(lane_base + col0 + p * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) S[p * 32 + j] = fmaf(egc, S[p * 32 + j], cke * v[j]);
+    }
+    const int64_t done = (int64_t)n * kC + cl;
+    if (a.c.snap_interval > 0 && done % a.c.snap_interval == 0) {
+      const int64_t s = m.snap_off + done / a.c.snap_interval - 1;
+      if (s < a.c.snaps_capacity) {
+        float4 *d = reinterpret_cast<float4 *>(a.c.snaps + ((s * H + h) * kDK + c) * dv + col0);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) d[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+      } else if (tid == 0) {
+        raise_error(a.c.err, ERR_SNAP_CAPACITY);
+      }
+    }
+    if (!cta_wait(bar_o, ph_o)) { aborted = true; break; }
+    ph_o ^= 1;
+    pend_o = false;
+    tc_fence_after();
+    if (quarter < 2) {
+      const int r = c;
+      __nv_bfloat16 *orow = a.c.out + ((int64_t)(m.tok0 + n * kC + r) * H + h) * dv + col0;
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        float v[32];
+        tmem_ld32(lane_base + 128 + col0 + p * 32, v);
+        if (r < cl) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + p * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) dst[q4] = pack8(v + 8 * q4);
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+  if (aborted) {
+    if (tid == 0) coop_abort(a);
+    cp_async_wait<0>();
+    if (pend_s) mbar_wait(bar_s, ph_s);
+    if (pend_o) mbar_wait(bar_o, ph_o);
+  } else if (m.ok) {
+    float4 *d = reinterpret_cast<float4 *>(a.c.pool + (((int64_t)m.dst * H + h) * kDK + c) * dv + col0);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) d[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    coop_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                const CoopArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023) {  // the swizzled layouts need a 1024-byte aligned base
+    if (threadIdx.x == 0) coop_abort(a);
+    return;
+  }
+  if ((int)blockIdx.x < a.units)
+    coop_chain(smem, a, blockIdx.x);
+  else
+    coop_producer(smem, &tm_q, &tm_k, &tm_v, &tm_g, a);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -706,6 +1197,54 @@ cudaError_t launch_dv(const PrefillPlan &p, const CUtensorMap &mq, const CUtenso
   return cudaGetLastError();
 }
 
+// Grid of the cooperative kernel on the current device (0 when it cannot run
+// there: no cooperative launch, or fewer than 16 producer CTAs would remain).
+int coop_grid(int units) {
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(coop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kCoopSmem) != cudaSuccess)
+      return 0;
+    attr = true;
+  }
+  int dev = 0, sms = 0, coop = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, coop_kernel, kThreads, kCoopSmem) !=
+          cudaSuccess)
+    return 0;
+  const int grid = sms * per_sm;
+  return grid >= units + 16 ? grid : 0;
+}
+
+cudaError_t launch_coop(const PrefillPlan &p, int grid, const CUtensorMap &mq,
+                        const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mg) {
+  CoopArgs a;
+  a.c.beta = static_cast<const __nv_bfloat16 *>(p.beta);
+  a.c.meta = p.meta;
+  a.c.order = p.order;
+  a.c.pool = p.pool;
+  a.c.out = static_cast<__nv_bfloat16 *>(p.out);
+  a.c.snaps = p.snaps;
+  a.c.snaps_capacity = p.snaps_capacity;
+  a.c.snap_interval = p.snap_interval;
+  a.c.H = p.H;
+  a.c.dv = p.dv;
+  a.c.n_dvb = 1;
+  a.c.err = p.err;
+  a.units = p.B * p.H;
+  a.ring = p.coop_ring;
+  a.ready = p.coop_flags;
+  a.consumed = p.coop_flags + (size_t)a.units * kCoopRing;
+  a.hdr = p.coop_hdr;
+  a.epoch = p.epoch;
+  CUtensorMap q = mq, k = mk, v = mv, g = mg;
+  void *args[] = {&q, &k, &v, &g, &a};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(coop_kernel), dim3(grid),
+                                     dim3(kThreads), args, kCoopSmem, p.stream);
+}
+
 }  // namespace
 
 bool chunked_supported(const PrefillPlan &p) {
@@ -713,12 +1252,21 @@ bool chunked_supported(const PrefillPlan &p) {
          (p.snap_interval % kC) == 0 && encode_fn() != nullptr;
 }
 
-cudaError_t launch_chunked_prefill(const PrefillPlan &p) {
+bool coop_supported(const PrefillPlan &p) {
+  return chunked_supported(p) && p.dv == 128 && p.coop_ring != nullptr &&
+         (int64_t)p.B * p.H <= kCoopMaxUnits && coop_grid(p.B * p.H) > 0;
+}
+
+cudaError_t launch_chunked_prefill(const PrefillPlan &p, int mode) {
   CUtensorMap mq, mk, mv, mg;
   const uint64_t T = (uint64_t)p.T_total;
   if (!make_map(&mq, p.q, (uint64_t)p.H * kDK, T) || !make_map(&mk, p.k, (uint64_t)p.H * kDK, T) ||
       !make_map(&mv, p.v, (uint64_t)p.H * p.dv, T) || !make_map(&mg, p.g, (uint64_t)p.H * kDK, T))
     return cudaErrorInvalidValue;
+  // cooperative producer/chain grid when few (sequence, head) pairs would
+  // leave most SMs idle; otherwise one CTA per (sequence, head, dv block)
+  if (mode == kChunkCoop || (mode == kChunkAuto && coop_supported(p)))
+    return launch_coop(p, coop_grid(p.B * p.H), mq, mk, mv, mg);
   // one dv block of 128 per (sequence, head) when that fills the GPU, else 64
   const bool narrow = (int64_t)p.B * p.H < 148 && p.dv == 128;
   if (p.dv == 64 || narrow) return launch_dv<64>(p, mq, mk, mv, mg);

@@ -38,15 +38,28 @@ static_assert(sizeof(SeqMeta) == 32, "SeqMeta is 32 bytes");
 
 constexpr int kClaimsPerState = 4;  // one claim word per (slot, head, column block)
 
+// Cooperative prefill (few (sequence, head) pairs): per pair a ring of chunk
+// packages handed from producer CTAs to the pair's state-carrying CTA.
+constexpr int kCoopMaxUnits = 64;      // (sequence, head) pairs it serves at most
+constexpr int kCoopRing = 4;           // packages in flight per pair
+constexpr size_t kCoopPkgBytes = 92160;
+
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WorkspaceLayout {
-  size_t meta_off, order_off, claims_off, total;
+  size_t meta_off, order_off, claims_off, coop_off, coop_flags_off, coop_ring_off, total;
+  int64_t coop_units;
   __host__ __device__ WorkspaceLayout(int64_t B, int64_t H, int64_t n_slots) {
     meta_off = 256;
     order_off = meta_off + align256((size_t)B * sizeof(SeqMeta));
     claims_off = order_off + align256((size_t)B * sizeof(int32_t));
-    total = claims_off + align256((size_t)n_slots * H * kClaimsPerState * sizeof(uint32_t));
+    coop_off = claims_off + align256((size_t)n_slots * H * kClaimsPerState * sizeof(uint32_t));
+    coop_units = (B * H <= kCoopMaxUnits) ? B * H : 0;
+    // header (ticket, abort, max chunks) | ready[u][ring] | consumed[u][ring] | ring
+    coop_flags_off = coop_off + 256;
+    coop_ring_off = coop_flags_off + align256((size_t)coop_units * kCoopRing * 16);
+    total = coop_units ? coop_ring_off + (size_t)coop_units * kCoopRing * kCoopPkgBytes
+                       : coop_off;
   }
 };
 
@@ -88,6 +101,10 @@ struct PrefillPlan {
   uint32_t *claims;
   uint32_t epoch;
   cudaStream_t stream;
+  // cooperative mode (null when the workspace has no room for it)
+  uint32_t *coop_hdr;           // [0] ticket, [1] abort, [2] max chunks per sequence
+  unsigned long long *coop_flags;  // ready[units][ring] then consumed[units][ring]
+  uint8_t *coop_ring;           // [units][ring][kCoopPkgBytes]
 };
 
 struct DecodePlan {
@@ -107,9 +124,11 @@ cudaError_t launch_meta(const PrefillPlan &p);
 cudaError_t launch_recurrent_prefill(const PrefillPlan &p);
 cudaError_t launch_recurrent_decode(const DecodePlan &p);
 cudaError_t launch_decode128(const DecodePlan &p);
-// Returns cudaErrorNotSupported when the chunked tensor-core kernel does not
-// apply to these shapes.
+// The chunked tensor-core prefill: whether it applies to these shapes, whether
+// its cooperative mode can run, and the launch (mode: which variant).
+enum ChunkMode { kChunkAuto = 0, kChunkPerState = 1, kChunkCoop = 2 };
 bool chunked_supported(const PrefillPlan &p);
-cudaError_t launch_chunked_prefill(const PrefillPlan &p);
+bool coop_supported(const PrefillPlan &p);
+cudaError_t launch_chunked_prefill(const PrefillPlan &p, int mode);
 
 }  // namespace kda

@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(kMetaThreads) meta_kernel(PrefillPlan p) {
   bad = __syncthreads_or(bad);
   if (bad) {
     if (tid == 0) raise_error(p.err, ERR_BAD_CU);
+    if (tid == 0 && p.coop_hdr) p.coop_hdr[0] = p.coop_hdr[1] = p.coop_hdr[2] = 0;
     for (int b = tid; b < B; b += kMetaThreads) {
       SeqMeta m = {0, 0, -1, 0, 0, 0, 0};
       p.meta[b] = m;
@@ -107,7 +108,26 @@ __global__ void __launch_bounds__(kMetaThreads) meta_kernel(PrefillPlan p) {
     __syncthreads();
   }
 
-  // 5. longest first (stable: ties keep batch order)
+  // 5. cooperative-mode header: ticket and abort cleared, longest sequence in chunks
+  if (p.coop_hdr) {
+    int mx = 0;
+    for (int b = tid; b < B; b += kMetaThreads) {
+      const SeqMeta m = p.meta[b];
+      if (m.ok) mx = max(mx, (m.len + 63) / 64);
+    }
+    for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    __shared__ int wmax[kMetaThreads / 32];
+    if ((tid & 31) == 0) wmax[tid >> 5] = mx;
+    __syncthreads();
+    if (tid == 0) {
+      for (int w = 1; w < kMetaThreads / 32; ++w) mx = max(mx, wmax[w]);
+      p.coop_hdr[0] = 0;
+      p.coop_hdr[1] = 0;
+      p.coop_hdr[2] = (uint32_t)mx;
+    }
+  }
+
+  // 6. longest first (stable: ties keep batch order)
   for (int b = tid; b < B; b += kMetaThreads) {
     int rank = b;
     if (B <= kMaxSortedB) {

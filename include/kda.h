@@ -61,12 +61,23 @@ typedef enum {
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 
-/* Which prefill algorithm to run.  AUTO picks the tensor-core chunked kernel
- * for bf16 with dk = dv = 128 and snap_interval % 64 == 0, else the
- * token-recurrent CUDA-core kernel (exact fp32 recurrence, any supported
- * shape).  The other two force one of them (CHUNKED returns
- * KDA_ERR_UNSUPPORTED where it does not apply). */
-typedef enum { KDA_ALGO_AUTO = 0, KDA_ALGO_RECURRENT = 1, KDA_ALGO_CHUNKED = 2 } kda_algo;
+/* Which prefill algorithm to run.  AUTO picks the tensor-core chunked
+ * prefill for bf16 with dk = 128, dv in {64, 128} and snap_interval % 64 == 0,
+ * else the token-recurrent CUDA-core kernel (exact fp32 recurrence, any
+ * supported shape).  The chunked prefill has two variants: one CTA per
+ * (sequence, head, dv block), and, when a batch has at most 64 (sequence,
+ * head) pairs with dv = 128 and the workspace was sized for it, a cooperative
+ * grid in which the other SMs prepare chunks for the per-pair CTAs.  CHUNKED
+ * lets the library choose the variant; CHUNKED_PER_STATE and CHUNKED_COOP
+ * force one.  A forced choice that does not apply returns
+ * KDA_ERR_UNSUPPORTED. */
+typedef enum {
+  KDA_ALGO_AUTO = 0,
+  KDA_ALGO_RECURRENT = 1,
+  KDA_ALGO_CHUNKED = 2,
+  KDA_ALGO_CHUNKED_PER_STATE = 3,
+  KDA_ALGO_CHUNKED_COOP = 4
+} kda_algo;
 
 typedef struct {
   int32_t B;              /* prefill: sequences in the packed batch; decode: N sequences */

@@ -49,9 +49,13 @@ def test_snapshot_count_and_workspace_bytes(lib):
     assert kda.kda_snapshot_count([0, 64], 0) == 0
     n1 = kda.kda_workspace_bytes(1, 32, 1)
     n2 = kda.kda_workspace_bytes(16, 32, 1024)
-    assert n1 >= 256 and n2 > n1 and n2 % 256 == 0
-    # claims: one word per (slot, head, column block) of the pool
-    assert n2 >= 1024 * 32 * 4 * 4
+    assert n1 % 256 == 0 and n2 % 256 == 0
+    # few (sequence, head) pairs: room for the cooperative prefill's package
+    # ring (4 packages of 90 KiB per pair)
+    assert n1 >= 32 * 4 * 92160
+    # claims: one word per (slot, head, column block) of the pool; 512 pairs
+    # use the per-state prefill, so no ring
+    assert 1024 * 32 * 4 * 4 <= n2 < 1024 * 32 * 4 * 4 + 16 * 32 * 64 + 4096
 
 
 def test_status_strings(lib):

@@ -14,6 +14,9 @@ from kda_cases import (TOL, assert_untouched, gpu_prefill, oracle_prefill, rel, 
 
 pytestmark = pytest.mark.gpu
 CH = kda.KDA_ALGO_CHUNKED
+PER = kda.KDA_ALGO_CHUNKED_PER_STATE
+COOP = kda.KDA_ALGO_CHUNKED_COOP
+MODES = pytest.mark.parametrize("mode", [PER, COOP], ids=["per_state", "coop"])
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -47,13 +50,15 @@ def _check(b, snap, out, pool, snaps, tol=TOL["bf16"]):
     return e_out, e_state
 
 
+@MODES
 @pytest.mark.parametrize("lens", [[64], [1], [63, 65], [200, 130, 7], [129, 0, 256]])
-def test_chunked_ragged_varlen(lens):
-    """Ragged tails and empty sequences; the narrow (64-column) dv blocks."""
+def test_chunked_ragged_varlen(lens, mode):
+    """Ragged tails and empty sequences, in both chunked variants (the
+    per-state one with narrow 64-column dv blocks)."""
     B = len(lens)
     slots = [[-1, b] for b in range(B)]
     b = _case(lens, 3, B + 2, slots)
-    out, pool, snaps, (st, bits) = gpu_prefill(b, 64, algo=CH)
+    out, pool, snaps, (st, bits) = gpu_prefill(b, 64, algo=mode)
     assert st == kda.KDA_OK and bits == 0
     _check(b, 64, out, pool, snaps)
 
@@ -81,55 +86,61 @@ def test_chunked_dv64_heads():
     _check(b, 128, out, pool, snaps)
 
 
-def test_chunked_matches_recurrent_path():
+@MODES
+def test_chunked_matches_recurrent_path(mode):
     lens = [300, 77]
     b = _case(lens, 4, 4, [[0, 2], [-1, 3]])
-    o1, p1, s1, _ = gpu_prefill(b, 64, algo=CH)
+    o1, p1, s1, _ = gpu_prefill(b, 64, algo=mode)
     o2, p2, s2, _ = gpu_prefill(b, 64, algo=kda.KDA_ALGO_RECURRENT)
     assert rel(o1, o2.float().cpu().numpy()) <= TOL["bf16"]
     assert rel(s1, s2.cpu().numpy()) <= TOL["bf16"]
     assert rel(p1[2:4], p2[2:4].cpu().numpy()) <= TOL["bf16"]
 
 
-def test_chunked_snapshot_equals_prefix_final_state():
+@MODES
+def test_chunked_snapshot_equals_prefix_final_state(mode):
     """Snapshot j is bit-identical to the final state of a prefill of the
     first (j+1)*interval tokens (same kernel path, same chunking)."""
     L, I = 320, 64
     b = _case([L], 2, 2, [[-1, 0]])
-    _, _, snaps, _ = gpu_prefill(b, I, algo=CH)
+    _, _, snaps, _ = gpu_prefill(b, I, algo=mode)
     for j in range(L // I):
         n = (j + 1) * I
         bj = inputs.Batch(q=b.q[:n], k=b.k[:n], v=b.v[:n], g=b.g[:n], beta=b.beta[:n],
                           cu_seqlens=torch.tensor([0, n], dtype=torch.int32),
                           init_slots=b.init_slots, pool=b.pool)
-        _, pj, _, _ = gpu_prefill(bj, 0, algo=CH)
+        _, pj, _, _ = gpu_prefill(bj, 0, algo=mode)
         assert torch.equal(snaps[j].cpu(), pj[0].cpu()), f"snapshot {j}"
 
 
-def test_chunked_resume_chain_is_exact_on_chunk_boundaries():
+@MODES
+def test_chunked_resume_chain_is_exact_on_chunk_boundaries(mode):
     """prefill(L1) -> slot, then prefill(L2) from that slot equals prefill(L1+L2)
     bit for bit when L1 is a multiple of the chunk (the state round-trips
     through the fp32 pool exactly)."""
     L1, L2 = 128, 100
     b = _case([L1 + L2], 2, 3, [[-1, 0]])
-    o_all, p_all, _, _ = gpu_prefill(b, 0, algo=CH)
+    o_all, p_all, _, _ = gpu_prefill(b, 0, algo=mode)
     b1 = inputs.Batch(q=b.q[:L1], k=b.k[:L1], v=b.v[:L1], g=b.g[:L1], beta=b.beta[:L1],
                       cu_seqlens=torch.tensor([0, L1], dtype=torch.int32),
                       init_slots=torch.tensor([[-1, 1]], dtype=torch.int32), pool=b.pool)
-    o1, p1, _, _ = gpu_prefill(b1, 0, algo=CH)
+    o1, p1, _, _ = gpu_prefill(b1, 0, algo=mode)
     b2 = inputs.Batch(q=b.q[L1:], k=b.k[L1:], v=b.v[L1:], g=b.g[L1:], beta=b.beta[L1:],
                       cu_seqlens=torch.tensor([0, L2], dtype=torch.int32),
                       init_slots=torch.tensor([[1, 2]], dtype=torch.int32),
                       pool=p1.cpu())
-    o2, p2, _, _ = gpu_prefill(b2, 0, algo=CH)
+    o2, p2, _, _ = gpu_prefill(b2, 0, algo=mode)
     assert torch.equal(torch.cat([o1, o2]).cpu(), o_all.cpu())
     assert torch.equal(p2[2].cpu(), p_all[0].cpu())
 
 
-def test_chunked_deterministic():
+@MODES
+def test_chunked_deterministic(mode):
+    """Bit-identical across runs (the cooperative variant's producers take
+    chunks in a different order every run; each package is computed the same)."""
     b = _case([500, 64], 3, 4, [[2, 0], [-1, 1]])
-    o1, p1, s1, _ = gpu_prefill(b, 64, algo=CH)
-    o2, p2, s2, _ = gpu_prefill(b, 64, algo=CH)
+    o1, p1, s1, _ = gpu_prefill(b, 64, algo=mode)
+    o2, p2, s2, _ = gpu_prefill(b, 64, algo=mode)
     assert torch.equal(o1.cpu(), o2.cpu()) and torch.equal(p1.cpu(), p2.cpu())
     assert torch.equal(s1.cpu(), s2.cpu())
 
@@ -138,7 +149,33 @@ def test_auto_selects_chunked_for_bf16_128():
     b = _case([100], 2, 1, [[-1, 0]])
     o_auto, _, _, _ = gpu_prefill(b, 0)
     o_ch, _, _, _ = gpu_prefill(b, 0, algo=CH)
+    o_coop, _, _, _ = gpu_prefill(b, 0, algo=COOP)
     assert torch.equal(o_auto.cpu(), o_ch.cpu())
+    assert torch.equal(o_auto.cpu(), o_coop.cpu())  # few (sequence, head) pairs: cooperative
+
+
+def test_coop_and_per_state_agree_with_resume():
+    """Both variants of the chunked prefill, on a resumed varlen batch with
+    snapshots, agree with each other to the bf16 tolerance (their arithmetic
+    differs: the cooperative one expands U = U~ - W S')."""
+    lens = [400, 129, 64]
+    b = _case(lens, 8, 8, [[5, 0], [-1, 1], [6, 2]])
+    o1, p1, s1, st1 = gpu_prefill(b, 128, algo=PER)
+    o2, p2, s2, st2 = gpu_prefill(b, 128, algo=COOP)
+    assert st1 == (0, 0) and st2 == (0, 0)
+    assert rel(o2, o1.float().cpu().numpy()) <= TOL["bf16"]
+    assert rel(s2, s1.cpu().numpy()) <= TOL["bf16"]
+    assert rel(p2[:3], p1[:3].cpu().numpy()) <= TOL["bf16"]
+    _check(b, 128, o2, p2, s2)
+
+
+def test_coop_refused_for_many_pairs():
+    """More than 64 (sequence, head) pairs: the cooperative variant does not
+    apply and forcing it is refused up front."""
+    b = _case([64] * 5, 16, 6, [[-1, i] for i in range(5)])
+    with pytest.raises(kda.KdaError) as e:
+        gpu_prefill(b, 0, algo=COOP)
+    assert e.value.status == kda.KDA_ERR_UNSUPPORTED
 
 
 # ------------------------------------------------------------ full-size workloads
