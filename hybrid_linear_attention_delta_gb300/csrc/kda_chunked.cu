@@ -70,7 +70,8 @@ struct Layout {
   static constexpr uint32_t kBeta = 64;                // f32[64]
   static constexpr uint32_t kTot = kBeta + 256;        // f32[128] G_C (chunk decay)
   static constexpr uint32_t kAnc = kTot + 512;         // f32[128] a (anchor decay)
-  static constexpr uint32_t kBytes = kMisc + kAnc + 512;
+  static constexpr uint32_t kSeqs = kAnc + 512;        // int2[64] (tok0, len) per sequence
+  static constexpr uint32_t kBytes = kMisc + kSeqs + 512;
   // prep scratch: per 4-row group decay sums f32[16][128], inside the W buffer
   static constexpr uint32_t kGpart = kW;
   // solve scratch (fp32): L (swizzled 64x64) in the W buffer, X^T in the U
@@ -745,6 +746,11 @@ __device__ __forceinline__ uint4 pack8(const float *v) {
                     pack_bf16x2(v[6], v[7]));
 }
 
+__device__ __forceinline__ void copy16(uint8_t *dst, const uint8_t *src, int bytes, int tid) {
+  for (int e = tid; e < bytes / 16; e += kThreads)
+    reinterpret_cast<uint4 *>(dst)[e] = reinterpret_cast<const uint4 *>(src)[e];
+}
+
 // Producer role: prepares chunks of any pair, in ticket order.
 __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                               const CUtensorMap *tm_v, const CUtensorMap *tm_g,
@@ -760,8 +766,13 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
   float *s_tot = reinterpret_cast<float *>(misc + Ly::kTot);
   float *s_anc = reinterpret_cast<float *>(misc + Ly::kAnc);
   float *s_gpart = reinterpret_cast<float *>(smem + Ly::kGpart);
+  int2 *s_seq = reinterpret_cast<int2 *>(misc + Ly::kSeqs);  // (tok0, len or 0) per sequence
   volatile int *s_item = reinterpret_cast<volatile int *>(misc + 32);
 
+  for (int r = tid; r < units / H; r += kThreads) {
+    const SeqMeta m = a.c.meta[a.c.order[r]];
+    s_seq[r] = make_int2(m.tok0, m.ok ? m.len : 0);
+  }
   if (tid == 0) {
     mbar_init(bar_tma0, 1);
     mbar_init(bar_tma0 + 8, 1);
@@ -781,15 +792,13 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       if (*reinterpret_cast<volatile uint32_t *>(a.hdr + 1)) return -1;
       const int t = (int)atomicAdd(a.hdr, 1u);
       if (t >= total) return -1;
-      const SeqMeta m = a.c.meta[a.c.order[(t % units) / H]];
-      if (m.ok && (t / units) * kC < m.len) return t;
+      if ((t / units) * kC < s_seq[(t % units) / H].y) return t;
     }
   };
   auto issue = [&](int t, int st) {  // thread 0: TMA loads of chunk t into stage st
     const int u = t % units, h = u % H;
-    const SeqMeta m = a.c.meta[a.c.order[u / H]];
     const uint32_t sb = sbase + st * Ly::kStage, bar = bar_tma0 + 8 * st;
-    const int y = m.tok0 + (t / units) * kC;
+    const int y = s_seq[u / H].x + (t / units) * kC;
     mbar_expect_tx(bar, 8 * 8192);
     tma_load_2d(sb, tm_k, h * kDK, y, bar);
     tma_load_2d(sb + 16384, tm_k, h * kDK + 64, y, bar);
@@ -801,32 +810,32 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     tma_load_2d(sb + Ly::kG + 8192, tm_g, h * kDK + 64, y, bar);
   };
 
+  // tickets run one chunk ahead of the loads, which run one chunk ahead of the work
   if (tid == 0) {
-    const int t = take();
-    s_item[0] = t;
-    if (t >= 0) issue(t, 0);
+    const int t0 = take();
+    s_item[0] = t0;
+    s_item[1] = t0 >= 0 ? take() : -1;
+    if (t0 >= 0) issue(t0, 0);
   }
   __syncthreads();
-  int cur = s_item[0];
+  int cur = s_item[0], next = s_item[1];
   uint32_t uses[2] = {0, 0}, mma_phase = 0;
   bool tma_pending[2] = {cur >= 0, false}, mma_pending = false, aborted = false;
   for (int it = 0; cur >= 0; ++it) {
     const int st = it & 1;
     if (tid == 0) {  // the other stage was released at the end of the previous chunk
-      const int t = take();
-      s_item[1] = t;
-      if (t >= 0) issue(t, st ^ 1);
+      if (next >= 0) issue(next, st ^ 1);
+      s_item[2] = next >= 0 ? take() : -1;
     }
-    __syncthreads();
-    const int next = s_item[1];
     if (next >= 0) tma_pending[st ^ 1] = true;
     if (!cta_wait(bar_tma0 + 8 * st, uses[st] & 1)) { aborted = true; break; }
     ++uses[st];
     tma_pending[st] = false;
+    const int after = s_item[2];
 
     const int n = cur / units, u = cur % units, h = u % H;
-    const SeqMeta m = a.c.meta[a.c.order[u / H]];
-    const int t0 = m.tok0 + n * kC, cl = min(kC, m.len - n * kC);
+    const int2 sq = s_seq[u / H];
+    const int t0 = sq.x + n * kC, cl = min(kC, sq.y - n * kC);
     uint8_t *stage = smem + st * Ly::kStage;
     const uint32_t sb = sbase + st * Ly::kStage;
 
@@ -877,54 +886,41 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     }
     mma_pending = true;
 
-    // while they run: take the ring slot, copy the parts that are ready
-    const int slot = n % kCoopRing;
-    uint8_t *pk = a.ring + ((size_t)u * kCoopRing + slot) * kCoopPkgBytes;
-    {
-      int ok = 1;
-      if (tid == 0 && n >= kCoopRing)
-        ok = coop_flag_wait(a.consumed + u * kCoopRing + slot, coop_tag(a.epoch, n - kCoopRing),
-                            a.hdr + 1);
-      if (__syncthreads_or(!ok)) { aborted = true; break; }
-    }
-    for (int e = tid; e < 1024; e += kThreads)  // K- (the g slot)
-      *reinterpret_cast<uint4 *>(pk + kPkKm + 16 * e) =
-          *reinterpret_cast<const uint4 *>(stage + Ly::kG + 16 * e);
-    for (int e = tid; e < 512; e += kThreads)  // M (rows 64..127 of [T; M])
-      *reinterpret_cast<uint4 *>(pk + kPkM + 16 * e) =
-          *reinterpret_cast<const uint4 *>(smem + Ly::kTM + 8192 + 16 * e);
-    if (tid < 128) {
-      float *dec = reinterpret_cast<float *>(pk + kPkDec);
-      dec[tid] = expf(s_tot[tid]);
-      dec[128 + tid] = expf(s_tot[tid] - s_anc[tid]);
-      dec[256 + tid] = expf(s_anc[tid]);
-    }
-    if (quarter < 2) {  // U~ (rows 0..63 of tmem[128, 256)) as bf16 [token][dv]
+    // The package is staged in shared memory in its final layout, then copied
+    // out with coalesced stores: U~ -> the U buffer (now free); P -> the v slot
+    // (K half 0) and the solve scratch (K half 1); Q~ -> the W buffer once the
+    // MMAs reading W are done; the decays -> the k slot; K- and M stay where
+    // they are.
+    if (quarter < 2) {  // U~: rows 0..63 of tmem[128, 256)
       const int r = quarter * 32 + lane;
 #pragma unroll
       for (int p = 0; p < 2; ++p) {
         float v[32];
         tmem_ld32(lane_base + 128 + colhalf * 64 + p * 32, v);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          *reinterpret_cast<uint4 *>(pk + kPkU + colhalf * 8192 + sw128_chunk(r, p * 4 + q4)) =
-              pack8(v + 8 * q4);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint4 w = pack8(v + 8 * q4);
+          st_shared_v4(sbase + Ly::kU + colhalf * 8192 + sw128_chunk(r, p * 4 + q4), w.x, w.y, w.z,
+                       w.w);
+        }
       }
     }
     if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
     mma_phase ^= 1;
     mma_pending = false;
     tc_fence_after();
-    {  // P: row i (all 128), K-half colhalf
+    {  // P: row i (all 128), K half colhalf
       const int i = quarter * 32 + lane;
+      const uint32_t dst = colhalf ? sbase + Ly::kScr : sb + Ly::kV;
 #pragma unroll
       for (int p = 0; p < 2; ++p) {
         float v[32];
         tmem_ld32(lane_base + 256 + colhalf * 64 + p * 32, v);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          *reinterpret_cast<uint4 *>(pk + kPkP + colhalf * 16384 + sw128_chunk(i, p * 4 + q4)) =
-              pack8(v + 8 * q4);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint4 w = pack8(v + 8 * q4);
+          st_shared_v4(dst + sw128_chunk(i, p * 4 + q4), w.x, w.y, w.z, w.w);
+        }
       }
     }
     if (quarter < 2) {  // Q~ = Q+ - M W (rows 0..63)
@@ -943,16 +939,40 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
             d[2 * j] = bf16lo(qv[j]) - v[8 * q4 + 2 * j];
             d[2 * j + 1] = bf16hi(qv[j]) - v[8 * q4 + 2 * j + 1];
           }
-          *reinterpret_cast<uint4 *>(pk + kPkQ + colhalf * 8192 + sw128_chunk(r, p * 4 + q4)) =
-              pack8(d);
+          const uint4 w = pack8(d);
+          st_shared_v4(sbase + Ly::kW + colhalf * 8192 + sw128_chunk(r, p * 4 + q4), w.x, w.y, w.z,
+                       w.w);
         }
       }
     }
+    if (tid < 128) {
+      float *dec = reinterpret_cast<float *>(stage);
+      dec[tid] = expf(s_tot[tid]);
+      dec[128 + tid] = expf(s_tot[tid] - s_anc[tid]);
+      dec[256 + tid] = expf(s_anc[tid]);
+    }
     tc_fence_before();
+    const int slot = n % kCoopRing;
+    {
+      int ok = 1;
+      if (tid == 0 && n >= kCoopRing)
+        ok = coop_flag_wait(a.consumed + u * kCoopRing + slot, coop_tag(a.epoch, n - kCoopRing),
+                            a.hdr + 1);
+      if (__syncthreads_or(!ok)) { aborted = true; break; }
+    }
+    uint8_t *pk = a.ring + ((size_t)u * kCoopRing + slot) * kCoopPkgBytes;
+    copy16(pk + kPkP, stage + Ly::kV, 16384, tid);
+    copy16(pk + kPkP + 16384, smem + Ly::kScr, 16384, tid);
+    copy16(pk + kPkKm, stage + Ly::kG, 16384, tid);
+    copy16(pk + kPkU, smem + Ly::kU, 16384, tid);
+    copy16(pk + kPkQ, smem + Ly::kW, 16384, tid);
+    copy16(pk + kPkM, smem + Ly::kTM + 8192, 8192, tid);
+    copy16(pk + kPkDec, stage, 1536, tid);
     __threadfence();
     __syncthreads();
     if (tid == 0) st_release_u64(a.ready + u * kCoopRing + slot, coop_tag(a.epoch, n));
     cur = next;
+    next = after;
   }
   if (aborted) {
     if (tid == 0) coop_abort(a);
@@ -965,7 +985,9 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Chain role: carries the state of pair u through its packages.
+// Chain role: carries the state of pair u through its packages.  Per chunk n:
+// issue its MMAs, then (while they run) retire chunk n-1's outputs and start
+// copying package n+1, then update the state.
 __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, colhalf = warp >> 2;
@@ -973,16 +995,17 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u) {
   const int H = a.c.H, h = u % H, dv = a.c.dv;
   const SeqMeta m = a.c.meta[a.c.order[u / H]];
   uint8_t *misc = smem + kChMisc;
-  const uint32_t bar_s = sbase + kChMisc, bar_o = bar_s + 8;
+  const uint32_t bar_s = sbase + kChMisc, bar_o0 = bar_s + 8;  // bar_o for buffers 0, 1
   if (tid == 0) {
     mbar_init(bar_s, 1);
-    mbar_init(bar_o, 1);
+    mbar_init(bar_o0, 1);
+    mbar_init(bar_o0 + 8, 1);
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(sbase + kChMisc + 16, 256);
+  if (warp == 0) tmem_alloc(sbase + kChMisc + 32, 512);
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc + 16);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc + 32);
   const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
   const int c = quarter * 32 + lane, col0 = colhalf * 64;
 
@@ -1015,22 +1038,44 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u) {
     cp_async_commit();
     return true;
   };
+  // outputs of chunk n from output buffer n & 1 (rows 0..63)
+  auto retire = [&](int n) {
+    if (quarter >= 2) return;
+    const int cl = min(kC, m.len - n * kC);
+    __nv_bfloat16 *orow = a.c.out + ((int64_t)(m.tok0 + n * kC + c) * H + h) * dv + col0;
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      float v[32];
+      tmem_ld32(lane_base + 128 + 128 * (n & 1) + col0 + p * 32, v);
+      if (c < cl) {
+        uint4 *dst = reinterpret_cast<uint4 *>(orow + p * 32);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) dst[q4] = pack8(v + 8 * q4);
+      }
+    }
+  };
 
-  bool aborted = false, pend_s = false, pend_o = false;
-  uint32_t ph_s = 0, ph_o = 0;
-  if (N > 0 && !fetch(0)) aborted = true;
+  bool aborted = false, pend_s = false, pend_o[2] = {false, false};
+  uint32_t ph_s = 0, ph_o[2] = {0, 0};
+  if (N > 0) {
+    if (!fetch(0)) {
+      aborted = true;
+    } else {
+      cp_async_wait<0>();
+      fence_async_smem();
+      __syncthreads();
+    }
+  }
   for (int n = 0; n < N && !aborted; ++n) {
     const int st = n & 1;
     const int cl = min(kC, m.len - n * kC);
-    if (n + 1 < N) {
-      if (!fetch(n + 1)) { aborted = true; break; }
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    fence_async_smem();
-    __syncthreads();
     if (tid == 0) st_release_u64(consumed + n % kCoopRing, coop_tag(a.epoch, n));
+    if (n > 0) {  // chunk n-1's output MMAs still read S'
+      if (!cta_wait(bar_o0 + 8 * (st ^ 1), ph_o[st ^ 1])) { aborted = true; break; }
+      ph_o[st ^ 1] ^= 1;
+      pend_o[st ^ 1] = false;
+      tc_fence_after();
+    }
     const uint32_t sp = sbase + st * (uint32_t)kCoopPkgBytes;
     const float *dec = reinterpret_cast<const float *>(smem + st * kCoopPkgBytes + kPkDec);
     const float egc = dec[c], cke = dec[128 + c], ea = dec[256 + c];
@@ -1057,18 +1102,23 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u) {
         mma_bf16(tmem, sw128_desc(sp + kPkP + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                  sw128_desc(sbase + kChS + kk * 2048, 16384, 1024), idesc_bf16(128, 128, 0, 1, 1), 1);
       mma_commit(bar_s);
+      const uint32_t o = tmem + 128 + 128 * st;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)  // O = Q~ S'
-        mma_bf16(tmem + 128, sw128_desc(sp + kPkQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+        mma_bf16(o, sw128_desc(sp + kPkQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
                  sw128_desc(sbase + kChS + kk * 2048, 16384, 1024), idesc_bf16(128, 128, 0, 1),
                  kk > 0);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)  // O += M U~
-        mma_bf16(tmem + 128, sw128_desc(sp + kPkM + kk * 32, 16, 1024),
+        mma_bf16(o, sw128_desc(sp + kPkM + kk * 32, 16, 1024),
                  sw128_desc(sp + kPkU + kk * 2048, 8192, 1024), idesc_bf16(128, 128, 0, 1), 1);
-      mma_commit(bar_o);
+      mma_commit(bar_o0 + 8 * st);
     }
-    pend_s = pend_o = true;
+    pend_s = pend_o[st] = true;
+    // under chunk n's MMAs: chunk n-1's outputs, then package n+1 into the
+    // stage chunk n-1 used (all of its MMAs are done)
+    if (n > 0) retire(n - 1);
+    if (n + 1 < N && !fetch(n + 1)) { aborted = true; break; }
     if (!cta_wait(bar_s, ph_s)) { aborted = true; break; }
     ph_s ^= 1;
     pend_s = false;
@@ -1091,32 +1141,29 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u) {
         raise_error(a.c.err, ERR_SNAP_CAPACITY);
       }
     }
-    if (!cta_wait(bar_o, ph_o)) { aborted = true; break; }
-    ph_o ^= 1;
-    pend_o = false;
-    tc_fence_after();
-    if (quarter < 2) {
-      const int r = c;
-      __nv_bfloat16 *orow = a.c.out + ((int64_t)(m.tok0 + n * kC + r) * H + h) * dv + col0;
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        float v[32];
-        tmem_ld32(lane_base + 128 + col0 + p * 32, v);
-        if (r < cl) {
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + p * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) dst[q4] = pack8(v + 8 * q4);
-        }
-      }
+    if (n + 1 < N) {
+      cp_async_wait<0>();
+      fence_async_smem();
     }
     tc_fence_before();
     __syncthreads();
+  }
+  if (!aborted && N > 0) {
+    const int b = (N - 1) & 1;
+    if (cta_wait(bar_o0 + 8 * b, ph_o[b])) {
+      pend_o[b] = false;
+      tc_fence_after();
+      retire(N - 1);
+    } else {
+      aborted = true;
+    }
   }
   if (aborted) {
     if (tid == 0) coop_abort(a);
     cp_async_wait<0>();
     if (pend_s) mbar_wait(bar_s, ph_s);
-    if (pend_o) mbar_wait(bar_o, ph_o);
+    for (int b = 0; b < 2; ++b)
+      if (pend_o[b]) mbar_wait(bar_o0 + 8 * b, ph_o[b]);
   } else if (m.ok) {
     float4 *d = reinterpret_cast<float4 *>(a.c.pool + (((int64_t)m.dst * H + h) * kDK + c) * dv + col0);
 #pragma unroll
@@ -1124,7 +1171,7 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u) {
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
