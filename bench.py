@@ -235,11 +235,11 @@ def bench_prefill(args, torch, kda, inputs, world, rank):
                                pool, out, w.snap_interval, snaps, workspace=ws)
         host_out.copy_(out, non_blocking=True)
 
-    for _ in range(2):
+    e2e_ms = []
+    for _ in range(0 if args.no_e2e else 2):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_ms = []
-    for _ in range(max(3, args.steps // 2)):
+    for _ in range(0 if args.no_e2e else max(3, args.steps // 2)):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -338,6 +338,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="decode only (profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -357,15 +359,16 @@ def main():
     kda.lib()   # raises if the CUDA library has not been built
 
     P = peaks()
-    pre = bench_prefill(args, torch, kda, inputs, world, rank)
-    step_s = statistics.mean(pre["call_ms"]) / 1e3
-    kern_s = statistics.mean(pre["kern_ms"]) / 1e3
-    e2e_s = statistics.mean(pre["e2e_ms"]) / 1e3
-    if world > 1:
-        t = torch.tensor([step_s, e2e_s], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_s, e2e_s = float(t[0]), float(t[1])
-    tokens = pre["T"] * world
+    if not args.no_prefill:
+        pre = bench_prefill(args, torch, kda, inputs, world, rank)
+        step_s = statistics.mean(pre["call_ms"]) / 1e3
+        kern_s = statistics.mean(pre["kern_ms"]) / 1e3
+        e2e_s = statistics.mean(pre["e2e_ms"]) / 1e3 if pre["e2e_ms"] else float("nan")
+        if world > 1:
+            t = torch.tensor([step_s, e2e_s], device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            step_s, e2e_s = float(t[0]), float(t[1])
+        tokens = pre["T"] * world
 
     dec = {}
     if not args.no_decode:
@@ -381,11 +384,15 @@ def main():
                                       "unit": "GB/s", "frac": gbs / P["hbm_gbs"],
                                       "traffic": ncu_traffic("decode128_" + name,
                                                              ["kda_decode.cu"]),
+                                      "kernel": "decode128_kernel",
                                       "peak_source": P["source"]}}
 
     if rank != 0:
         if world > 1:
             torch.distributed.barrier()
+        return 0
+    if args.no_prefill:
+        print(json.dumps({"metric": METRIC, "note": "decode-only run", "decode": dec}), flush=True)
         return 0
 
     cpu = None
@@ -415,7 +422,8 @@ def main():
                    "l2": "flushed between timed steps (256 MiB write)"},
         "roofline": {"bound": "hbm", "achieved": algo_gbs, "peak": P["hbm_gbs"], "unit": "GB/s",
                      "frac": algo_gbs / P["hbm_gbs"],
-                     "traffic": ncu_traffic("prefill_" + HEADLINE, [chunked, "kda_recurrent.cu"]),
+                     "traffic": ncu_traffic("prefill_" + HEADLINE, [chunked, "kda_sm100.cuh"]),
+                     "kernel": "coop_kernel (cooperative chunked prefill)",
                      "kernel_ms": kern_s * 1e3, "algorithmic_bytes": pre["nbytes"],
                      "peak_source": P["source"],
                      "tensor": {"achieved": algo_tflops, "unit": "TFLOP/s",
@@ -423,8 +431,9 @@ def main():
                                 "frac": algo_tflops / P.get("bf16_tflops", 1900.0),
                                 "algorithmic_flops": pre["flops"]}},
         "cpu_baseline": cpu,
-        "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": pre["h2d"],
-                "d2h_bytes_per_step": pre["d2h"]},
+        "e2e": None if args.no_e2e else {"value": tokens / e2e_s, "unit": "tokens/s",
+                                         "h2d_bytes_per_step": pre["h2d"],
+                                         "d2h_bytes_per_step": pre["d2h"]},
         "gpu_launches": pre["launches"],
         "clocks": pre["clocks"],
         "decode": dec,
