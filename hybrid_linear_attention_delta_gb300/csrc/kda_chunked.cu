@@ -213,10 +213,15 @@ __device__ __forceinline__ void solve_T(const float *L, float *XT, float *Xd, fl
 // (s_tot); beta (s_beta, zero past the end); v rows past a ragged end zeroed.
 // Thread: channels [8 cq, 8 cq + 8) x rows [4 rg, 4 rg + 4), 16-byte accesses.
 // Ends with the operand writes fenced for the tensor cores and a barrier.
+// A channel whose decay within one half of the chunk exceeds kMaxHalfDecay
+// nats would overflow e^{|G - a|} in fp32 / bf16; such a chunk raises
+// ERR_DECAY_RANGE (the token-recurrent algorithm has no such limit).
+constexpr float kMaxHalfDecay = 80.f;
+
 template <class Ly, int VCOLS>
 __device__ __forceinline__ void prep_chunk(uint32_t sb, int cl, const __nv_bfloat16 *beta_t0,
                                            int H, float *s_gpart, float *s_beta, float *s_tot,
-                                           float *s_anc, int tid) {
+                                           float *s_anc, int tid, uint32_t *err) {
   const int cq = tid & 15, rg = tid >> 4;
   const uint32_t okq = (cq >> 3) * 16384, og = Ly::kG + (cq >> 3) * 8192;
   float gl[4][8];  // in-group inclusive cumulative decay
@@ -263,6 +268,7 @@ __device__ __forceinline__ void prep_chunk(uint32_t sb, int cl, const __nv_bfloa
     pre[0] = p0.x - a0.x; pre[1] = p0.y - a0.y; pre[2] = p0.z - a0.z; pre[3] = p0.w - a0.w;
     pre[4] = p1.x - a1.x; pre[5] = p1.y - a1.y; pre[6] = p1.z - a1.z; pre[7] = p1.w - a1.w;
   }
+  int out_of_range = 0;
 #pragma unroll
   for (int rr = 0; rr < 4; ++rr) {
     const int r = 4 * rg + rr;
@@ -276,6 +282,7 @@ __device__ __forceinline__ void prep_chunk(uint32_t sb, int cl, const __nv_bfloa
       for (int j = 0; j < 4; ++j) {
         const float x0 = pre[2 * j] + gl[rr][2 * j];  // G_r - a
         const float x1 = pre[2 * j + 1] + gl[rr][2 * j + 1];
+        out_of_range |= fabsf(x0) > kMaxHalfDecay || fabsf(x1) > kMaxHalfDecay;
         const float e0 = __expf(x0), e1 = __expf(x1);
         const float f0 = __expf(-x0), f1 = __expf(-x1);
         const float k0 = bf16lo(kv[j]), k1 = bf16hi(kv[j]);
@@ -290,7 +297,7 @@ __device__ __forceinline__ void prep_chunk(uint32_t sb, int cl, const __nv_bfloa
     st_shared_v4(sb + og + ck, km[0], km[1], km[2], km[3]);
   }
   fence_async_smem();
-  __syncthreads();
+  if (__syncthreads_or(out_of_range) && tid == 0) raise_error(err, ERR_DECAY_RANGE);
 }
 
 // MMA1: [K+; Q+] K-^T -> d (64 columns: rows 0..63 A-raw, rows 64..127 Q+K-^T).
@@ -488,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------------------------ prep
     prep_chunk<Ly, DV>(sb, cl, a.beta + (int64_t)t0 * H + h, H, s_gpart, s_beta, s_tot, s_anc,
-                       tid);
+                       tid, a.err);
 
     // ------------------------------------------------------------ MMA1
     if (tid == 0) {
@@ -840,7 +847,7 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     const uint32_t sb = sbase + st * Ly::kStage;
 
     prep_chunk<Ly, 128>(sb, cl, a.c.beta + (int64_t)t0 * H + h, H, s_gpart, s_beta, s_tot, s_anc,
-                        tid);
+                        tid, a.c.err);
     if (tid == 0) {
       issue_mma1<Ly>(tmem + 256, sb);
       mma_commit(bar_mma);

@@ -7,6 +7,10 @@
 //   [.., +align(B*4))        int32 order[B]: sequences, longest first
 //   [.., +align(n_slots*H*4*4)) uint32 claims: epoch stamps that detect two
 //                            sequences of one call writing the same state
+//   when B*H <= kCoopMaxUnits, the cooperative prefill's section:
+//   [.., +256)               uint32 ticket, abort word, longest sequence in chunks
+//   [.., +align(B*H*4*16))   u64 ready[B*H][4], consumed[B*H][4] flags
+//   [.., +B*H*4*92160)       package ring, 4 chunk packages per (sequence, head)
 #pragma once
 
 #include <cuda_bf16.h>
@@ -23,6 +27,7 @@ enum ErrBits : uint32_t {
   ERR_BAD_CU = 4u,
   ERR_SNAP_CAPACITY = 8u,
   ERR_TIMEOUT = 16u,
+  ERR_DECAY_RANGE = 32u,
 };
 
 struct SeqMeta {

@@ -205,7 +205,10 @@ int64_t kda_snapshot_count(const int32_t *cu_seqlens_host, int32_t B, int32_t sn
  * last call to this function, and clears the record.  If detail is not NULL
  * it receives the raw error bits (1 slot out of range, 2 duplicate slot or a
  * source that is another sequence's destination, 4 bad cu_seqlens, 8 snapshot
- * buffer too small, 16 wait timeout). */
+ * buffer too small, 16 wait timeout, 32 a channel's decay within half a
+ * 64-token chunk exceeded 80 nats, beyond the chunked algorithm's exponent
+ * range: its results are not reliable, run that batch with
+ * KDA_ALGO_RECURRENT). */
 kda_status kda_device_status(const kda_args *a, uint32_t *detail);
 
 /* Human-readable name of a status code (static string). */

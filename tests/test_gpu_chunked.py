@@ -244,3 +244,34 @@ def test_prefill_1m_full_sampled():
     assert oracle.rel_l2(out[:, h, lo:hi].float().cpu().numpy(), res.out[:, 0, lo:hi]) <= TOL["bf16"]
     assert oracle.rel_l2(snaps[:, h, :, lo:hi].cpu().numpy(), res.snaps[:, 0, :, lo:hi]) <= TOL["bf16"]
     assert oracle.rel_l2(pool[0, h, :, lo:hi].cpu().numpy(), res.final[0, 0, :, lo:hi]) <= TOL["bf16"]
+
+
+@MODES
+def test_chunked_flags_decay_beyond_its_range(mode):
+    """Two g = -60 gates of one channel within 32 tokens push the chunked
+    algorithm's scaled operands beyond fp32 range: the call reports it (error
+    bit 32) instead of returning silent garbage, and the token-recurrent
+    algorithm computes the same batch to tolerance."""
+    b = _case([96], 2, 1, [[-1, 0]])
+    b.g = b.g.clone()
+    b.g[10, 0, 5] = -60.0
+    b.g[20, 0, 5] = -60.0
+    _, _, _, (st, bits) = gpu_prefill(b, 0, algo=mode)
+    assert st == kda.KDA_ERR_DEVICE_CHECK and bits & 32
+    out, pool, _, (st, bits) = gpu_prefill(b, 0, algo=kda.KDA_ALGO_RECURRENT)
+    assert st == kda.KDA_OK and bits == 0
+    ro, rpool, _ = oracle_prefill(b, 0)
+    assert rel(out, ro) <= TOL["bf16"] and rel(pool[0], rpool[0]) <= TOL["bf16"]
+
+
+@MODES
+def test_chunked_single_large_gate_is_exact(mode):
+    """One g = -60 gate (the state of that channel is wiped at one token) stays
+    inside the chunked algorithm's range: no flag, no inf/NaN, oracle parity."""
+    b = _case([200], 2, 1, [[-1, 0]])
+    b.g = b.g.clone()
+    b.g[70, 1, 3] = -60.0
+    out, pool, snaps, (st, bits) = gpu_prefill(b, 64, algo=mode)
+    assert st == kda.KDA_OK and bits == 0
+    assert torch.isfinite(out.float()).all() and torch.isfinite(pool).all()
+    _check(b, 64, out, pool, snaps)
