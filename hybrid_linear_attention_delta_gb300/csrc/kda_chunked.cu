@@ -70,10 +70,13 @@ struct Layout {
   static constexpr uint32_t kBeta = 64;                // f32[64]
   static constexpr uint32_t kTot = kBeta + 256;        // f32[128] G_C (chunk decay)
   static constexpr uint32_t kAnc = kTot + 512;         // f32[128] a (anchor decay)
-  static constexpr uint32_t kSeqs = kAnc + 512;        // int2[64] (tok0, len) per sequence
+  static constexpr uint32_t kEa = kAnc + 512;          // f32[128] e^{a} (cooperative producer)
+  static constexpr uint32_t kCke = kEa + 512;          // f32[128] e^{G_C - a} (cooperative producer)
+  static constexpr uint32_t kSeqs = kCke + 512;        // int2[64] (tok0, len) per sequence
   static constexpr uint32_t kBytes = kMisc + kSeqs + 512;
-  // prep scratch: per 4-row group decay sums f32[16][128], inside the W buffer
-  static constexpr uint32_t kGpart = kW;
+  // prep scratch: per 4-row group decay sums f32[16][128], in the T rows of
+  // [T; M] (8 KiB; the solve rewrites them and zeroes T's upper blocks)
+  static constexpr uint32_t kGpart = kTM;
   // solve scratch (fp32): L (swizzled 64x64) in the W buffer, X^T in the U
   // buffer, diagonal blocks of X and Y^T in kScr
   static constexpr uint32_t kXd = kScr;                 // f32[4][16][16]
@@ -167,11 +170,18 @@ __device__ __forceinline__ void solve_level(const float *L, float *XT, const flo
 //    one output element per thread and pass, each a 16-term float4 dot
 //    product per block (A rows from L, X columns from X^T, X_aa rows from
 //    Xd, Y columns from Y^T).
-// T is written as bf16 into rows 0..63 of the K-major [T; M] operand; its
-// blocks above the diagonal stay zero from the start of the kernel.
+// T is written as bf16 into rows 0..63 of the K-major [T; M] operand; the
+// threads without a diagonal column zero its blocks above the diagonal (the
+// rows also hold the decay prefix scratch of the chunk's preparation).
 __device__ __forceinline__ void solve_T(const float *L, float *XT, float *Xd, float *YT,
                                         const float *beta, uint8_t *tm, int tid) {
-  if (tid < 64) {  // one column of one diagonal block per thread
+  if (tid >= 64) {  // zero T's upper blocks: row r of block rb, chunks 2 (rb + 1) .. 7
+    const int e = tid - 64;  // 192 chunks: 16 rows x 6, 16 x 4, 16 x 2
+    const int rb = e < 96 ? 0 : (e < 160 ? 1 : 2);
+    const int base_e = rb == 0 ? 0 : (rb == 1 ? 96 : 160);
+    const int per = 6 - 2 * rb, r = 16 * rb + (e - base_e) / per, c = 2 * (rb + 1) + (e - base_e) % per;
+    *reinterpret_cast<uint4 *>(tm + sw128_chunk(r, c)) = make_uint4(0, 0, 0, 0);
+  } else {  // one column of one diagonal block per thread
     const int a = tid >> 4, jj = tid & 15, base = 16 * a;
     float x[16];
 #pragma unroll
@@ -210,7 +220,8 @@ __device__ __forceinline__ void solve_T(const float *L, float *XT, float *Xd, fl
 
 // Decay-scaled operands of one chunk, in place in its stage: K+ over k, Q+
 // over q, K- over g; per channel the anchor a (s_anc) and the chunk decay G_C
-// (s_tot); beta (s_beta, zero past the end); v rows past a ragged end zeroed.
+// (s_tot); beta (s_beta, from beta_r of threads 0..63, which load_beta
+// fetched before the chunk's tiles landed); v rows past a ragged end zeroed.
 // Thread: channels [8 cq, 8 cq + 8) x rows [4 rg, 4 rg + 4), 16-byte accesses.
 // Ends with the operand writes fenced for the tensor cores and a barrier.
 // A channel whose decay within one half of the chunk exceeds kMaxHalfDecay
@@ -218,10 +229,16 @@ __device__ __forceinline__ void solve_T(const float *L, float *XT, float *Xd, fl
 // ERR_DECAY_RANGE (the token-recurrent algorithm has no such limit).
 constexpr float kMaxHalfDecay = 80.f;
 
+// beta of row tid of a chunk (threads 0..63; zero past the chunk's end), read
+// early so that its global-memory latency overlaps the wait for the tiles
+__device__ __forceinline__ float load_beta(const __nv_bfloat16 *beta_t0, int H, int cl, int tid) {
+  return tid < cl ? __bfloat162float(beta_t0[(int64_t)tid * H]) : 0.f;
+}
+
 template <class Ly, int VCOLS>
-__device__ __forceinline__ void prep_chunk(uint32_t sb, int cl, const __nv_bfloat16 *beta_t0,
-                                           int H, float *s_gpart, float *s_beta, float *s_tot,
-                                           float *s_anc, int tid, uint32_t *err) {
+__device__ __forceinline__ void prep_chunk(uint32_t sb, int cl, float beta_r, float *s_gpart,
+                                           float *s_beta, float *s_tot, float *s_anc, int tid,
+                                           uint32_t *err) {
   const int cq = tid & 15, rg = tid >> 4;
   const uint32_t okq = (cq >> 3) * 16384, og = Ly::kG + (cq >> 3) * 8192;
   float gl[4][8];  // in-group inclusive cumulative decay
@@ -240,7 +257,7 @@ __device__ __forceinline__ void prep_chunk(uint32_t sb, int cl, const __nv_bfloa
   float4 *gp = reinterpret_cast<float4 *>(s_gpart + rg * 128 + 8 * cq);
   gp[0] = make_float4(gl[3][0], gl[3][1], gl[3][2], gl[3][3]);
   gp[1] = make_float4(gl[3][4], gl[3][5], gl[3][6], gl[3][7]);
-  if (tid < 64) s_beta[tid] = tid < cl ? __bfloat162float(beta_t0[(int64_t)tid * H]) : 0.f;
+  if (tid < 64) s_beta[tid] = beta_r;
   if (cl < kC) {  // ragged tail: zero the v rows past the sequence end
     for (int e = tid; e < (kC - cl) * (VCOLS / 8); e += kThreads) {
       const int r = cl + e / (VCOLS / 8), chk = e % (VCOLS / 8);
@@ -364,16 +381,13 @@ __device__ __forceinline__ void extract_w(uint32_t lane_base, int quarter, int c
                                           uint32_t w) {
   if (quarter >= 2) return;
   const int r = quarter * 32 + lane;
+  float v[64];
+  tmem_ld64(lane_base + colhalf * 64, v);
 #pragma unroll
-  for (int p = 0; p < 2; ++p) {
-    float v[32];
-    tmem_ld32(lane_base + colhalf * 64 + p * 32, v);
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4)
-      st_shared_v4(w + colhalf * 8192 + sw128_chunk(r, p * 4 + q4),
-                   pack_bf16x2(v[q4 * 8], v[q4 * 8 + 1]), pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]),
-                   pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]), pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]));
-  }
+  for (int q8 = 0; q8 < 8; ++q8)
+    st_shared_v4(w + colhalf * 8192 + sw128_chunk(r, q8), pack_bf16x2(v[q8 * 8], v[q8 * 8 + 1]),
+                 pack_bf16x2(v[q8 * 8 + 2], v[q8 * 8 + 3]), pack_bf16x2(v[q8 * 8 + 4], v[q8 * 8 + 5]),
+                 pack_bf16x2(v[q8 * 8 + 6], v[q8 * 8 + 7]));
 }
 
 template <int DV>
@@ -484,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sb = sbase + st * Ly::kStage;
     const int t0 = m.tok0 + n * kC;
     const int cl = min(kC, m.len - n * kC);
+    const float beta_n = tid < 64 ? load_beta(a.beta + (int64_t)t0 * H + h, H, cl, tid) : 0.f;
 
     if (!cta_wait(bar_tma0 + 8 * st, (n >> 1) & 1)) { aborted = true; break; }
     tma_pending[st] = false;
@@ -494,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------ prep
-    prep_chunk<Ly, DV>(sb, cl, a.beta + (int64_t)t0 * H + h, H, s_gpart, s_beta, s_tot, s_anc,
+    prep_chunk<Ly, DV>(sb, cl, beta_n, s_gpart, s_beta, s_tot, s_anc,
                        tid, a.err);
 
     // ------------------------------------------------------------ MMA1
@@ -695,26 +710,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 32 bits and the chunk number + 1 below; every wait is bounded and an abort
 // word stops all CTAs after a timeout.
 //
-// With P = K-^T W and Q~ = Q+ - M W (computed by the producer), and
-// S' = Diag(e^{a}) S (bf16 operand), the single-CTA kernel's update becomes
-//     S_next = Diag(e^{G_C}) S + Diag(e^{G_C - a}) (K-^T U~ - P S')
-//     O      = Q~ S' + M U~
-// (U = U~ - W S' expanded), so the state's critical path per chunk is one
-// MMA group of the chain CTA.
+// With U = U~ - W S' expanded (S' = Diag(e^{a}) S), the single-CTA kernel's
+// update is
+//     S_next = Diag(e^{G_C}) S + Diag(e^{G_C - a}) (K-^T U~ - P S'),  P = K-^T W
+//     O      = Q~ S' + M U~,                                          Q~ = Q+ - M W.
+// The producer folds the per-channel factors into its operands,
+//     K^ = K- Diag(e^{G_C - a})            (= K Diag(e^{G_C - G_r}) per row: at most |K|)
+//     P^ = Diag(e^{G_C - a}) P Diag(e^{a}) (= K^^T (W Diag(e^{a})), from an MMA on K^)
+//     Q^ = Q~ Diag(e^{a}),
+// so that with the state itself as the bf16 operand
+//     S_next = Diag(e^{G_C}) S + K^^T U~ - P^ S,    O = Q^ S + M U~,
+// and the chain CTA works on the transposed state: S^T (bf16, in TMEM) is the
+// A operand of  acc^T = U~^T K^ - S^T P^^T  and  O^T = S^T Q^^T + U~^T M^T.
+// Only the S-dependent half of each (8 MMAs of K = 16) waits for the state.
 
 // package layout (bytes); each operand in the shared-memory layout the chain
 // CTA feeds to its MMAs, so packages are copied verbatim
-constexpr uint32_t kPkP = 0;        // P [128 i][128 j] bf16, K-major, 2 halves x 16 KiB
-constexpr uint32_t kPkKm = 32768;   // K- [64 tok][128 ch] bf16, 2 halves x 8 KiB
+constexpr uint32_t kPkP = 0;        // -P^ [128 i][128 c] bf16, K-major, 2 halves x 16 KiB
+constexpr uint32_t kPkKm = 32768;   // K^ [64 tok][128 ch] bf16, 2 halves x 8 KiB
 constexpr uint32_t kPkU = 49152;    // U~ [64 tok][128 dv] bf16, 2 halves x 8 KiB
-constexpr uint32_t kPkQ = 65536;    // Q~ [64 tok][128 ch] bf16, K-major, 2 halves x 8 KiB
+constexpr uint32_t kPkQ = 65536;    // Q^ [64 tok][128 ch] bf16, K-major, 2 halves x 8 KiB
 constexpr uint32_t kPkM = 81920;    // M [64 tok][64 tok] bf16, K-major, 8 KiB
-constexpr uint32_t kPkDec = 90112;  // f32 e^{G_C}[128], e^{G_C - a}[128], e^{a}[128]
+constexpr uint32_t kPkDec = 90112;  // f32 e^{G_C}[128]
 static_assert(kPkDec + 1536 <= kCoopPkgBytes && kCoopPkgBytes % 1024 == 0, "package layout");
-// chain CTA shared memory: two package stages, S' (2 halves x 16 KiB), misc
-constexpr uint32_t kChS = 2 * (uint32_t)kCoopPkgBytes;
-constexpr uint32_t kChMisc = kChS + 32768;
-constexpr uint32_t kChBytes = kChMisc + 64;
+// a package is fetched as kPkPieces bulk copies of kPkPiece bytes
+constexpr uint32_t kPkPieces = 5, kPkPiece = (uint32_t)kCoopPkgBytes / kPkPieces;
+static_assert(kPkPiece % 16 == 0 && kPkPiece * kPkPieces == kCoopPkgBytes, "bulk copy pieces");
+// chain CTA shared memory: two package stages, two output staging tiles
+// ([64 tok][128 dv] bf16 each, stored with one TMA box), mbarriers, TMEM slot
+constexpr uint32_t kChO = 2 * (uint32_t)kCoopPkgBytes;
+constexpr uint32_t kChMisc = kChO + 2 * 16384;
+constexpr uint32_t kChBytes = kChMisc + 128;
 constexpr uint32_t kCoopSmem =
     Layout<128>::kBytes > kChBytes ? Layout<128>::kBytes : kChBytes;
 
@@ -753,10 +779,6 @@ __device__ __forceinline__ uint4 pack8(const float *v) {
                     pack_bf16x2(v[6], v[7]));
 }
 
-__device__ __forceinline__ void copy16(uint8_t *dst, const uint8_t *src, int bytes, int tid) {
-  for (int e = tid; e < bytes / 16; e += kThreads)
-    reinterpret_cast<uint4 *>(dst)[e] = reinterpret_cast<const uint4 *>(src)[e];
-}
 
 // Producer role: prepares chunks of any pair, in ticket order.
 __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUtensorMap *tm_k,
@@ -772,6 +794,8 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
   float *s_beta = reinterpret_cast<float *>(misc + Ly::kBeta);
   float *s_tot = reinterpret_cast<float *>(misc + Ly::kTot);
   float *s_anc = reinterpret_cast<float *>(misc + Ly::kAnc);
+  float *s_ea = reinterpret_cast<float *>(misc + Ly::kEa);
+  float *s_cke = reinterpret_cast<float *>(misc + Ly::kCke);
   float *s_gpart = reinterpret_cast<float *>(smem + Ly::kGpart);
   int2 *s_seq = reinterpret_cast<int2 *>(misc + Ly::kSeqs);  // (tok0, len or 0) per sequence
   volatile int *s_item = reinterpret_cast<volatile int *>(misc + 32);
@@ -779,6 +803,12 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
   for (int r = tid; r < units / H; r += kThreads) {
     const SeqMeta m = a.c.meta[a.c.order[r]];
     s_seq[r] = make_int2(m.tok0, m.ok ? m.len : 0);
+  }
+  if (tid == 0) {
+    prefetch_tmap(tm_q);
+    prefetch_tmap(tm_k);
+    prefetch_tmap(tm_v);
+    prefetch_tmap(tm_g);
   }
   if (tid == 0) {
     mbar_init(bar_tma0, 1);
@@ -794,14 +824,17 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
   const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
   const int total = (int)a.hdr[2] * units;
 
-  auto take = [&]() -> int {  // thread 0: next ticket that names a real chunk, or -1
-    for (;;) {
-      if (*reinterpret_cast<volatile uint32_t *>(a.hdr + 1)) return -1;
-      const int t = (int)atomicAdd(a.hdr, 1u);
-      if (t >= total) return -1;
-      if ((t / units) * kC < s_seq[(t % units) / H].y) return t;
-    }
+  // Tickets come from a global counter (chunk index major).  A producer
+  // works through its tickets in increasing order and a ticket only ever
+  // waits for smaller ones, so the smallest unfinished ticket can always
+  // proceed.  take_from(t) validates a raw ticket, drawing again past
+  // chunks beyond a sequence's end.
+  auto valid = [&](int t) { return (t / units) * kC < s_seq[(t % units) / H].y; };
+  auto take_from = [&](int t) -> int {  // thread 0
+    while (t < total && !valid(t)) t = (int)atomicAdd(a.hdr, 1u);
+    return t < total ? t : -1;
   };
+  auto take = [&]() -> int { return take_from((int)atomicAdd(a.hdr, 1u)); };
   auto issue = [&](int t, int st) {  // thread 0: TMA loads of chunk t into stage st
     const int u = t % units, h = u % H;
     const uint32_t sb = sbase + st * Ly::kStage, bar = bar_tma0 + 8 * st;
@@ -817,46 +850,60 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     tma_load_2d(sb + Ly::kG + 8192, tm_g, h * kDK + 64, y, bar);
   };
 
-  // tickets run one chunk ahead of the loads, which run one chunk ahead of the work
+  // the tiles of a chunk are loaded while the chunk before it is worked on:
+  // each chunk's tiles are requested at the end of the chunk two before it,
+  // into the stage that chunk used (the first two up front)
   if (tid == 0) {
     const int t0 = take();
     s_item[0] = t0;
     s_item[1] = t0 >= 0 ? take() : -1;
     if (t0 >= 0) issue(t0, 0);
+    if (s_item[1] >= 0) issue(s_item[1], 1);
   }
   __syncthreads();
   int cur = s_item[0], next = s_item[1];
   uint32_t uses[2] = {0, 0}, mma_phase = 0;
-  bool tma_pending[2] = {cur >= 0, false}, mma_pending = false, aborted = false;
+  bool tma_pending[2] = {cur >= 0, next >= 0}, mma_pending = false, aborted = false;
+  // thread 0: the previous package, stored with bulk copies and published
+  // (ready flag) once they are complete, at the next chunk's first MMA
+  bool pend = false;
+  unsigned long long *pend_flag = nullptr, pend_tag = 0, slot_seen = 0;
+  int raw_ticket = 0;  // thread 0: drawn at a chunk's first MMA, validated at its second
   for (int it = 0; cur >= 0; ++it) {
     const int st = it & 1;
-    if (tid == 0) {  // the other stage was released at the end of the previous chunk
-      if (next >= 0) issue(next, st ^ 1);
-      s_item[2] = next >= 0 ? take() : -1;
-    }
-    if (next >= 0) tma_pending[st ^ 1] = true;
+    const int n = cur / units, u = cur % units;
+    const int cl = min(kC, s_seq[u / H].y - n * kC);
+    const uint32_t sb = sbase + st * Ly::kStage;
+    const float beta_n = tid < 64 ? load_beta(a.c.beta + (int64_t)(s_seq[u / H].x + n * kC) * H + u % H,
+                                              H, cl, tid)
+                                   : 0.f;
     if (!cta_wait(bar_tma0 + 8 * st, uses[st] & 1)) { aborted = true; break; }
     ++uses[st];
     tma_pending[st] = false;
-    const int after = s_item[2];
 
-    const int n = cur / units, u = cur % units, h = u % H;
-    const int2 sq = s_seq[u / H];
-    const int t0 = sq.x + n * kC, cl = min(kC, sq.y - n * kC);
-    uint8_t *stage = smem + st * Ly::kStage;
-    const uint32_t sb = sbase + st * Ly::kStage;
-
-    prep_chunk<Ly, 128>(sb, cl, a.c.beta + (int64_t)t0 * H + h, H, s_gpart, s_beta, s_tot, s_anc,
+    prep_chunk<Ly, 128>(sb, cl, beta_n, s_gpart, s_beta, s_tot, s_anc,
                         tid, a.c.err);
     if (tid == 0) {
       issue_mma1<Ly>(tmem + 256, sb);
       mma_commit(bar_mma);
+      raw_ticket = next >= 0 ? (int)atomicAdd(a.hdr, 1u) : total;  // used at MMA2
+      // the previous package's stores are complete: it is published
+      bulk_wait<0>();
+      if (pend) {
+        fence_proxy_async_all();
+        st_release_u64(pend_flag, pend_tag);
+        pend = false;
+      }
     }
     mma_pending = true;
     if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
     mma_phase ^= 1;
     mma_pending = false;
     tc_fence_after();
+    if (tid < 128) {
+      s_ea[tid] = expf(s_anc[tid]);
+      s_cke[tid] = expf(s_tot[tid] - s_anc[tid]);
+    }
     float *Lm = reinterpret_cast<float *>(smem + Ly::kW);
     extract_am(lane_base + 256, quarter, colhalf, lane, s_beta, Lm, sbase + Ly::kTM);
     tc_fence_before();
@@ -864,27 +911,43 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     solve_T(Lm, reinterpret_cast<float *>(smem + Ly::kU),
             reinterpret_cast<float *>(smem + Ly::kXd),
             reinterpret_cast<float *>(smem + Ly::kYt), s_beta, smem + Ly::kTM, tid);
+    for (int e = tid; e < 1024; e += kThreads) {  // K^ = K- Diag(e^{G_C - a}) -> solve scratch
+      const int half = e >> 9, r = (e >> 3) & 63, q = e & 7;
+      const uint32_t off = half * 8192 + r * 128 + q * 16;
+      const float4 *f = reinterpret_cast<const float4 *>(s_cke + half * 64 + 8 * (q ^ (r & 7)));
+      const float4 f0 = f[0], f1 = f[1];
+      const uint4 w = ld_shared_v4(sb + Ly::kG + off);
+      st_shared_v4(sbase + Ly::kScr + off, pack_bf16x2(bf16lo(w.x) * f0.x, bf16hi(w.x) * f0.y),
+                   pack_bf16x2(bf16lo(w.y) * f0.z, bf16hi(w.y) * f0.w),
+                   pack_bf16x2(bf16lo(w.z) * f1.x, bf16hi(w.z) * f1.y),
+                   pack_bf16x2(bf16lo(w.w) * f1.z, bf16hi(w.w) * f1.w));
+    }
     fence_async_smem();
     __syncthreads();
     if (tid == 0) {
       issue_mma2<Ly, 128>(tmem, sbase + Ly::kTM, sb);
       mma_commit(bar_mma);
+      s_item[2] = next >= 0 ? take_from(raw_ticket) : -1;
+      // peek at this chunk's ring slot early; it is waited for only if the
+      // pair's chain CTA had not yet copied out the chunk that used it before
+      slot_seen = n >= kCoopRing ? ld_relaxed_u64(a.consumed + u * kCoopRing + n % kCoopRing) : 0;
     }
     mma_pending = true;
     if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
     mma_phase ^= 1;
     mma_pending = false;
+    const int after = s_item[2];
     tc_fence_after();
     extract_w(lane_base, quarter, colhalf, lane, sbase + Ly::kW);
     tc_fence_before();
     fence_async_smem();
     __syncthreads();
-    if (tid == 0) {  // P = K-^T W -> tmem[256, 384); M W -> tmem[384, 512)
+    if (tid == 0) {  // P^ = K^^T W -> tmem[256, 384); M W -> tmem[384, 512)
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t bd = sw128_desc(sbase + Ly::kW + kk * 2048, 8192, 1024);
-        mma_bf16(tmem + 256, sw128_desc(sb + Ly::kG + kk * 2048, 8192, 1024), bd,
+        mma_bf16(tmem + 256, sw128_desc(sbase + Ly::kScr + kk * 2048, 8192, 1024), bd,
                  idesc_bf16(128, 128, 1, 1), kk > 0);
         mma_bf16(tmem + 384, sw128_desc(sbase + Ly::kTM + 8192 + kk * 32, 16, 1024), bd,
                  idesc_bf16(128, 128, 0, 1), kk > 0);
@@ -893,93 +956,105 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     }
     mma_pending = true;
 
-    // The package is staged in shared memory in its final layout, then copied
-    // out with coalesced stores: U~ -> the U buffer (now free); P -> the v slot
-    // (K half 0) and the solve scratch (K half 1); Q~ -> the W buffer once the
-    // MMAs reading W are done; the decays -> the k slot; K- and M stay where
-    // they are.
+    // The package is staged in shared memory in its final layout, outside
+    // both input stages, then written out with bulk copies: K^ in the solve
+    // scratch, U~ in the U buffer, -P^ in the S0 region, Q^ in the W buffer
+    // once the MMAs reading W are done, M where the solve left it, e^{G_C}
+    // in the e^{G_C - a} vector.
     if (quarter < 2) {  // U~: rows 0..63 of tmem[128, 256)
       const int r = quarter * 32 + lane;
+      float v[64];
+      tmem_ld64(lane_base + 128 + colhalf * 64, v);
 #pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        float v[32];
-        tmem_ld32(lane_base + 128 + colhalf * 64 + p * 32, v);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint4 w = pack8(v + 8 * q4);
-          st_shared_v4(sbase + Ly::kU + colhalf * 8192 + sw128_chunk(r, p * 4 + q4), w.x, w.y, w.z,
-                       w.w);
-        }
+      for (int q8 = 0; q8 < 8; ++q8) {
+        const uint4 w = pack8(v + 8 * q8);
+        st_shared_v4(sbase + Ly::kU + colhalf * 8192 + sw128_chunk(r, q8), w.x, w.y, w.z, w.w);
       }
     }
     if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
     mma_phase ^= 1;
     mma_pending = false;
     tc_fence_after();
-    {  // P: row i (all 128), K half colhalf
+    {  // -P^ = -(K^^T W) Diag(e^{a}): row i (all 128), K half colhalf
       const int i = quarter * 32 + lane;
-      const uint32_t dst = colhalf ? sbase + Ly::kScr : sb + Ly::kV;
+      const uint32_t dst = sbase + Ly::kS0 + colhalf * 16384;
+      float v[64];
+      tmem_ld64(lane_base + 256 + colhalf * 64, v);
+      const float4 *ea = reinterpret_cast<const float4 *>(s_ea + colhalf * 64);
 #pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        float v[32];
-        tmem_ld32(lane_base + 256 + colhalf * 64 + p * 32, v);
+      for (int q4 = 0; q4 < 16; ++q4) {
+        const float4 e4 = ea[q4];
+        v[4 * q4] *= -e4.x;
+        v[4 * q4 + 1] *= -e4.y;
+        v[4 * q4 + 2] *= -e4.z;
+        v[4 * q4 + 3] *= -e4.w;
+      }
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint4 w = pack8(v + 8 * q4);
-          st_shared_v4(dst + sw128_chunk(i, p * 4 + q4), w.x, w.y, w.z, w.w);
-        }
+      for (int q8 = 0; q8 < 8; ++q8) {
+        const uint4 w = pack8(v + 8 * q8);
+        st_shared_v4(dst + sw128_chunk(i, q8), w.x, w.y, w.z, w.w);
       }
     }
     if (quarter < 2) {  // Q~ = Q+ - M W (rows 0..63)
       const int r = quarter * 32 + lane;
+      float v[64];
+      tmem_ld64(lane_base + 384 + colhalf * 64, v);
 #pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        float v[32];
-        tmem_ld32(lane_base + 384 + colhalf * 64 + p * 32, v);
+      for (int q8 = 0; q8 < 8; ++q8) {
+        const uint4 qw = ld_shared_v4(sb + Ly::kQ + colhalf * 16384 + sw128_chunk(r, q8));
+        const uint32_t qv[4] = {qw.x, qw.y, qw.z, qw.w};
+        const float4 *ea = reinterpret_cast<const float4 *>(s_ea + colhalf * 64 + 8 * q8);
+        const float4 e0 = ea[0], e1 = ea[1];
+        const float es[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+        float d[8];  // Q^ = (Q+ - M W) Diag(e^{a}), over W (its MMAs are done)
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint4 qw = ld_shared_v4(sb + Ly::kQ + colhalf * 16384 + sw128_chunk(r, p * 4 + q4));
-          const uint32_t qv[4] = {qw.x, qw.y, qw.z, qw.w};
-          float d[8];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            d[2 * j] = bf16lo(qv[j]) - v[8 * q4 + 2 * j];
-            d[2 * j + 1] = bf16hi(qv[j]) - v[8 * q4 + 2 * j + 1];
-          }
-          const uint4 w = pack8(d);
-          st_shared_v4(sbase + Ly::kW + colhalf * 8192 + sw128_chunk(r, p * 4 + q4), w.x, w.y, w.z,
-                       w.w);
+        for (int j = 0; j < 4; ++j) {
+          d[2 * j] = (bf16lo(qv[j]) - v[8 * q8 + 2 * j]) * es[2 * j];
+          d[2 * j + 1] = (bf16hi(qv[j]) - v[8 * q8 + 2 * j + 1]) * es[2 * j + 1];
         }
+        const uint4 w = pack8(d);
+        st_shared_v4(sbase + Ly::kW + colhalf * 8192 + sw128_chunk(r, q8), w.x, w.y, w.z, w.w);
       }
     }
-    if (tid < 128) {
-      float *dec = reinterpret_cast<float *>(stage);
-      dec[tid] = expf(s_tot[tid]);
-      dec[128 + tid] = expf(s_tot[tid] - s_anc[tid]);
-      dec[256 + tid] = expf(s_anc[tid]);
-    }
+    if (tid < 128) s_cke[tid] = expf(s_tot[tid]);  // e^{G_C} for the package
     tc_fence_before();
+    fence_async_smem();  // the staged package, for the bulk stores
     const int slot = n % kCoopRing;
     {
       int ok = 1;
-      if (tid == 0 && n >= kCoopRing)
+      __syncthreads();
+      if (tid == 0 && n >= kCoopRing && slot_seen < coop_tag(a.epoch, n - kCoopRing))
         ok = coop_flag_wait(a.consumed + u * kCoopRing + slot, coop_tag(a.epoch, n - kCoopRing),
                             a.hdr + 1);
+      if (tid == 0 && after >= 0) issue(after, st);  // before the stores, on the same engine
+      // the package, piece by piece from where it was staged (W, U, solve
+      // scratch, S0 region, M, e^{G_C}); these are first overwritten after
+      // the next chunk's first MMA, where thread 0 waits for the stores
+      if (tid == 0 && ok) {
+        uint8_t *pk = a.ring + ((size_t)u * kCoopRing + slot) * kCoopPkgBytes;
+        bulk_s2g(pk + kPkP, sbase + Ly::kS0, 32768);
+        bulk_s2g(pk + kPkKm, sbase + Ly::kScr, 16384);
+        bulk_s2g(pk + kPkU, sbase + Ly::kU, 16384);
+        bulk_s2g(pk + kPkQ, sbase + Ly::kW, 16384);
+        bulk_s2g(pk + kPkM, sbase + Ly::kTM + 8192, 8192);
+        bulk_s2g(pk + kPkDec, sbase + Ly::kMisc + Ly::kCke, 512);
+        bulk_commit();
+        pend = true;
+        pend_flag = a.ready + u * kCoopRing + slot;
+        pend_tag = coop_tag(a.epoch, n);
+      }
+      if (after >= 0) tma_pending[st] = true;
       if (__syncthreads_or(!ok)) { aborted = true; break; }
     }
-    uint8_t *pk = a.ring + ((size_t)u * kCoopRing + slot) * kCoopPkgBytes;
-    copy16(pk + kPkP, stage + Ly::kV, 16384, tid);
-    copy16(pk + kPkP + 16384, smem + Ly::kScr, 16384, tid);
-    copy16(pk + kPkKm, stage + Ly::kG, 16384, tid);
-    copy16(pk + kPkU, smem + Ly::kU, 16384, tid);
-    copy16(pk + kPkQ, smem + Ly::kW, 16384, tid);
-    copy16(pk + kPkM, smem + Ly::kTM + 8192, 8192, tid);
-    copy16(pk + kPkDec, stage, 1536, tid);
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) st_release_u64(a.ready + u * kCoopRing + slot, coop_tag(a.epoch, n));
     cur = next;
     next = after;
+  }
+  if (tid == 0) {  // the last package: complete, then published (unless aborted)
+    bulk_wait<0>();
+    if (pend && !aborted) {
+      fence_proxy_async_all();
+      st_release_u64(pend_flag, pend_tag);
+    }
   }
   if (aborted) {
     if (tid == 0) coop_abort(a);
@@ -992,206 +1067,271 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Chain role: carries the state of pair u through its packages.  Per chunk n:
-// issue its MMAs, then (while they run) retire chunk n-1's outputs and start
-// copying package n+1, then update the state.
-__device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u) {
+// Chain role: carries the state of pair u through its packages, with its warps
+// specialised:
+//   warps 0-3 (state): thread j holds column j of S (row j of S^T) for all 128
+//     channels in fp32 registers.  Per chunk n it stores bf16(S^T) into TMEM
+//     buffer n & 1 (the A operand of the chunk's state-dependent MMAs),
+//     retires chunk n-1's outputs while those MMAs run, then applies
+//     S <- Diag(e^{G_C}) S + acc and writes snapshots.
+//   warp 4, one lane (MMA): per chunk, acc^T = U~^T K^ and O^T = U~^T M^T as
+//     soon as the package has landed, then acc^T -= S^T P^^T (commit: acc
+//     ready) and O^T += S^T Q^^T (commit: outputs ready, stage free).
+//   warp 5, one lane (loader): waits until package n is in the ring, fetches
+//     it into stage n & 1 with bulk copies, and hands the ring slot back.
+// TMEM columns: acc^T [0, 128); O^T[b] [128 + 64 b, +64); S^T[b] as bf16
+// pairs [256 + 64 b, +64).  Every wait is bounded; a role that gives up
+// raises the abort word and leaves its loop, and the others then time out.
+// Warp-uniform bounded wait: every lane polls, and all lanes give up together
+// if any did, so the warp stays converged for the tcgen05 loads and stores.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
+// the four state warps of a chain CTA
+__device__ __forceinline__ void state_warps_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArgs &a, int u) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, colhalf = warp >> 2;
   const uint32_t sbase = smem_u32(smem);
   const int H = a.c.H, h = u % H, dv = a.c.dv;
   const SeqMeta m = a.c.meta[a.c.order[u / H]];
-  uint8_t *misc = smem + kChMisc;
-  const uint32_t bar_s = sbase + kChMisc, bar_o0 = bar_s + 8;  // bar_o for buffers 0, 1
+  // mbarriers: full[2] (package landed), empty[2] (stage free: MMAs done and
+  // the state warps read its decays), sready[2] (S^T stored), accf / acce
+  // (acc^T ready / read), of[2] / oe[2] (O^T ready / read), drain
+  const uint32_t bars = sbase + kChMisc;
+  const uint32_t full0 = bars, empty0 = bars + 16, sready0 = bars + 32, accf = bars + 48,
+                 acce = bars + 56, of0 = bars + 64, oe0 = bars + 80, drain = bars + 96;
   if (tid == 0) {
-    mbar_init(bar_s, 1);
-    mbar_init(bar_o0, 1);
-    mbar_init(bar_o0 + 8, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1 + 4);
+      mbar_init(sready0 + 8 * s, 4);
+      mbar_init(of0 + 8 * s, 1);
+      mbar_init(oe0 + 8 * s, 4);
+    }
+    mbar_init(accf, 1);
+    mbar_init(acce, 4);
+    mbar_init(drain, 1);
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(sbase + kChMisc + 32, 512);
+  if (warp == 0) tmem_alloc(bars + 112, 512);
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc + 32);
-  const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-  const int c = quarter * 32 + lane, col0 = colhalf * 64;
-
-  float S[64];
-  if (m.ok && m.src >= 0) {
-    const float4 *s0 =
-        reinterpret_cast<const float4 *>(a.c.pool + (((int64_t)m.src * H + h) * kDK + c) * dv + col0);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float4 t = s0[j];
-      S[4 * j] = t.x; S[4 * j + 1] = t.y; S[4 * j + 2] = t.z; S[4 * j + 3] = t.w;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 64; ++j) S[j] = 0.f;
-  }
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kChMisc + 112);
   const int N = m.ok ? (m.len + kC - 1) / kC : 0;
-  const unsigned long long *ready = a.ready + u * kCoopRing;
-  unsigned long long *consumed = a.consumed + u * kCoopRing;
-  const uint8_t *ring_u = a.ring + (size_t)u * kCoopRing * kCoopPkgBytes;
+  bool failed = false;
 
-  // wait for package n and start copying it into stage n & 1 (all threads)
-  auto fetch = [&](int n) -> bool {
-    int ok = 1;
-    if (tid == 0) ok = coop_flag_wait(ready + n % kCoopRing, coop_tag(a.epoch, n), a.hdr + 1);
-    if (__syncthreads_or(!ok)) return false;
-    const uint8_t *src = ring_u + (size_t)(n % kCoopRing) * kCoopPkgBytes;
-    const uint32_t dst = sbase + (n & 1) * (uint32_t)kCoopPkgBytes;
-    for (int e = tid; e < (int)(kCoopPkgBytes / 16); e += kThreads) cp_async16(dst + 16 * e, src + 16 * e);
-    cp_async_commit();
-    return true;
-  };
-  // outputs of chunk n from output buffer n & 1 (rows 0..63)
-  auto retire = [&](int n) {
-    if (quarter >= 2) return;
-    const int cl = min(kC, m.len - n * kC);
-    __nv_bfloat16 *orow = a.c.out + ((int64_t)(m.tok0 + n * kC + c) * H + h) * dv + col0;
+  if (warp < 4) {
+    const int j = tid;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const int64_t cs = dv;  // stride between channels (rows) of a state
+    float S[kDK];
+    if (m.ok && m.src >= 0) {
+      const float *s0 = a.c.pool + ((int64_t)m.src * H + h) * kDK * dv + j;
 #pragma unroll
-    for (int p = 0; p < 2; ++p) {
-      float v[32];
-      tmem_ld32(lane_base + 128 + 128 * (n & 1) + col0 + p * 32, v);
-      if (c < cl) {
-        uint4 *dst = reinterpret_cast<uint4 *>(orow + p * 32);
+      for (int c = 0; c < kDK; ++c) S[c] = s0[c * cs];
+    } else {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) dst[q4] = pack8(v + 8 * q4);
+      for (int c = 0; c < kDK; ++c) S[c] = 0.f;
+    }
+    // outputs of chunk n from O^T buffer n & 1: token t of the chunk is column t.
+    // A whole chunk goes through staging tile n & 1 and one TMA store; the
+    // ragged last chunk of a sequence is written directly, row by row.
+    auto retire = [&](int n) -> bool {
+      const int b = n & 1;
+      if (!warp_wait(of0 + 8 * b, (n >> 1) & 1)) return false;
+      tc_fence_after();
+      uint32_t v0[32], v1[32];
+      tmem_ld32_async(lane_base + 128 + 64 * b, v0);
+      tmem_ld32_async(lane_base + 128 + 64 * b + 32, v1);
+      tmem_wait_ld();
+      reg_fence(v0);
+      reg_fence(v1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(oe0 + 8 * b);
+      const int cl = min(kC, m.len - n * kC);
+      if (cl == kC) {
+        if (tid == 0) bulk_wait_read<1>();  // chunk n-2's store has read tile b
+        state_warps_sync();
+        uint8_t *stg = smem + kChO + b * 16384 + 2 * j;
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          *reinterpret_cast<__nv_bfloat16 *>(stg + t * 256) = __float2bfloat16_rn(__uint_as_float(v0[t]));
+          *reinterpret_cast<__nv_bfloat16 *>(stg + (t + 32) * 256) =
+              __float2bfloat16_rn(__uint_as_float(v1[t]));
+        }
+        fence_async_smem();
+        state_warps_sync();
+        if (tid == 0) {
+          tma_store_2d(tm_o, sbase + kChO + b * 16384, h * dv, m.tok0 + n * kC);
+          bulk_commit();
+        }
+      } else {
+        const int64_t ts = (int64_t)H * dv;
+        __nv_bfloat16 *o = a.c.out + ((int64_t)(m.tok0 + n * kC) * H + h) * dv + j;
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          if (t < cl) o[t * ts] = __float2bfloat16_rn(__uint_as_float(v0[t]));
+          if (t + 32 < cl) o[(t + 32) * ts] = __float2bfloat16_rn(__uint_as_float(v1[t]));
+        }
+      }
+      return true;
+    };
+    for (int n = 0; n < N; ++n) {
+      const int b = n & 1;
+      // bf16(S^T) -> S^T[b]: column q holds channels 2q (low half) and 2q + 1.
+      // Buffer b was last read by chunk n-2's MMAs, which retire(n-2) waited for.
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        uint32_t r[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) r[q] = pack_bf16x2(S[64 * p + 2 * q], S[64 * p + 2 * q + 1]);
+        tmem_st32(lane_base + 256 + 64 * b + 32 * p, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sready0 + 8 * b);
+      if (n > 0 && !retire(n - 1)) { failed = true; break; }
+      if (!warp_wait(full0 + 8 * b, (n >> 1) & 1) || !warp_wait(accf, n & 1)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      const float4 *egc = reinterpret_cast<const float4 *>(smem + b * kCoopPkgBytes + kPkDec);
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {  // S = Diag(e^{G_C}) S + acc, 64 channels at a time
+        uint32_t v[2][32];
+        tmem_ld32_async(lane_base + 64 * p, v[0]);
+        tmem_ld32_async(lane_base + 64 * p + 32, v[1]);
+        tmem_wait_ld();
+        reg_fence(v[0]);
+        reg_fence(v[1]);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int c = 64 * p + 32 * hh + 4 * q;
+            const float4 e = egc[c / 4];
+            S[c] = fmaf(e.x, S[c], __uint_as_float(v[hh][4 * q]));
+            S[c + 1] = fmaf(e.y, S[c + 1], __uint_as_float(v[hh][4 * q + 1]));
+            S[c + 2] = fmaf(e.z, S[c + 2], __uint_as_float(v[hh][4 * q + 2]));
+            S[c + 3] = fmaf(e.w, S[c + 3], __uint_as_float(v[hh][4 * q + 3]));
+          }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(acce);
+        mbar_arrive(empty0 + 8 * b);
+      }
+      const int cl = min(kC, m.len - n * kC);
+      const int64_t done = (int64_t)n * kC + cl;
+      if (a.c.snap_interval > 0 && done % a.c.snap_interval == 0) {
+        const int64_t s = m.snap_off + done / a.c.snap_interval - 1;
+        if (s < a.c.snaps_capacity) {
+          float *d = a.c.snaps + (s * H + h) * kDK * dv + j;
+#pragma unroll
+          for (int c = 0; c < kDK; ++c) d[c * cs] = S[c];
+        } else if (j == 0) {
+          raise_error(a.c.err, ERR_SNAP_CAPACITY);
+        }
       }
     }
-  };
-
-  bool aborted = false, pend_s = false, pend_o[2] = {false, false};
-  uint32_t ph_s = 0, ph_o[2] = {0, 0};
-  if (N > 0) {
-    if (!fetch(0)) {
-      aborted = true;
-    } else {
-      cp_async_wait<0>();
-      fence_async_smem();
-      __syncthreads();
+    if (!failed && N > 0 && !retire(N - 1)) failed = true;
+    if (!failed && m.ok) {
+      float *d = a.c.pool + ((int64_t)m.dst * H + h) * kDK * dv + j;
+#pragma unroll
+      for (int c = 0; c < kDK; ++c) d[c * cs] = S[c];
     }
-  }
-  for (int n = 0; n < N && !aborted; ++n) {
-    const int st = n & 1;
-    const int cl = min(kC, m.len - n * kC);
-    if (tid == 0) st_release_u64(consumed + n % kCoopRing, coop_tag(a.epoch, n));
-    if (n > 0) {  // chunk n-1's output MMAs still read S'
-      if (!cta_wait(bar_o0 + 8 * (st ^ 1), ph_o[st ^ 1])) { aborted = true; break; }
-      ph_o[st ^ 1] ^= 1;
-      pend_o[st ^ 1] = false;
-      tc_fence_after();
-    }
-    const uint32_t sp = sbase + st * (uint32_t)kCoopPkgBytes;
-    const float *dec = reinterpret_cast<const float *>(smem + st * kCoopPkgBytes + kPkDec);
-    const float egc = dec[c], cke = dec[128 + c], ea = dec[256 + c];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {  // S' = Diag(e^{a}) S (MN-major: row = channel c)
-      float w8[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) w8[t] = ea * S[8 * j + t];
-      const int col = col0 + 8 * j;
-      const uint4 pw = pack8(w8);
-      st_shared_v4(sbase + kChS + (col >> 6) * 16384 + sw128_chunk(c, (col & 63) >> 3), pw.x, pw.y,
-                   pw.z, pw.w);
-    }
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)  // K-^T U~
-        mma_bf16(tmem, sw128_desc(sp + kPkKm + kk * 2048, 8192, 1024),
-                 sw128_desc(sp + kPkU + kk * 2048, 8192, 1024), idesc_bf16(128, 128, 1, 1), kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // -= P S'
-        mma_bf16(tmem, sw128_desc(sp + kPkP + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                 sw128_desc(sbase + kChS + kk * 2048, 16384, 1024), idesc_bf16(128, 128, 0, 1, 1), 1);
-      mma_commit(bar_s);
-      const uint32_t o = tmem + 128 + 128 * st;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // O = Q~ S'
-        mma_bf16(o, sw128_desc(sp + kPkQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
-                 sw128_desc(sbase + kChS + kk * 2048, 16384, 1024), idesc_bf16(128, 128, 0, 1),
-                 kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)  // O += M U~
-        mma_bf16(o, sw128_desc(sp + kPkM + kk * 32, 16, 1024),
-                 sw128_desc(sp + kPkU + kk * 2048, 8192, 1024), idesc_bf16(128, 128, 0, 1), 1);
-      mma_commit(bar_o0 + 8 * st);
-    }
-    pend_s = pend_o[st] = true;
-    // under chunk n's MMAs: chunk n-1's outputs, then package n+1 into the
-    // stage chunk n-1 used (all of its MMAs are done)
-    if (n > 0) retire(n - 1);
-    if (n + 1 < N && !fetch(n + 1)) { aborted = true; break; }
-    if (!cta_wait(bar_s, ph_s)) { aborted = true; break; }
-    ph_s ^= 1;
-    pend_s = false;
-    tc_fence_after();
-#pragma unroll
-    for (int p = 0; p < 2; ++p) {
-      float v[32];
-      tmem_ld32(lane_base + col0 + p * 32, v);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) S[p * 32 + j] = fmaf(egc, S[p * 32 + j], cke * v[j]);
-    }
-    const int64_t done = (int64_t)n * kC + cl;
-    if (a.c.snap_interval > 0 && done % a.c.snap_interval == 0) {
-      const int64_t s = m.snap_off + done / a.c.snap_interval - 1;
-      if (s < a.c.snaps_capacity) {
-        float4 *d = reinterpret_cast<float4 *>(a.c.snaps + ((s * H + h) * kDK + c) * dv + col0);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) d[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
-      } else if (tid == 0) {
-        raise_error(a.c.err, ERR_SNAP_CAPACITY);
+    if (tid == 0) bulk_wait<0>();  // every output store complete
+  } else if (warp == 4 && lane == 0) {
+    bool issued = false;
+    for (int n = 0; n < N; ++n) {
+      const int b = n & 1;
+      const uint32_t sp = sbase + b * (uint32_t)kCoopPkgBytes;
+      if (!mbar_wait(full0 + 8 * b, (n >> 1) & 1) || (n > 0 && !mbar_wait(acce, (n - 1) & 1)) ||
+          (n > 1 && !mbar_wait(oe0 + 8 * b, ((n - 2) >> 1) & 1))) {
+        failed = true;
+        break;
       }
-    }
-    if (n + 1 < N) {
-      cp_async_wait<0>();
-      fence_async_smem();
-    }
-    tc_fence_before();
-    __syncthreads();
-  }
-  if (!aborted && N > 0) {
-    const int b = (N - 1) & 1;
-    if (cta_wait(bar_o0 + 8 * b, ph_o[b])) {
-      pend_o[b] = false;
       tc_fence_after();
-      retire(N - 1);
-    } else {
-      aborted = true;
+      issued = true;
+      const uint32_t o = tmem + 128 + 64 * b, sa = tmem + 256 + 64 * b;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)  // acc^T = U~^T K^
+        mma_bf16(tmem, sw128_desc(sp + kPkU + kk * 2048, 8192, 1024),
+                 sw128_desc(sp + kPkKm + kk * 2048, 8192, 1024), idesc_bf16(128, 128, 1, 1), kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)  // O^T = U~^T M^T
+        mma_bf16(o, sw128_desc(sp + kPkU + kk * 2048, 8192, 1024),
+                 sw128_desc(sp + kPkM + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0), kk > 0);
+      if (!mbar_wait(sready0 + 8 * b, (n >> 1) & 1)) { failed = true; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // acc^T += S^T (-P^)^T
+        mma_bf16_ts(tmem, sa + kk * 8,
+                    sw128_desc(sp + kPkP + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                    idesc_bf16(128, 128, 0, 0), 1);
+      mma_commit(accf);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // O^T += S^T Q^^T
+        mma_bf16_ts(o, sa + kk * 8,
+                    sw128_desc(sp + kPkQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                    idesc_bf16(128, 64, 0, 0), 1);
+      mma_commit(of0 + 8 * b);
+      mma_commit(empty0 + 8 * b);
+    }
+    if (issued) {  // every MMA done before the tensor memory is released
+      mma_commit(drain);
+      if (!mbar_wait(drain, 0)) failed = true;
+    }
+  } else if (warp == 5 && lane == 0) {
+    const unsigned long long *ready = a.ready + u * kCoopRing;
+    unsigned long long *consumed = a.consumed + u * kCoopRing;
+    const uint8_t *ring_u = a.ring + (size_t)u * kCoopRing * kCoopPkgBytes;
+    for (int n = 0; n < N; ++n) {
+      const int b = n & 1;
+      if ((n > 1 && !mbar_wait(empty0 + 8 * b, ((n - 2) >> 1) & 1)) ||
+          !coop_flag_wait(ready + n % kCoopRing, coop_tag(a.epoch, n), a.hdr + 1)) {
+        failed = true;
+        break;
+      }
+      fence_proxy_async_all();  // the package was written with ordinary stores
+      const uint8_t *src = ring_u + (size_t)(n % kCoopRing) * kCoopPkgBytes;
+      const uint32_t dst = sbase + b * (uint32_t)kCoopPkgBytes, bar = full0 + 8 * b;
+      mbar_expect_tx(bar, (uint32_t)kCoopPkgBytes);
+      for (uint32_t q = 0; q < kPkPieces; ++q) bulk_g2s(dst + q * kPkPiece, src + q * kPkPiece, kPkPiece, bar);
+      if (!mbar_wait(bar, (n >> 1) & 1)) {
+        failed = true;
+        mbar_wait(bar, (n >> 1) & 1);  // the copy is still writing this CTA's memory
+        break;
+      }
+      st_release_u64(consumed + n % kCoopRing, coop_tag(a.epoch, n));
     }
   }
-  if (aborted) {
-    if (tid == 0) coop_abort(a);
-    cp_async_wait<0>();
-    if (pend_s) mbar_wait(bar_s, ph_s);
-    for (int b = 0; b < 2; ++b)
-      if (pend_o[b]) mbar_wait(bar_o0 + 8 * b, ph_o[b]);
-  } else if (m.ok) {
-    float4 *d = reinterpret_cast<float4 *>(a.c.pool + (((int64_t)m.dst * H + h) * kDK + c) * dv + col0);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) d[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
-  }
+  if (failed) coop_abort(a);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 512);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     coop_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                const CoopArgs a) {
+                const __grid_constant__ CUtensorMap tm_o, const CoopArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023) {  // the swizzled layouts need a 1024-byte aligned base
     if (threadIdx.x == 0) coop_abort(a);
     return;
   }
   if ((int)blockIdx.x < a.units)
-    coop_chain(smem, a, blockIdx.x);
+    coop_chain(smem, &tm_o, a, blockIdx.x);
   else
     coop_producer(smem, &tm_q, &tm_k, &tm_v, &tm_g, a);
 }
@@ -1210,6 +1350,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2D map over a [rows][inner] bf16 array, 64 x 64 boxes, 128-byte swizzle.
+// Output map of the cooperative chain: [rows][inner] bf16, boxes of 64 rows x
+// 128 columns, unswizzled (the staging tile is plain row-major).
+bool make_store_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {128, 64};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -1293,8 +1447,10 @@ cudaError_t launch_coop(const PrefillPlan &p, int grid, const CUtensorMap &mq,
   a.consumed = p.coop_flags + (size_t)a.units * kCoopRing;
   a.hdr = p.coop_hdr;
   a.epoch = p.epoch;
-  CUtensorMap q = mq, k = mk, v = mv, g = mg;
-  void *args[] = {&q, &k, &v, &g, &a};
+  CUtensorMap q = mq, k = mk, v = mv, g = mg, o;
+  if (!make_store_map(&o, p.out, (uint64_t)p.H * p.dv, (uint64_t)p.T_total))
+    return cudaErrorInvalidValue;
+  void *args[] = {&q, &k, &v, &g, &o, &a};
   return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(coop_kernel), dim3(grid),
                                      dim3(kThreads), args, kCoopSmem, p.stream);
 }
