@@ -77,10 +77,11 @@ struct Layout {
   // prep scratch: per 4-row group decay sums f32[16][128], in the T rows of
   // [T; M] (8 KiB; the solve rewrites them and zeroes T's upper blocks)
   static constexpr uint32_t kGpart = kTM;
-  // solve scratch (fp32): L (swizzled 64x64) in the W buffer, X^T in the U
-  // buffer, diagonal blocks of X and Y^T in kScr
-  static constexpr uint32_t kXd = kScr;                 // f32[4][16][16]
-  static constexpr uint32_t kYt = kScr + 4096;          // f32[3][16][20]
+  // solve scratch (fp32): L (swizzled 64x64) in the W buffer, X_00^T in the U
+  // buffer; X_11, Y^T and the transposed diagonal blocks of A in kScr
+  static constexpr uint32_t kXd = kScr;                 // f32[32][32]
+  static constexpr uint32_t kYt = kScr + 4096;          // f32[32][32]
+  static constexpr uint32_t kLT = kScr + 8192;          // f32[2][32][32]
   static_assert(kStage % 1024 == 0, "stage alignment");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
@@ -122,95 +123,111 @@ __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
   return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
 }
 
-// One level of the block solve: the 4 - D blocks X_ab with a - b = D, from
-// the blocks of earlier levels.  Each thread owns 4 - D output elements (one
-// per block) and computes them side by side.
-template <int D>
-__device__ __forceinline__ void solve_level(const float *L, float *XT, const float *Xd, float *YT,
-                                            const float *beta, uint8_t *tm, int tid) {
-  constexpr int NB = 4 - D;
-  const int k = tid >> 4, j = tid & 15;  // row k (of Y) / r (of X), column j
-  float acc[NB][2];
-#pragma unroll
-  for (int b = 0; b < NB; ++b) {  // Y_b[k][j] = sum_{b<=c<b+D} A[16(b+D)+k][16c+.] X[16c+.][16b+j]
-    acc[b][0] = acc[b][1] = 0.f;
-#pragma unroll
-    for (int cc = 0; cc < D; ++cc) {
-      const int c = b + cc, ar = 16 * (b + D) + k, xr = 16 * b + j;
-      acc[b][0] = dot4(ld4(L, ar, 16 * c), ld4(XT, xr, 16 * c), acc[b][0]);
-      acc[b][1] = dot4(ld4(L, ar, 16 * c + 4), ld4(XT, xr, 16 * c + 4), acc[b][1]);
-      acc[b][0] = dot4(ld4(L, ar, 16 * c + 8), ld4(XT, xr, 16 * c + 8), acc[b][0]);
-      acc[b][1] = dot4(ld4(L, ar, 16 * c + 12), ld4(XT, xr, 16 * c + 12), acc[b][1]);
-    }
-  }
-#pragma unroll
-  for (int b = 0; b < NB; ++b) YT[b * 320 + j * 20 + k] = acc[b][0] + acc[b][1];
-  __syncthreads();
-#pragma unroll
-  for (int b = 0; b < NB; ++b) {  // X_ab[r][j] = -sum_k X_aa[r][k] Y_b[k][j]
-    const int a = b + D, r = k;
-    const float4 *xr = reinterpret_cast<const float4 *>(Xd + a * 256 + r * 16);
-    const float4 *yc = reinterpret_cast<const float4 *>(YT + b * 320 + j * 20);
-    const float v = -(dot4(xr[0], yc[0], dot4(xr[1], yc[1], 0.f)) +
-                      dot4(xr[2], yc[2], dot4(xr[3], yc[3], 0.f)));
-    XT[fidx(16 * b + j, 16 * a + r)] = v;
-    st_bf(tm, sw128_offset(16 * a + r, 16 * b + j), v * beta[16 * b + j]);
-  }
-  __syncthreads();
+// A 32 x 32 fp32 matrix stored by rows of 8 float4 chunks, chunk c of row r
+// at position c ^ (r & 7) (rows that differ in their low bits hit different
+// banks).
+__device__ __forceinline__ int sidx(int r, int i) {
+  return r * 32 + ((((i >> 2) ^ (r & 7)) << 2) | (i & 3));
+}
+__device__ __forceinline__ float4 ld4s(const float *M, int r, int i) {
+  return *reinterpret_cast<const float4 *>(M + sidx(r, i));
 }
 
 // T = (I + A)^{-1} Diag(beta) for the 64x64 strictly lower A held in L
 // (fidx layout, fp32, zero on and above the diagonal).  X = (I + A)^{-1} is
-// built by 16x16 blocks:
-//  * the four diagonal blocks X_aa by forward substitution, column by column;
-//    four lanes share a column, each owning four consecutive rows, and
-//    combine the partial sums of a step with two shuffles;
-//  * the blocks below the diagonal level by level (a - b = 1, 2, 3):
-//        Y_b = sum_{b<=c<a} A_ac X_cb ,   X_ab = -X_aa Y_b ,
-//    one output element per thread and pass, each a 16-term float4 dot
-//    product per block (A rows from L, X columns from X^T, X_aa rows from
-//    Xd, Y columns from Y^T).
-// T is written as bf16 into rows 0..63 of the K-major [T; M] operand; the
-// threads without a diagonal column zero its blocks above the diagonal (the
-// rows also hold the decay prefix scratch of the chunk's preparation).
-__device__ __forceinline__ void solve_T(const float *L, float *XT, float *Xd, float *YT,
-                                        const float *beta, uint8_t *tm, int tid) {
-  if (tid >= 64) {  // zero T's upper blocks: row r of block rb, chunks 2 (rb + 1) .. 7
-    const int e = tid - 64;  // 192 chunks: 16 rows x 6, 16 x 4, 16 x 2
-    const int rb = e < 96 ? 0 : (e < 160 ? 1 : 2);
-    const int base_e = rb == 0 ? 0 : (rb == 1 ? 96 : 160);
-    const int per = 6 - 2 * rb, r = 16 * rb + (e - base_e) / per, c = 2 * (rb + 1) + (e - base_e) % per;
-    *reinterpret_cast<uint4 *>(tm + sw128_chunk(r, c)) = make_uint4(0, 0, 0, 0);
-  } else {  // one column of one diagonal block per thread
-    const int a = tid >> 4, jj = tid & 15, base = 16 * a;
-    float x[16];
+// built from 32 x 32 blocks:
+//  * the diagonal blocks X_00, X_11 by forward substitution, one column per
+//    thread (threads 0..63), the column in registers;
+//  * the block below them, X_10 = -X_11 (A_10 X_00), as two 32 x 32 x 32
+//    products, each thread owning rows {p, p + 16} x columns {q, q + 16}
+//    (p = tid / 16, q = tid % 16).
+// Scratch: X_00^T in XT (fidx rows 0..31), X_11 row-major in Xd and
+// Y^T = (A_10 X_00)^T in YT (sidx layout, 4 KiB each).  LT holds the two
+// diagonal blocks of A transposed (LT[b][m][i] = A[32b + i][32b + m],
+// written by extract_am), so the substitution runs column by column: once
+// x[m] is known it is folded into the running sums of every later row, and
+// x[m + 1] is one multiply-add away.  T is written as bf16
+// into rows 0..63 of the K-major [T; M] operand at tm; the threads without a
+// diagonal column zero its upper block (the rows also hold the decay prefix
+// scratch of the chunk's preparation).  Ends with a barrier.
+__device__ __forceinline__ void solve_T(const float *L, const float *LT, float *XT, float *Xd,
+                                        float *YT, const float *beta, uint8_t *tm, int tid) {
+  if (tid >= 64) {  // T's upper block: rows 0..31, 16-byte chunks 4..7
+    const int e = tid - 64;
+    if (e < 128) *reinterpret_cast<uint4 *>(tm + sw128_chunk(e >> 2, 4 + (e & 3))) = make_uint4(0, 0, 0, 0);
+  } else {
+    const int b = tid >> 5, j = tid & 31, base = 32 * b;
+    const float *lt = LT + b * 1024;
+    float x[32], t[32];  // column j of X_bb; t[i] = -sum_{m < i, m done} A[i][m] x[m]
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = (i == jj) ? 1.f : 0.f;
+    for (int i = 0; i < 32; ++i) t[i] = 0.f;
 #pragma unroll
-    for (int r = 1; r < 16; ++r) {
-      // L is zero on and above the diagonal, so entries i >= r contribute nothing
-      const float p0 = dot4(ld4(L, base + r, base + 0), make_float4(x[0], x[1], x[2], x[3]), 0.f);
-      const float p1 = dot4(ld4(L, base + r, base + 4), make_float4(x[4], x[5], x[6], x[7]), 0.f);
-      const float p2 = dot4(ld4(L, base + r, base + 8), make_float4(x[8], x[9], x[10], x[11]), 0.f);
-      const float p3 =
-          dot4(ld4(L, base + r, base + 12), make_float4(x[12], x[13], x[14], x[15]), 0.f);
-      if (r > jj) x[r] = -((p0 + p1) + (p2 + p3));
+    for (int m = 0; m < 32; ++m) {
+      x[m] = m < j ? 0.f : (m == j ? 1.f : t[m]);
+#pragma unroll
+      for (int i4 = (m + 1) / 4; i4 < 8; ++i4) {  // rows i > m of column m
+        const float4 l = *reinterpret_cast<const float4 *>(lt + m * 32 + 4 * i4);
+        const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (4 * i4 + e > m) t[4 * i4 + e] = fmaf(-lv[e], x[m], t[4 * i4 + e]);
+      }
+    }
+    const float bj = beta[base + j];
+    if (b == 0) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<float4 *>(XT + fidx(j, 4 * q)) =
+            make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) Xd[sidx(i, j)] = x[i];
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      *reinterpret_cast<float4 *>(XT + fidx(base + jj, base + 4 * q)) =
-          make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
-    const float bj = beta[base + jj];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      Xd[a * 256 + i * 16 + jj] = x[i];
-      st_bf(tm, sw128_offset(base + i, base + jj), x[i] * bj);
-    }
+    for (int i = 0; i < 32; ++i) st_bf(tm, sw128_offset(base + i, base + j), x[i] * bj);
   }
   __syncthreads();
-  solve_level<1>(L, XT, Xd, YT, beta, tm, tid);
-  solve_level<2>(L, XT, Xd, YT, beta, tm, tid);
-  solve_level<3>(L, XT, Xd, YT, beta, tm, tid);
+  const int pr = tid >> 4, qc = tid & 15;
+  {  // Y = A_10 X_00: Y[i][j] = sum_k A[32 + i][k] X_00^T[j][k]
+    float acc[2][2][4] = {};
+#pragma unroll
+    for (int k4 = 0; k4 < 8; ++k4) {
+      const float4 a0 = ld4(L, 32 + pr, 4 * k4), a1 = ld4(L, 48 + pr, 4 * k4);
+      const float4 x0 = ld4(XT, qc, 4 * k4), x1 = ld4(XT, qc + 16, 4 * k4);
+      acc[0][0][k4 & 3] = dot4(a0, x0, acc[0][0][k4 & 3]);
+      acc[0][1][k4 & 3] = dot4(a0, x1, acc[0][1][k4 & 3]);
+      acc[1][0][k4 & 3] = dot4(a1, x0, acc[1][0][k4 & 3]);
+      acc[1][1][k4 & 3] = dot4(a1, x1, acc[1][1][k4 & 3]);
+    }
+#pragma unroll
+    for (int ii = 0; ii < 2; ++ii)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+        YT[sidx(qc + 16 * jj, pr + 16 * ii)] =
+            (acc[ii][jj][0] + acc[ii][jj][1]) + (acc[ii][jj][2] + acc[ii][jj][3]);
+  }
+  __syncthreads();
+  {  // X_10 = -X_11 Y: X_10[i][j] = -sum_k X_11[i][k] Y^T[j][k]
+    float acc[2][2][4] = {};
+#pragma unroll
+    for (int k4 = 0; k4 < 8; ++k4) {
+      const float4 a0 = ld4s(Xd, pr, 4 * k4), a1 = ld4s(Xd, pr + 16, 4 * k4);
+      const float4 y0 = ld4s(YT, qc, 4 * k4), y1 = ld4s(YT, qc + 16, 4 * k4);
+      acc[0][0][k4 & 3] = dot4(a0, y0, acc[0][0][k4 & 3]);
+      acc[0][1][k4 & 3] = dot4(a0, y1, acc[0][1][k4 & 3]);
+      acc[1][0][k4 & 3] = dot4(a1, y0, acc[1][0][k4 & 3]);
+      acc[1][1][k4 & 3] = dot4(a1, y1, acc[1][1][k4 & 3]);
+    }
+#pragma unroll
+    for (int ii = 0; ii < 2; ++ii)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int i = pr + 16 * ii, j = qc + 16 * jj;
+        const float v = -((acc[ii][jj][0] + acc[ii][jj][1]) + (acc[ii][jj][2] + acc[ii][jj][3]));
+        st_bf(tm, sw128_offset(32 + i, j), v * beta[j]);
+      }
+  }
+  __syncthreads();
 }
 
 // ------------------------------------------------------------------ chunk phases
@@ -329,21 +346,27 @@ __device__ __forceinline__ void issue_mma1(uint32_t d, uint32_t sb) {
 }
 
 // A (rows 0..63 of the MMA1 result at taddr) into the fp32 system L (fidx
-// layout, Diag(beta) strict_lower, zero elsewhere); M = lower_incl(Q+ K-^T)
-// (rows 64..127) as bf16 into rows 64..127 of [T; M] at tm.
+// layout, Diag(beta) strict_lower, zero elsewhere), and its two diagonal
+// 32 x 32 blocks transposed into LT (LT[b][m][i] = A[32b + i][32b + m]);
+// M = lower_incl(Q+ K-^T) (rows 64..127) as bf16 into rows 64..127 of [T; M]
+// at tm.
 __device__ __forceinline__ void extract_am(uint32_t taddr, int quarter, int colhalf, int lane,
-                                           const float *s_beta, float *Lm, uint32_t tm) {
+                                           const float *s_beta, float *Lm, float *LT, uint32_t tm) {
   float v[32];
   tmem_ld32(taddr + colhalf * 32, v);
   const int rr = quarter * 32 + lane;
   if (quarter < 2) {
     const float br = s_beta[rr];
+    float a[32];
 #pragma unroll
-    for (int q4 = 0; q4 < 8; ++q4) {
-      const int i = colhalf * 32 + q4 * 4;
-      *reinterpret_cast<float4 *>(Lm + fidx(rr, i)) =
-          make_float4(i < rr ? br * v[q4 * 4] : 0.f, i + 1 < rr ? br * v[q4 * 4 + 1] : 0.f,
-                      i + 2 < rr ? br * v[q4 * 4 + 2] : 0.f, i + 3 < rr ? br * v[q4 * 4 + 3] : 0.f);
+    for (int e = 0; e < 32; ++e) a[e] = colhalf * 32 + e < rr ? br * v[e] : 0.f;
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4)
+      *reinterpret_cast<float4 *>(Lm + fidx(rr, colhalf * 32 + q4 * 4)) =
+          make_float4(a[q4 * 4], a[q4 * 4 + 1], a[q4 * 4 + 2], a[q4 * 4 + 3]);
+    if (quarter == colhalf) {  // a diagonal block: lane = row within it
+#pragma unroll
+      for (int e = 0; e < 32; ++e) LT[quarter * 1024 + e * 32 + lane] = a[e];
     }
   } else {
     const int r = rr - 64;
@@ -538,7 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // A (rows 0..63) into the fp32 system; M (rows 64..127) into [T; M]
     float *Lm = reinterpret_cast<float *>(smem + Ly::kW);
-    extract_am(lane_base + 256, quarter, colhalf, lane, s_beta, Lm, sbase + Ly::kTM);
+    extract_am(lane_base + 256, quarter, colhalf, lane, s_beta, Lm,
+               reinterpret_cast<float *>(smem + Ly::kLT), sbase + Ly::kTM);
     tc_fence_before();
     __syncthreads();
 
@@ -554,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------ solve
-    solve_T(Lm, reinterpret_cast<float *>(smem + Ly::kU),
+    solve_T(Lm, reinterpret_cast<const float *>(smem + Ly::kLT), reinterpret_cast<float *>(smem + Ly::kU),
             reinterpret_cast<float *>(smem + Ly::kXd),
             reinterpret_cast<float *>(smem + Ly::kYt), s_beta, smem + Ly::kTM, tid);
     fence_async_smem();
@@ -862,6 +886,17 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
   }
   __syncthreads();
   int cur = s_item[0], next = s_item[1];
+  // beta of chunk t, row tid (threads 0..63); a chunk's beta is loaded at the
+  // end of the chunk before it, where its latency hides under thread 0's
+  // slot wait and copy issue that the closing barrier waits for anyway
+  auto beta_of = [&](int t) -> float {
+    if (tid >= 64 || t < 0) return 0.f;
+    const int tn = t / units, tu = t % units;
+    const int2 tq = s_seq[tu / H];
+    return load_beta(a.c.beta + (int64_t)(tq.x + tn * kC) * H + tu % H, H,
+                     min(kC, tq.y - tn * kC), tid);
+  };
+  float beta_r = beta_of(cur);
   uint32_t uses[2] = {0, 0}, mma_phase = 0;
   bool tma_pending[2] = {cur >= 0, next >= 0}, mma_pending = false, aborted = false;
   // thread 0: the previous package, stored with bulk copies and published
@@ -874,9 +909,7 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     const int n = cur / units, u = cur % units;
     const int cl = min(kC, s_seq[u / H].y - n * kC);
     const uint32_t sb = sbase + st * Ly::kStage;
-    const float beta_n = tid < 64 ? load_beta(a.c.beta + (int64_t)(s_seq[u / H].x + n * kC) * H + u % H,
-                                              H, cl, tid)
-                                   : 0.f;
+    const float beta_n = beta_r;
     if (!cta_wait(bar_tma0 + 8 * st, uses[st] & 1)) { aborted = true; break; }
     ++uses[st];
     tma_pending[st] = false;
@@ -905,10 +938,11 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       s_cke[tid] = expf(s_tot[tid] - s_anc[tid]);
     }
     float *Lm = reinterpret_cast<float *>(smem + Ly::kW);
-    extract_am(lane_base + 256, quarter, colhalf, lane, s_beta, Lm, sbase + Ly::kTM);
+    extract_am(lane_base + 256, quarter, colhalf, lane, s_beta, Lm,
+               reinterpret_cast<float *>(smem + Ly::kLT), sbase + Ly::kTM);
     tc_fence_before();
     __syncthreads();
-    solve_T(Lm, reinterpret_cast<float *>(smem + Ly::kU),
+    solve_T(Lm, reinterpret_cast<const float *>(smem + Ly::kLT), reinterpret_cast<float *>(smem + Ly::kU),
             reinterpret_cast<float *>(smem + Ly::kXd),
             reinterpret_cast<float *>(smem + Ly::kYt), s_beta, smem + Ly::kTM, tid);
     for (int e = tid; e < 1024; e += kThreads) {  // K^ = K- Diag(e^{G_C - a}) -> solve scratch
@@ -1023,6 +1057,7 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     {
       int ok = 1;
       __syncthreads();
+      beta_r = beta_of(next);
       if (tid == 0 && n >= kCoopRing && slot_seen < coop_tag(a.epoch, n - kCoopRing))
         ok = coop_flag_wait(a.consumed + u * kCoopRing + slot, coop_tag(a.epoch, n - kCoopRing),
                             a.hdr + 1);
