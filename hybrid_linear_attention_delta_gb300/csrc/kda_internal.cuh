@@ -9,8 +9,8 @@
 //                            sequences of one call writing the same state
 //   when B*H <= kCoopMaxUnits, the cooperative prefill's section:
 //   [.., +256)               uint32 ticket, abort word, longest sequence in chunks
-//   [.., +align(B*H*4*16))   u64 ready[B*H][4], consumed[B*H][4] flags
-//   [.., +B*H*4*92160)       package ring, 4 chunk packages per (sequence, head)
+//   [.., +align(B*H*8*16))   u64 ready[B*H][8], consumed[B*H][8] flags
+//   [.., +B*H*8*92160)       package ring, 8 chunk packages per (sequence, head)
 #pragma once
 
 #include <cuda_bf16.h>
@@ -46,7 +46,7 @@ constexpr int kClaimsPerState = 4;  // one claim word per (slot, head, column bl
 // Cooperative prefill (few (sequence, head) pairs): per pair a ring of chunk
 // packages handed from producer CTAs to the pair's state-carrying CTA.
 constexpr int kCoopMaxUnits = 64;      // (sequence, head) pairs it serves at most
-constexpr int kCoopRing = 4;           // packages in flight per pair
+constexpr int kCoopRing = 8;           // packages in flight per pair
 constexpr size_t kCoopPkgBytes = 92160;
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

@@ -51,8 +51,8 @@ def test_snapshot_count_and_workspace_bytes(lib):
     n2 = kda.kda_workspace_bytes(16, 32, 1024)
     assert n1 % 256 == 0 and n2 % 256 == 0
     # few (sequence, head) pairs: room for the cooperative prefill's package
-    # ring (4 packages of 90 KiB per pair)
-    assert n1 >= 32 * 4 * 92160
+    # ring (8 packages of 90 KiB per pair)
+    assert n1 >= 32 * 8 * 92160
     # claims: one word per (slot, head, column block) of the pool; 512 pairs
     # use the per-state prefill, so no ring
     assert 1024 * 32 * 4 * 4 <= n2 < 1024 * 32 * 4 * 4 + 16 * 32 * 64 + 4096
@@ -102,8 +102,9 @@ def test_host_visible_errors_return_without_launch(lib):
     a = _args(B=4, T_total=7, workspace=V(1 << 20), workspace_bytes=1 << 20)
     st = lib.kda_decode(fake, fake, fake, fake, fake, fake, fake, fake, 2, None, ctypes.byref(a))
     assert st == kda.KDA_ERR_INVALID_ARG
-    # forcing the chunked algorithm on an fp32 batch is unsupported
-    a = _args(algo=kda.KDA_ALGO_CHUNKED, workspace=V(1 << 20), workspace_bytes=1 << 20)
+    # forcing the chunked algorithm on an fp32 batch is unsupported (with a
+    # workspace large enough for the cooperative mode's package ring)
+    a = _args(algo=kda.KDA_ALGO_CHUNKED, workspace=V(1 << 26), workspace_bytes=1 << 26)
     st = lib.kda_prefill_varlen(fake, fake, fake, fake, fake, fake, fake, fake, fake, 0, None,
                                 ctypes.byref(a))
     assert st == kda.KDA_ERR_UNSUPPORTED
