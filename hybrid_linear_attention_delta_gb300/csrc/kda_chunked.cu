@@ -899,8 +899,15 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
   float beta_r = beta_of(cur);
   uint32_t uses[2] = {0, 0}, mma_phase = 0;
   bool tma_pending[2] = {cur >= 0, next >= 0}, mma_pending = false, aborted = false;
-  // thread 0: the previous package, stored with bulk copies and published
-  // (ready flag) once they are complete, at the next chunk's first MMA
+  // Thread kPub owns the copy engine: at the end of a chunk it requests the
+  // tiles of the chunk two ahead, waits for the ring slot and stores the
+  // package with bulk copies (shared -> global bulk writes run at about
+  // 29 B/cycle per SM, so the loads go first).  At the next chunk's first MMA
+  // it waits until the stores have read their sources, and during that
+  // chunk's staging (its warp has no rows to stage) until they are complete,
+  // then publishes the package (ready flag).  Thread 0 issues the MMAs and
+  // takes tickets.
+  constexpr int kPub = 64;
   bool pend = false;
   unsigned long long *pend_flag = nullptr, pend_tag = 0, slot_seen = 0;
   int raw_ticket = 0;  // thread 0: drawn at a chunk's first MMA, validated at its second
@@ -920,14 +927,8 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       issue_mma1<Ly>(tmem + 256, sb);
       mma_commit(bar_mma);
       raw_ticket = next >= 0 ? (int)atomicAdd(a.hdr, 1u) : total;  // used at MMA2
-      // the previous package's stores are complete: it is published
-      bulk_wait<0>();
-      if (pend) {
-        fence_proxy_async_all();
-        st_release_u64(pend_flag, pend_tag);
-        pend = false;
-      }
     }
+    if (tid == kPub) bulk_wait_read<0>();  // the previous package's sources are free
     mma_pending = true;
     if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
     mma_phase ^= 1;
@@ -962,10 +963,10 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       issue_mma2<Ly, 128>(tmem, sbase + Ly::kTM, sb);
       mma_commit(bar_mma);
       s_item[2] = next >= 0 ? take_from(raw_ticket) : -1;
-      // peek at this chunk's ring slot early; it is waited for only if the
+    }
+    if (tid == kPub)  // peek at this chunk's ring slot early; it is waited for only if the
       // pair's chain CTA had not yet copied out the chunk that used it before
       slot_seen = n >= kCoopRing ? ld_relaxed_u64(a.consumed + u * kCoopRing + n % kCoopRing) : 0;
-    }
     mma_pending = true;
     if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
     mma_phase ^= 1;
@@ -1004,6 +1005,11 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
         const uint4 w = pack8(v + 8 * q8);
         st_shared_v4(sbase + Ly::kU + colhalf * 8192 + sw128_chunk(r, q8), w.x, w.y, w.z, w.w);
       }
+    } else if (tid == kPub && pend) {  // the previous package is complete: publish it
+      bulk_wait<0>();
+      fence_proxy_async_all();
+      st_release_u64(pend_flag, pend_tag);
+      pend = false;
     }
     if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
     mma_phase ^= 1;
@@ -1058,14 +1064,14 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       int ok = 1;
       __syncthreads();
       beta_r = beta_of(next);
-      if (tid == 0 && n >= kCoopRing && slot_seen < coop_tag(a.epoch, n - kCoopRing))
+      if (tid == kPub && after >= 0) issue(after, st);  // before the stores, on the same engine
+      if (tid == kPub && n >= kCoopRing && slot_seen < coop_tag(a.epoch, n - kCoopRing))
         ok = coop_flag_wait(a.consumed + u * kCoopRing + slot, coop_tag(a.epoch, n - kCoopRing),
                             a.hdr + 1);
-      if (tid == 0 && after >= 0) issue(after, st);  // before the stores, on the same engine
       // the package, piece by piece from where it was staged (W, U, solve
       // scratch, S0 region, M, e^{G_C}); these are first overwritten after
-      // the next chunk's first MMA, where thread 0 waits for the stores
-      if (tid == 0 && ok) {
+      // the next chunk's first MMA, where thread kPub waits for the stores
+      if (tid == kPub && ok) {
         uint8_t *pk = a.ring + ((size_t)u * kCoopRing + slot) * kCoopPkgBytes;
         bulk_s2g(pk + kPkP, sbase + Ly::kS0, 32768);
         bulk_s2g(pk + kPkKm, sbase + Ly::kScr, 16384);
@@ -1084,7 +1090,7 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     cur = next;
     next = after;
   }
-  if (tid == 0) {  // the last package: complete, then published (unless aborted)
+  if (tid == kPub) {  // the last package: complete, then published (unless aborted)
     bulk_wait<0>();
     if (pend && !aborted) {
       fence_proxy_async_all();
