@@ -136,8 +136,8 @@ __device__ __forceinline__ float4 ld4s(const float *M, int r, int i) {
 // T = (I + A)^{-1} Diag(beta) for the 64x64 strictly lower A held in L
 // (fidx layout, fp32, zero on and above the diagonal).  X = (I + A)^{-1} is
 // built from 32 x 32 blocks:
-//  * the diagonal blocks X_00, X_11 by forward substitution, one column per
-//    thread (threads 0..63), the column in registers;
+//  * the diagonal blocks X_00, X_11 by forward substitution, each column
+//    shared by two lanes of a warp (rows 0..15 and 16..31; threads 0..127);
 //  * the block below them, X_10 = -X_11 (A_10 X_00), as two 32 x 32 x 32
 //    products, each thread owning rows {p, p + 16} x columns {q, q + 16}
 //    (p = tid / 16, q = tid % 16).
@@ -152,39 +152,67 @@ __device__ __forceinline__ float4 ld4s(const float *M, int r, int i) {
 // scratch of the chunk's preparation).  Ends with a barrier.
 __device__ __forceinline__ void solve_T(const float *L, const float *LT, float *XT, float *Xd,
                                         float *YT, const float *beta, uint8_t *tm, int tid) {
-  if (tid >= 64) {  // T's upper block: rows 0..31, 16-byte chunks 4..7
-    const int e = tid - 64;
-    if (e < 128) *reinterpret_cast<uint4 *>(tm + sw128_chunk(e >> 2, 4 + (e & 3))) = make_uint4(0, 0, 0, 0);
+  if (tid >= 128) {  // T's upper block: rows 0..31, 16-byte chunks 4..7
+    const int e = tid - 128;
+    *reinterpret_cast<uint4 *>(tm + sw128_chunk(e >> 2, 4 + (e & 3))) = make_uint4(0, 0, 0, 0);
   } else {
-    const int b = tid >> 5, j = tid & 31, base = 32 * b;
-    const float *lt = LT + b * 1024;
-    float x[32], t[32];  // column j of X_bb; t[i] = -sum_{m < i, m done} A[i][m] x[m]
+    // warp w: block b = w / 2, columns 16 (w % 2) .. +15 of it; a column's
+    // rows 0..15 belong to lane c, rows 16..31 to lane c + 16 (c = lane % 16)
+    const int lane = tid & 31, w = tid >> 5, b = w >> 1, half = lane >> 4;
+    const int j = 16 * (w & 1) + (lane & 15), base = 32 * b;
+    const float *lt = LT + b * 1024 + 16 * half;
+    float t[16], xo[16];  // running sums and values of this lane's rows 16 half + e
 #pragma unroll
-    for (int i = 0; i < 32; ++i) t[i] = 0.f;
+    for (int e = 0; e < 16; ++e) t[e] = 0.f;
+    auto sel = [&](int m, float v) { return m < j ? 0.f : (m == j ? 1.f : v); };
 #pragma unroll
-    for (int m = 0; m < 32; ++m) {
-      x[m] = m < j ? 0.f : (m == j ? 1.f : t[m]);
+    for (int g = 0; g < 8; ++g) {  // columns m0 .. m0 + 3, owned by the lanes of half g / 4
+      const int m0 = 4 * g;
+      float l[4][16];  // column m0 + k of A at this lane's rows
 #pragma unroll
-      for (int i4 = (m + 1) / 4; i4 < 8; ++i4) {  // rows i > m of column m
-        const float4 l = *reinterpret_cast<const float4 *>(lt + m * 32 + 4 * i4);
-        const float lv[4] = {l.x, l.y, l.z, l.w};
+      for (int k = 0; k < 4; ++k)
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (4 * i4 + e > m) t[4 * i4 + e] = fmaf(-lv[e], x[m], t[4 * i4 + e]);
+        for (int q = 0; q < 4; ++q) {
+          const float4 v = *reinterpret_cast<const float4 *>(lt + (m0 + k) * 32 + 4 * q);
+          l[k][4 * q] = v.x;
+          l[k][4 * q + 1] = v.y;
+          l[k][4 * q + 2] = v.z;
+          l[k][4 * q + 3] = v.w;
+        }
+      // the 4 x 4 triangle, on every lane (meaningful on the owner of rows m0..m0+3)
+      const int e0 = m0 & 15;
+      const float y0 = sel(m0, t[e0]);
+      const float y1 = sel(m0 + 1, fmaf(-l[0][e0 + 1], y0, t[e0 + 1]));
+      const float y2 = sel(m0 + 2, fmaf(-l[1][e0 + 2], y1, fmaf(-l[0][e0 + 2], y0, t[e0 + 2])));
+      const float y3 =
+          sel(m0 + 3, fmaf(-l[2][e0 + 3], y2,
+                           fmaf(-l[1][e0 + 3], y1, fmaf(-l[0][e0 + 3], y0, t[e0 + 3]))));
+      const int src = (lane & 15) + 16 * (g >> 2);
+      const float x0 = __shfl_sync(0xffffffffu, y0, src), x1 = __shfl_sync(0xffffffffu, y1, src);
+      const float x2 = __shfl_sync(0xffffffffu, y2, src), x3 = __shfl_sync(0xffffffffu, y3, src);
+      if (half == (g >> 2)) {
+        xo[e0] = x0;
+        xo[e0 + 1] = x1;
+        xo[e0 + 2] = x2;
+        xo[e0 + 3] = x3;
       }
+#pragma unroll
+      for (int e = 0; e < 16; ++e)  // columns m0.. of A are zero at rows <= their index
+        t[e] = fmaf(-l[3][e], x3, fmaf(-l[2][e], x2, fmaf(-l[1][e], x1, fmaf(-l[0][e], x0, t[e]))));
     }
     const float bj = beta[base + j];
+    const int r0 = 16 * half;
     if (b == 0) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<float4 *>(XT + fidx(j, 4 * q)) =
-            make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<float4 *>(XT + fidx(j, r0 + 4 * q)) =
+            make_float4(xo[4 * q], xo[4 * q + 1], xo[4 * q + 2], xo[4 * q + 3]);
     } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) Xd[sidx(i, j)] = x[i];
+      for (int e = 0; e < 16; ++e) Xd[sidx(r0 + e, j)] = xo[e];
     }
 #pragma unroll
-    for (int i = 0; i < 32; ++i) st_bf(tm, sw128_offset(base + i, base + j), x[i] * bj);
+    for (int e = 0; e < 16; ++e) st_bf(tm, sw128_offset(base + r0 + e, base + j), xo[e] * bj);
   }
   __syncthreads();
   const int pr = tid >> 4, qc = tid & 15;
