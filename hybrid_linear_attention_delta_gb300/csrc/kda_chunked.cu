@@ -762,31 +762,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 32 bits and the chunk number + 1 below; every wait is bounded and an abort
 // word stops all CTAs after a timeout.
 //
-// With U = U~ - W S' expanded (S' = Diag(e^{a}) S), the single-CTA kernel's
-// update is
-//     S_next = Diag(e^{G_C}) S + Diag(e^{G_C - a}) (K-^T U~ - P S'),  P = K-^T W
-//     O      = Q~ S' + M U~,                                          Q~ = Q+ - M W.
+// The single-CTA kernel's update is, with S' = Diag(e^{a}) S,
+//     U = U~ - W S',  S_next = Diag(e^{G_C}) S + Diag(e^{G_C - a}) K-^T U,
+//     O = Q+ S' + M U.
 // The producer folds the per-channel factors into its operands,
-//     K^ = K- Diag(e^{G_C - a})            (= K Diag(e^{G_C - G_r}) per row: at most |K|)
-//     P^ = Diag(e^{G_C - a}) P Diag(e^{a}) (= K^^T (W Diag(e^{a})), from an MMA on K^)
-//     Q^ = Q~ Diag(e^{a}),
+//     K^  = K- Diag(e^{G_C - a})   (= K Diag(e^{G_C - G_r}) per row: at most |K|)
+//     W^  = W Diag(e^{a}),  Q+' = Q+ Diag(e^{a}),
 // so that with the state itself as the bf16 operand
-//     S_next = Diag(e^{G_C}) S + K^^T U~ - P^ S,    O = Q^ S + M U~,
+//     U = U~ - W^ S,   S_next = Diag(e^{G_C}) S + K^^T U,   O = Q+' S + M U,
 // and the chain CTA works on the transposed state: S^T (bf16, in TMEM) is the
-// A operand of  acc^T = U~^T K^ - S^T P^^T  and  O^T = S^T Q^^T + U~^T M^T.
-// Only the S-dependent half of each (8 MMAs of K = 16) waits for the state.
+// A operand of X^T = S^T W^^T and of O^T = S^T Q+'^T; the state warps form
+// U^T = U~^T - X^T (bf16, in TMEM), the A operand of acc^T = U^T K^ and of
+// O^T += U^T M^T.
 
 // package layout (bytes); each operand in the shared-memory layout the chain
-// CTA feeds to its MMAs, so packages are copied verbatim
-constexpr uint32_t kPkP = 0;        // -P^ [128 i][128 c] bf16, K-major, 2 halves x 16 KiB
-constexpr uint32_t kPkKm = 32768;   // K^ [64 tok][128 ch] bf16, 2 halves x 8 KiB
-constexpr uint32_t kPkU = 49152;    // U~ [64 tok][128 dv] bf16, 2 halves x 8 KiB
-constexpr uint32_t kPkQ = 65536;    // Q^ [64 tok][128 ch] bf16, K-major, 2 halves x 8 KiB
-constexpr uint32_t kPkM = 81920;    // M [64 tok][64 tok] bf16, K-major, 8 KiB
-constexpr uint32_t kPkDec = 90112;  // f32 e^{G_C}[128]
-static_assert(kPkDec + 1536 <= kCoopPkgBytes && kCoopPkgBytes % 1024 == 0, "package layout");
+// CTA feeds to its MMAs (U~ is read by its state warps), copied verbatim
+constexpr uint32_t kPkW = 0;        // W^ [64 tok][128 ch] bf16, K-major, 2 halves x 8 KiB
+constexpr uint32_t kPkKm = 16384;   // K^ [64 tok][128 ch] bf16, 2 halves x 8 KiB
+constexpr uint32_t kPkU = 32768;    // U~ [64 tok][128 dv] bf16, 2 halves x 8 KiB
+constexpr uint32_t kPkQ = 49152;    // Q+' [64 tok][128 ch] bf16, K-major, 2 halves x 8 KiB
+constexpr uint32_t kPkM = 65536;    // M [64 tok][64 tok] bf16, K-major, 8 KiB
+constexpr uint32_t kPkDec = 73728;  // f32 e^{G_C}[128]
+static_assert(kPkDec + 512 <= kCoopPkgBytes && kCoopPkgBytes % 1024 == 0, "package layout");
 // a package is fetched as kPkPieces bulk copies of kPkPiece bytes
-constexpr uint32_t kPkPieces = 5, kPkPiece = (uint32_t)kCoopPkgBytes / kPkPieces;
+constexpr uint32_t kPkPieces = 4, kPkPiece = (uint32_t)kCoopPkgBytes / kPkPieces;
 static_assert(kPkPiece % 16 == 0 && kPkPiece * kPkPieces == kCoopPkgBytes, "bulk copy pieces");
 // chain CTA shared memory: two package stages, two output staging tiles
 // ([64 tok][128 dv] bf16 each, stored with one TMA box), mbarriers, TMEM slot
@@ -1001,32 +1000,29 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     mma_pending = false;
     const int after = s_item[2];
     tc_fence_after();
-    extract_w(lane_base, quarter, colhalf, lane, sbase + Ly::kW);
-    tc_fence_before();
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {  // P^ = K^^T W -> tmem[256, 384); M W -> tmem[384, 512)
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t bd = sw128_desc(sbase + Ly::kW + kk * 2048, 8192, 1024);
-        mma_bf16(tmem + 256, sw128_desc(sbase + Ly::kScr + kk * 2048, 8192, 1024), bd,
-                 idesc_bf16(128, 128, 1, 1), kk > 0);
-        mma_bf16(tmem + 384, sw128_desc(sbase + Ly::kTM + 8192 + kk * 32, 16, 1024), bd,
-                 idesc_bf16(128, 128, 0, 1), kk > 0);
-      }
-      mma_commit(bar_mma);
-    }
-    mma_pending = true;
-
     // The package is staged in shared memory in its final layout, outside
-    // both input stages, then written out with bulk copies: K^ in the solve
-    // scratch, U~ in the U buffer, -P^ in the S0 region, Q^ in the W buffer
-    // once the MMAs reading W are done, M where the solve left it, e^{G_C}
-    // in the e^{G_C - a} vector.
-    if (quarter < 2) {  // U~: rows 0..63 of tmem[128, 256)
+    // both input stages, then written out with bulk copies: W^ = W Diag(e^{a})
+    // in the W buffer, K^ in the solve scratch, U~ in the U buffer,
+    // Q+' = Q+ Diag(e^{a}) in the S0 region, M where the solve left it and
+    // e^{G_C} in the e^{G_C - a} vector.
+    if (quarter < 2) {  // W^ and U~: rows 0..63 of tmem[0, 128) and [128, 256)
       const int r = quarter * 32 + lane;
       float v[64];
+      tmem_ld64(lane_base + colhalf * 64, v);
+      const float4 *ea = reinterpret_cast<const float4 *>(s_ea + colhalf * 64);
+#pragma unroll
+      for (int q4 = 0; q4 < 16; ++q4) {
+        const float4 e4 = ea[q4];
+        v[4 * q4] *= e4.x;
+        v[4 * q4 + 1] *= e4.y;
+        v[4 * q4 + 2] *= e4.z;
+        v[4 * q4 + 3] *= e4.w;
+      }
+#pragma unroll
+      for (int q8 = 0; q8 < 8; ++q8) {
+        const uint4 w = pack8(v + 8 * q8);
+        st_shared_v4(sbase + Ly::kW + colhalf * 8192 + sw128_chunk(r, q8), w.x, w.y, w.z, w.w);
+      }
       tmem_ld64(lane_base + 128 + colhalf * 64, v);
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) {
@@ -1039,50 +1035,16 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       st_release_u64(pend_flag, pend_tag);
       pend = false;
     }
-    if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
-    mma_phase ^= 1;
-    mma_pending = false;
-    tc_fence_after();
-    {  // -P^ = -(K^^T W) Diag(e^{a}): row i (all 128), K half colhalf
-      const int i = quarter * 32 + lane;
-      const uint32_t dst = sbase + Ly::kS0 + colhalf * 16384;
-      float v[64];
-      tmem_ld64(lane_base + 256 + colhalf * 64, v);
-      const float4 *ea = reinterpret_cast<const float4 *>(s_ea + colhalf * 64);
-#pragma unroll
-      for (int q4 = 0; q4 < 16; ++q4) {
-        const float4 e4 = ea[q4];
-        v[4 * q4] *= -e4.x;
-        v[4 * q4 + 1] *= -e4.y;
-        v[4 * q4 + 2] *= -e4.z;
-        v[4 * q4 + 3] *= -e4.w;
-      }
-#pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
-        const uint4 w = pack8(v + 8 * q8);
-        st_shared_v4(dst + sw128_chunk(i, q8), w.x, w.y, w.z, w.w);
-      }
-    }
-    if (quarter < 2) {  // Q~ = Q+ - M W (rows 0..63)
-      const int r = quarter * 32 + lane;
-      float v[64];
-      tmem_ld64(lane_base + 384 + colhalf * 64, v);
-#pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
-        const uint4 qw = ld_shared_v4(sb + Ly::kQ + colhalf * 16384 + sw128_chunk(r, q8));
-        const uint32_t qv[4] = {qw.x, qw.y, qw.z, qw.w};
-        const float4 *ea = reinterpret_cast<const float4 *>(s_ea + colhalf * 64 + 8 * q8);
-        const float4 e0 = ea[0], e1 = ea[1];
-        const float es[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-        float d[8];  // Q^ = (Q+ - M W) Diag(e^{a}), over W (its MMAs are done)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          d[2 * j] = (bf16lo(qv[j]) - v[8 * q8 + 2 * j]) * es[2 * j];
-          d[2 * j + 1] = (bf16hi(qv[j]) - v[8 * q8 + 2 * j + 1]) * es[2 * j + 1];
-        }
-        const uint4 w = pack8(d);
-        st_shared_v4(sbase + Ly::kW + colhalf * 8192 + sw128_chunk(r, q8), w.x, w.y, w.z, w.w);
-      }
+    for (int e = tid; e < 1024; e += kThreads) {  // Q+' = Q+ Diag(e^{a}) -> S0 region
+      const int half = e >> 9, r = (e >> 3) & 63, q = e & 7;
+      const uint32_t off = r * 128 + q * 16;
+      const float4 *f = reinterpret_cast<const float4 *>(s_ea + half * 64 + 8 * (q ^ (r & 7)));
+      const float4 f0 = f[0], f1 = f[1];
+      const uint4 w = ld_shared_v4(sb + Ly::kQ + half * 16384 + off);
+      st_shared_v4(sbase + Ly::kS0 + half * 8192 + off, pack_bf16x2(bf16lo(w.x) * f0.x, bf16hi(w.x) * f0.y),
+                   pack_bf16x2(bf16lo(w.y) * f0.z, bf16hi(w.y) * f0.w),
+                   pack_bf16x2(bf16lo(w.z) * f1.x, bf16hi(w.z) * f1.y),
+                   pack_bf16x2(bf16lo(w.w) * f1.z, bf16hi(w.w) * f1.w));
     }
     if (tid < 128) s_cke[tid] = expf(s_tot[tid]);  // e^{G_C} for the package
     tc_fence_before();
@@ -1101,10 +1063,10 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       // the next chunk's first MMA, where thread kPub waits for the stores
       if (tid == kPub && ok) {
         uint8_t *pk = a.ring + ((size_t)u * kCoopRing + slot) * kCoopPkgBytes;
-        bulk_s2g(pk + kPkP, sbase + Ly::kS0, 32768);
+        bulk_s2g(pk + kPkW, sbase + Ly::kW, 16384);
         bulk_s2g(pk + kPkKm, sbase + Ly::kScr, 16384);
         bulk_s2g(pk + kPkU, sbase + Ly::kU, 16384);
-        bulk_s2g(pk + kPkQ, sbase + Ly::kW, 16384);
+        bulk_s2g(pk + kPkQ, sbase + Ly::kS0, 16384);
         bulk_s2g(pk + kPkM, sbase + Ly::kTM + 8192, 8192);
         bulk_s2g(pk + kPkDec, sbase + Ly::kMisc + Ly::kCke, 512);
         bulk_commit();
@@ -1141,16 +1103,19 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
 //   warps 0-3 (state): thread j holds column j of S (row j of S^T) for all 128
 //     channels in fp32 registers.  Per chunk n it stores bf16(S^T) into TMEM
 //     buffer n & 1 (the A operand of the chunk's state-dependent MMAs),
-//     retires chunk n-1's outputs while those MMAs run, then applies
+//     retires chunk n-1's outputs while those MMAs run, forms
+//     U^T = U~^T - X^T (bf16, into TMEM), then applies
 //     S <- Diag(e^{G_C}) S + acc and writes snapshots.
-//   warp 4, one lane (MMA): per chunk, acc^T = U~^T K^ and O^T = U~^T M^T as
-//     soon as the package has landed, then acc^T -= S^T P^^T (commit: acc
-//     ready) and O^T += S^T Q^^T (commit: outputs ready, stage free).
+//   warp 4, one lane (MMA): per chunk, once S^T is stored, X^T = S^T W^^T
+//     (commit: X ready) and O^T = S^T Q+'^T; once the state warps stored
+//     U^T = U~^T - X^T, acc^T = U^T K^ (commit: acc ready) and O^T += U^T M^T
+//     (commit: outputs ready, stage free).
 //   warp 5, one lane (loader): waits until package n is in the ring, fetches
 //     it into stage n & 1 with bulk copies, and hands the ring slot back.
 // TMEM columns: acc^T [0, 128); O^T[b] [128 + 64 b, +64); S^T[b] as bf16
-// pairs [256 + 64 b, +64).  Every wait is bounded; a role that gives up
-// raises the abort word and leaves its loop, and the others then time out.
+// pairs [256 + 64 b, +64); X^T [384, 448); U^T as bf16 pairs [448, 480).
+// Every wait is bounded; a role that gives up raises the abort word and
+// leaves its loop, and the others then time out.
 // Warp-uniform bounded wait: every lane polls, and all lanes give up together
 // if any did, so the warp stays converged for the tcgen05 loads and stores.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
@@ -1166,11 +1131,13 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
   const int H = a.c.H, h = u % H, dv = a.c.dv;
   const SeqMeta m = a.c.meta[a.c.order[u / H]];
   // mbarriers: full[2] (package landed), empty[2] (stage free: MMAs done and
-  // the state warps read its decays), sready[2] (S^T stored), accf / acce
-  // (acc^T ready / read), of[2] / oe[2] (O^T ready / read), drain
+  // the state warps read its U~ and decays), sready[2] (S^T stored), xf
+  // (X^T ready), uready (U^T stored), accf (acc^T ready), of[2] / oe[2] (O^T
+  // ready / read), drain
   const uint32_t bars = sbase + kChMisc;
   const uint32_t full0 = bars, empty0 = bars + 16, sready0 = bars + 32, accf = bars + 48,
-                 acce = bars + 56, of0 = bars + 64, oe0 = bars + 80, drain = bars + 96;
+                 xf = bars + 56, of0 = bars + 64, oe0 = bars + 80, drain = bars + 96,
+                 uready = bars + 104;
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -1180,7 +1147,8 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
       mbar_init(oe0 + 8 * s, 4);
     }
     mbar_init(accf, 1);
-    mbar_init(acce, 4);
+    mbar_init(xf, 1);
+    mbar_init(uready, 4);
     mbar_init(drain, 1);
     fence_mbar_init();
   }
@@ -1264,10 +1232,28 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
       __syncwarp();
       if (lane == 0) mbar_arrive(sready0 + 8 * b);
       if (n > 0 && !retire(n - 1)) { failed = true; break; }
-      if (!warp_wait(full0 + 8 * b, (n >> 1) & 1) || !warp_wait(accf, n & 1)) {
+      if (!warp_wait(full0 + 8 * b, (n >> 1) & 1) || !warp_wait(xf, n & 1)) {
         failed = true;
         break;
       }
+      tc_fence_after();
+      {  // U^T = U~^T - X^T into tensor memory: column q holds tokens 2q (low half), 2q + 1
+        float x[64];
+        tmem_ld64(lane_base + 384, x);
+        const __nv_bfloat16 *ub = reinterpret_cast<const __nv_bfloat16 *>(
+            smem + b * kCoopPkgBytes + kPkU + (j >> 6) * 8192);
+        uint32_t r[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          r[q] = pack_bf16x2(__bfloat162float(ub[sw128_offset(2 * q, j & 63) >> 1]) - x[2 * q],
+                             __bfloat162float(ub[sw128_offset(2 * q + 1, j & 63) >> 1]) - x[2 * q + 1]);
+        tmem_st32(lane_base + 448, r);
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(uready);
+      if (!warp_wait(accf, n & 1)) { failed = true; break; }
       tc_fence_after();
       const float4 *egc = reinterpret_cast<const float4 *>(smem + b * kCoopPkgBytes + kPkDec);
 #pragma unroll
@@ -1292,10 +1278,7 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(acce);
-        mbar_arrive(empty0 + 8 * b);
-      }
+      if (lane == 0) mbar_arrive(empty0 + 8 * b);
       const int cl = min(kC, m.len - n * kC);
       const int64_t done = (int64_t)n * kC + cl;
       if (a.c.snap_interval > 0 && done % a.c.snap_interval == 0) {
@@ -1321,34 +1304,35 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
     for (int n = 0; n < N; ++n) {
       const int b = n & 1;
       const uint32_t sp = sbase + b * (uint32_t)kCoopPkgBytes;
-      if (!mbar_wait(full0 + 8 * b, (n >> 1) & 1) || (n > 0 && !mbar_wait(acce, (n - 1) & 1)) ||
-          (n > 1 && !mbar_wait(oe0 + 8 * b, ((n - 2) >> 1) & 1))) {
+      if (!mbar_wait(full0 + 8 * b, (n >> 1) & 1) ||
+          (n > 1 && !mbar_wait(oe0 + 8 * b, ((n - 2) >> 1) & 1)) ||
+          !mbar_wait(sready0 + 8 * b, (n >> 1) & 1)) {
         failed = true;
         break;
       }
       tc_fence_after();
       issued = true;
-      const uint32_t o = tmem + 128 + 64 * b, sa = tmem + 256 + 64 * b;
+      const uint32_t o = tmem + 128 + 64 * b, sa = tmem + 256 + 64 * b, xt = tmem + 384,
+                     ut = tmem + 448;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)  // acc^T = U~^T K^
-        mma_bf16(tmem, sw128_desc(sp + kPkU + kk * 2048, 8192, 1024),
-                 sw128_desc(sp + kPkKm + kk * 2048, 8192, 1024), idesc_bf16(128, 128, 1, 1), kk > 0);
+      for (int kk = 0; kk < 8; ++kk)  // X^T = S^T W^^T
+        mma_bf16_ts(xt, sa + kk * 8, sw128_desc(sp + kPkW + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                    idesc_bf16(128, 64, 0, 0), kk > 0);
+      mma_commit(xf);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)  // O^T = U~^T M^T
-        mma_bf16(o, sw128_desc(sp + kPkU + kk * 2048, 8192, 1024),
-                 sw128_desc(sp + kPkM + kk * 32, 16, 1024), idesc_bf16(128, 64, 1, 0), kk > 0);
-      if (!mbar_wait(sready0 + 8 * b, (n >> 1) & 1)) { failed = true; break; }
+      for (int kk = 0; kk < 8; ++kk)  // O^T = S^T Q+'^T
+        mma_bf16_ts(o, sa + kk * 8, sw128_desc(sp + kPkQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                    idesc_bf16(128, 64, 0, 0), kk > 0);
+      if (!mbar_wait(uready, n & 1)) { failed = true; break; }
       tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // acc^T += S^T (-P^)^T
-        mma_bf16_ts(tmem, sa + kk * 8,
-                    sw128_desc(sp + kPkP + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                    idesc_bf16(128, 128, 0, 0), 1);
+      for (int kk = 0; kk < 4; ++kk)  // acc^T = U^T K^
+        mma_bf16_ts(tmem, ut + kk * 8, sw128_desc(sp + kPkKm + kk * 2048, 8192, 1024),
+                    idesc_bf16(128, 128, 0, 1), kk > 0);
       mma_commit(accf);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // O^T += S^T Q^^T
-        mma_bf16_ts(o, sa + kk * 8,
-                    sw128_desc(sp + kPkQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+      for (int kk = 0; kk < 4; ++kk)  // O^T += U^T M^T
+        mma_bf16_ts(o, ut + kk * 8, sw128_desc(sp + kPkM + kk * 32, 16, 1024),
                     idesc_bf16(128, 64, 0, 0), 1);
       mma_commit(of0 + 8 * b);
       mma_commit(empty0 + 8 * b);

@@ -10,7 +10,7 @@
 //   when B*H <= kCoopMaxUnits, the cooperative prefill's section:
 //   [.., +256)               uint32 ticket, abort word, longest sequence in chunks
 //   [.., +align(B*H*8*16))   u64 ready[B*H][8], consumed[B*H][8] flags
-//   [.., +B*H*8*92160)       package ring, 8 chunk packages per (sequence, head)
+//   [.., +B*H*8*74752)       package ring, 8 chunk packages per (sequence, head)
 #pragma once
 
 #include <cuda_bf16.h>
@@ -47,7 +47,7 @@ constexpr int kClaimsPerState = 4;  // one claim word per (slot, head, column bl
 // packages handed from producer CTAs to the pair's state-carrying CTA.
 constexpr int kCoopMaxUnits = 64;      // (sequence, head) pairs it serves at most
 constexpr int kCoopRing = 8;           // packages in flight per pair
-constexpr size_t kCoopPkgBytes = 92160;
+constexpr size_t kCoopPkgBytes = 74752;
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
