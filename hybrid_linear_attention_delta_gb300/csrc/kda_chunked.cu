@@ -886,19 +886,31 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     return t < total ? t : -1;
   };
   auto take = [&]() -> int { return take_from((int)atomicAdd(a.hdr, 1u)); };
-  auto issue = [&](int t, int st) {  // thread 0: TMA loads of chunk t into stage st
+  // TMA loads of chunk t into stage st, one thread: the k, v and g tiles
+  // (with the byte count of all eight) and the q tiles, which the producer
+  // may request at different points
+  auto issue_kvg = [&](int t, int st) {
     const int u = t % units, h = u % H;
     const uint32_t sb = sbase + st * Ly::kStage, bar = bar_tma0 + 8 * st;
     const int y = s_seq[u / H].x + (t / units) * kC;
     mbar_expect_tx(bar, 8 * 8192);
     tma_load_2d(sb, tm_k, h * kDK, y, bar);
     tma_load_2d(sb + 16384, tm_k, h * kDK + 64, y, bar);
-    tma_load_2d(sb + Ly::kQ, tm_q, h * kDK, y, bar);
-    tma_load_2d(sb + Ly::kQ + 16384, tm_q, h * kDK + 64, y, bar);
     tma_load_2d(sb + Ly::kV, tm_v, h * 128, y, bar);
     tma_load_2d(sb + Ly::kV + 8192, tm_v, h * 128 + 64, y, bar);
     tma_load_2d(sb + Ly::kG, tm_g, h * kDK, y, bar);
     tma_load_2d(sb + Ly::kG + 8192, tm_g, h * kDK + 64, y, bar);
+  };
+  auto issue_q = [&](int t, int st) {
+    const int u = t % units, h = u % H;
+    const uint32_t sb = sbase + st * Ly::kStage, bar = bar_tma0 + 8 * st;
+    const int y = s_seq[u / H].x + (t / units) * kC;
+    tma_load_2d(sb + Ly::kQ, tm_q, h * kDK, y, bar);
+    tma_load_2d(sb + Ly::kQ + 16384, tm_q, h * kDK + 64, y, bar);
+  };
+  auto issue = [&](int t, int st) {
+    issue_kvg(t, st);
+    issue_q(t, st);
   };
 
   // the tiles of a chunk are loaded while the chunk before it is worked on:
@@ -930,10 +942,9 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
   // tiles of the chunk two ahead, waits for the ring slot and stores the
   // package with bulk copies (shared -> global bulk writes run at about
   // 29 B/cycle per SM, so the loads go first).  At the next chunk's first MMA
-  // it waits until the stores have read their sources, and during that
-  // chunk's staging (its warp has no rows to stage) until they are complete,
-  // then publishes the package (ready flag).  Thread 0 issues the MMAs and
-  // takes tickets.
+  // it waits until the stores are complete (their sources are then free) and
+  // publishes the package (ready flag).  Thread 0 issues the MMAs and takes
+  // tickets.
   constexpr int kPub = 64;
   bool pend = false;
   unsigned long long *pend_flag = nullptr, pend_tag = 0, slot_seen = 0;
@@ -955,7 +966,14 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       mma_commit(bar_mma);
       raw_ticket = next >= 0 ? (int)atomicAdd(a.hdr, 1u) : total;  // used at MMA2
     }
-    if (tid == kPub) bulk_wait_read<0>();  // the previous package's sources are free
+    if (tid == kPub) {  // the previous package is complete (its sources are free): publish it
+      bulk_wait<0>();
+      if (pend) {
+        fence_proxy_async_all();
+        st_release_u64(pend_flag, pend_tag);
+        pend = false;
+      }
+    }
     mma_pending = true;
     if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
     mma_phase ^= 1;
@@ -1005,6 +1023,11 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     // in the W buffer, K^ in the solve scratch, U~ in the U buffer,
     // Q+' = Q+ Diag(e^{a}) in the S0 region, M where the solve left it and
     // e^{G_C} in the e^{G_C - a} vector.
+    // the chunk two ahead goes to this chunk's stage: its k, v and g tiles are
+    // dead now (q is read once more, below), and thread kPub's warp has no
+    // rows to stage
+    if (tid == kPub && after >= 0) issue_kvg(after, st);
+    if (after >= 0) tma_pending[st] = true;
     if (quarter < 2) {  // W^ and U~: rows 0..63 of tmem[0, 128) and [128, 256)
       const int r = quarter * 32 + lane;
       float v[64];
@@ -1029,11 +1052,6 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
         const uint4 w = pack8(v + 8 * q8);
         st_shared_v4(sbase + Ly::kU + colhalf * 8192 + sw128_chunk(r, q8), w.x, w.y, w.z, w.w);
       }
-    } else if (tid == kPub && pend) {  // the previous package is complete: publish it
-      bulk_wait<0>();
-      fence_proxy_async_all();
-      st_release_u64(pend_flag, pend_tag);
-      pend = false;
     }
     for (int e = tid; e < 1024; e += kThreads) {  // Q+' = Q+ Diag(e^{a}) -> S0 region
       const int half = e >> 9, r = (e >> 3) & 63, q = e & 7;
@@ -1054,7 +1072,7 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       int ok = 1;
       __syncthreads();
       beta_r = beta_of(next);
-      if (tid == kPub && after >= 0) issue(after, st);  // before the stores, on the same engine
+      if (tid == kPub && after >= 0) issue_q(after, st);  // before the stores, on the same engine
       if (tid == kPub && n >= kCoopRing && slot_seen < coop_tag(a.epoch, n - kCoopRing))
         ok = coop_flag_wait(a.consumed + u * kCoopRing + slot, coop_tag(a.epoch, n - kCoopRing),
                             a.hdr + 1);
