@@ -542,6 +542,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t idesc_vneg = idesc_bf16(128, DV, 0, 1, 1);
   const uint32_t idesc_ke = idesc_bf16(128, DV, 1, 1);
 
+  // beta of row tid (threads 0..63) of the next kBetaAhead chunks, loaded
+  // in one burst every kBetaAhead chunks (a register load in flight holds up
+  // the next barrier, so its latency is paid once per burst)
+  constexpr int kBetaAhead = 8;
+  float beta_q[kBetaAhead];
 #pragma unroll 1
   for (int n = 0; n < nchunks; ++n) {
     const int st = n & 1;
@@ -549,7 +554,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sb = sbase + st * Ly::kStage;
     const int t0 = m.tok0 + n * kC;
     const int cl = min(kC, m.len - n * kC);
-    const float beta_n = tid < 64 ? load_beta(a.beta + (int64_t)t0 * H + h, H, cl, tid) : 0.f;
+    if (n % kBetaAhead == 0) {
+#pragma unroll
+      for (int k = 0; k < kBetaAhead; ++k)
+        beta_q[k] = (tid < 64 && n + k < nchunks)
+                        ? load_beta(a.beta + (int64_t)(t0 + k * kC) * H + h, H,
+                                    min(kC, m.len - (n + k) * kC), tid)
+                        : 0.f;
+    }
+    const float beta_n = beta_q[0];
+#pragma unroll
+    for (int k = 0; k + 1 < kBetaAhead; ++k) beta_q[k] = beta_q[k + 1];
 
     if (!cta_wait(bar_tma0 + 8 * st, (n >> 1) & 1)) { aborted = true; break; }
     tma_pending[st] = false;
