@@ -547,6 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the next barrier, so its latency is paid once per burst)
   constexpr int kBetaAhead = 8;
   float beta_q[kBetaAhead];
+  const int snap_every = a.snap_interval > 0 ? a.snap_interval / kC : 0;
+  int snap_left = snap_every;
+  int64_t snap_next = m.snap_off;
 #pragma unroll 1
   for (int n = 0; n < nchunks; ++n) {
     const int st = n & 1;
@@ -730,9 +733,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) S[p * 32 + j] = fmaf(egc, S[p * 32 + j], cke * v[j]);
       }
-      const int64_t done = (int64_t)n * kC + cl;
-      if (a.snap_interval > 0 && done % a.snap_interval == 0) {
-        const int64_t s = m.snap_off + done / a.snap_interval - 1;
+      // a snapshot after every snap_every full chunks (the interval is a
+      // multiple of the chunk, so a ragged last chunk never ends on one)
+      if (snap_every > 0 && --snap_left == 0 && cl == kC) {
+        snap_left = snap_every;
+        const int64_t s = snap_next++;
         if (s < a.snaps_capacity) {
           float4 *dst = reinterpret_cast<float4 *>(
               a.snaps + (((s * H + h) * kDK + c) * dv) + dv0 + col0);
@@ -1249,6 +1254,9 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
       }
       return true;
     };
+    const int snap_every = a.c.snap_interval > 0 ? a.c.snap_interval / kC : 0;
+    int snap_left = snap_every;
+    int64_t snap_next = m.snap_off;
     for (int n = 0; n < N; ++n) {
       const int b = n & 1;
       // bf16(S^T) -> S^T[b]: column q holds channels 2q (low half) and 2q + 1.
@@ -1312,10 +1320,12 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * b);
+      // a snapshot after every snap_every full chunks (the interval is a
+      // multiple of the chunk, so a ragged last chunk never ends on one)
       const int cl = min(kC, m.len - n * kC);
-      const int64_t done = (int64_t)n * kC + cl;
-      if (a.c.snap_interval > 0 && done % a.c.snap_interval == 0) {
-        const int64_t s = m.snap_off + done / a.c.snap_interval - 1;
+      if (snap_every > 0 && --snap_left == 0 && cl == kC) {
+        snap_left = snap_every;
+        const int64_t s = snap_next++;
         if (s < a.c.snaps_capacity) {
           float *d = a.c.snaps + (s * H + h) * kDK * dv + j;
 #pragma unroll
