@@ -27,7 +27,8 @@
 //         (the next chunk's tiles load while this one computes)
 //   prep  cumulative decay per channel, K+, Q+, K- (in place), S0'
 //   MMA1  [K+; Q+] K-^T                 M=128 N=64  K=128  -> A, Q+K-^T (TMEM)
-//   solve T = (I + A)^{-1} Diag(beta)    fp32, 16x16 blocks, CUDA cores
+//   solve T = (I + A)^{-1} Diag(beta)    fp32, 32x32 blocks, CUDA cores
+//         (an idle solve thread requests the next chunk's tiles)
 //   MMA2  [T; M] K+ and [T; M] V        -> W, U~ (TMEM)
 //   MMA3  U~ -= W S0'  (O = Q+ S0' was issued before the solve)
 //   MMA4  K-^T U       ;  O += M U
@@ -149,12 +150,17 @@ __device__ __forceinline__ float4 ld4s(const float *M, int r, int i) {
 // x[m + 1] is one multiply-add away.  T is written as bf16
 // into rows 0..63 of the K-major [T; M] operand at tm; the threads without a
 // diagonal column zero its upper block (the rows also hold the decay prefix
-// scratch of the chunk's preparation).  Ends with a barrier.
+// scratch of the chunk's preparation) and then run side(tid - 128), work of
+// the caller that does not touch the solve's buffers.  Ends with T fenced
+// for the tensor cores and a barrier.
+template <class Side>
 __device__ __forceinline__ void solve_T(const float *L, const float *LT, float *XT, float *Xd,
-                                        float *YT, const float *beta, uint8_t *tm, int tid) {
+                                        float *YT, const float *beta, uint8_t *tm, int tid,
+                                        const Side &side) {
   if (tid >= 128) {  // T's upper block: rows 0..31, 16-byte chunks 4..7
     const int e = tid - 128;
     *reinterpret_cast<uint4 *>(tm + sw128_chunk(e >> 2, 4 + (e & 3))) = make_uint4(0, 0, 0, 0);
+    side(e);
   } else {
     // warp w: block b = w / 2, columns 16 (w % 2) .. +15 of it; a column's
     // rows 0..15 belong to lane c, rows 16..31 to lane c + 16 (c = lane % 16)
@@ -255,6 +261,7 @@ __device__ __forceinline__ void solve_T(const float *L, const float *LT, float *
         st_bf(tm, sw128_offset(32 + i, j), v * beta[j]);
       }
   }
+  fence_async_smem();
   __syncthreads();
 }
 
@@ -571,11 +578,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (!cta_wait(bar_tma0 + 8 * st, (n >> 1) & 1)) { aborted = true; break; }
     tma_pending[st] = false;
-    if (n + 1 < nchunks) {  // the other stage was released at the end of chunk n-1
-      if (tid == 0) issue_tma(n + 1);
-      tma_pending[(n + 1) & 1] = true;
-      tma_parity[(n + 1) & 1] = ((n + 1) >> 1) & 1;
-    }
 
     // ------------------------------------------------------------ prep
     prep_chunk<Ly, DV>(sb, cl, beta_n, s_gpart, s_beta, s_tot, s_anc,
@@ -624,11 +626,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------ solve
+    // the next chunk's tiles go to the other stage (released at the end of
+    // chunk n-1), requested by a thread that the solve leaves idle
+    auto next_tiles = [&](int e) {
+      if (e == 0 && n + 1 < nchunks) issue_tma(n + 1);
+    };
     solve_T(Lm, reinterpret_cast<const float *>(smem + Ly::kLT), reinterpret_cast<float *>(smem + Ly::kU),
             reinterpret_cast<float *>(smem + Ly::kXd),
-            reinterpret_cast<float *>(smem + Ly::kYt), s_beta, smem + Ly::kTM, tid);
-    fence_async_smem();
-    __syncthreads();
+            reinterpret_cast<float *>(smem + Ly::kYt), s_beta, smem + Ly::kTM, tid, next_tiles);
+    if (n + 1 < nchunks) {
+      tma_pending[(n + 1) & 1] = true;
+      tma_parity[(n + 1) & 1] = ((n + 1) >> 1) & 1;
+    }
 
     // ------------------------------------------------------------ MMA2
     if (tid == 0) {
@@ -1008,22 +1017,39 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
                reinterpret_cast<float *>(smem + Ly::kLT), sbase + Ly::kTM);
     tc_fence_before();
     __syncthreads();
+    // while threads 0..127 solve for T, threads 128..255 stage the package
+    // operands that need only the prepared tiles: K^ = K- Diag(e^{G_C - a})
+    // into the upper half of the S0 region and Q+' = Q+ Diag(e^{a}) into its
+    // lower half (the previous package's stores finished before MMA1's wait)
+    auto stage_kq = [&](int e0) {
+      for (int e = e0; e < 1024; e += 128) {
+        const int half = e >> 9, r = (e >> 3) & 63, q = e & 7;
+        const uint32_t off = r * 128 + q * 16;
+        const float4 *f = reinterpret_cast<const float4 *>(s_cke + half * 64 + 8 * (q ^ (r & 7)));
+        const float4 f0 = f[0], f1 = f[1];
+        const uint4 w = ld_shared_v4(sb + Ly::kG + half * 8192 + off);
+        st_shared_v4(sbase + Ly::kS0 + 16384 + half * 8192 + off,
+                     pack_bf16x2(bf16lo(w.x) * f0.x, bf16hi(w.x) * f0.y),
+                     pack_bf16x2(bf16lo(w.y) * f0.z, bf16hi(w.y) * f0.w),
+                     pack_bf16x2(bf16lo(w.z) * f1.x, bf16hi(w.z) * f1.y),
+                     pack_bf16x2(bf16lo(w.w) * f1.z, bf16hi(w.w) * f1.w));
+      }
+      for (int e = e0; e < 1024; e += 128) {
+        const int half = e >> 9, r = (e >> 3) & 63, q = e & 7;
+        const uint32_t off = r * 128 + q * 16;
+        const float4 *f = reinterpret_cast<const float4 *>(s_ea + half * 64 + 8 * (q ^ (r & 7)));
+        const float4 f0 = f[0], f1 = f[1];
+        const uint4 w = ld_shared_v4(sb + Ly::kQ + half * 16384 + off);
+        st_shared_v4(sbase + Ly::kS0 + half * 8192 + off,
+                     pack_bf16x2(bf16lo(w.x) * f0.x, bf16hi(w.x) * f0.y),
+                     pack_bf16x2(bf16lo(w.y) * f0.z, bf16hi(w.y) * f0.w),
+                     pack_bf16x2(bf16lo(w.z) * f1.x, bf16hi(w.z) * f1.y),
+                     pack_bf16x2(bf16lo(w.w) * f1.z, bf16hi(w.w) * f1.w));
+      }
+    };
     solve_T(Lm, reinterpret_cast<const float *>(smem + Ly::kLT), reinterpret_cast<float *>(smem + Ly::kU),
             reinterpret_cast<float *>(smem + Ly::kXd),
-            reinterpret_cast<float *>(smem + Ly::kYt), s_beta, smem + Ly::kTM, tid);
-    for (int e = tid; e < 1024; e += kThreads) {  // K^ = K- Diag(e^{G_C - a}) -> solve scratch
-      const int half = e >> 9, r = (e >> 3) & 63, q = e & 7;
-      const uint32_t off = half * 8192 + r * 128 + q * 16;
-      const float4 *f = reinterpret_cast<const float4 *>(s_cke + half * 64 + 8 * (q ^ (r & 7)));
-      const float4 f0 = f[0], f1 = f[1];
-      const uint4 w = ld_shared_v4(sb + Ly::kG + off);
-      st_shared_v4(sbase + Ly::kScr + off, pack_bf16x2(bf16lo(w.x) * f0.x, bf16hi(w.x) * f0.y),
-                   pack_bf16x2(bf16lo(w.y) * f0.z, bf16hi(w.y) * f0.w),
-                   pack_bf16x2(bf16lo(w.z) * f1.x, bf16hi(w.z) * f1.y),
-                   pack_bf16x2(bf16lo(w.w) * f1.z, bf16hi(w.w) * f1.w));
-    }
-    fence_async_smem();
-    __syncthreads();
+            reinterpret_cast<float *>(smem + Ly::kYt), s_beta, smem + Ly::kTM, tid, stage_kq);
     if (tid == 0) {
       issue_mma2<Ly, 128>(tmem, sbase + Ly::kTM, sb);
       mma_commit(bar_mma);
@@ -1040,9 +1066,9 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     tc_fence_after();
     // The package is staged in shared memory in its final layout, outside
     // both input stages, then written out with bulk copies: W^ = W Diag(e^{a})
-    // in the W buffer, K^ in the solve scratch, U~ in the U buffer,
-    // Q+' = Q+ Diag(e^{a}) in the S0 region, M where the solve left it and
-    // e^{G_C} in the e^{G_C - a} vector.
+    // in the W buffer, U~ in the U buffer, K^ and Q+' in the S0 region (staged
+    // during the solve), M where the solve left it and e^{G_C} in the
+    // e^{G_C - a} vector.
     // the chunk two ahead goes to this chunk's stage: its k, v and g tiles are
     // dead now (q is read once more, below), and thread kPub's warp has no
     // rows to stage
@@ -1073,17 +1099,6 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
         st_shared_v4(sbase + Ly::kU + colhalf * 8192 + sw128_chunk(r, q8), w.x, w.y, w.z, w.w);
       }
     }
-    for (int e = tid; e < 1024; e += kThreads) {  // Q+' = Q+ Diag(e^{a}) -> S0 region
-      const int half = e >> 9, r = (e >> 3) & 63, q = e & 7;
-      const uint32_t off = r * 128 + q * 16;
-      const float4 *f = reinterpret_cast<const float4 *>(s_ea + half * 64 + 8 * (q ^ (r & 7)));
-      const float4 f0 = f[0], f1 = f[1];
-      const uint4 w = ld_shared_v4(sb + Ly::kQ + half * 16384 + off);
-      st_shared_v4(sbase + Ly::kS0 + half * 8192 + off, pack_bf16x2(bf16lo(w.x) * f0.x, bf16hi(w.x) * f0.y),
-                   pack_bf16x2(bf16lo(w.y) * f0.z, bf16hi(w.y) * f0.w),
-                   pack_bf16x2(bf16lo(w.z) * f1.x, bf16hi(w.z) * f1.y),
-                   pack_bf16x2(bf16lo(w.w) * f1.z, bf16hi(w.w) * f1.w));
-    }
     if (tid < 128) s_cke[tid] = expf(s_tot[tid]);  // e^{G_C} for the package
     tc_fence_before();
     fence_async_smem();  // the staged package, for the bulk stores
@@ -1096,13 +1111,13 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       if (tid == kPub && n >= kCoopRing && slot_seen < coop_tag(a.epoch, n - kCoopRing))
         ok = coop_flag_wait(a.consumed + u * kCoopRing + slot, coop_tag(a.epoch, n - kCoopRing),
                             a.hdr + 1);
-      // the package, piece by piece from where it was staged (W, U, solve
-      // scratch, S0 region, M, e^{G_C}); these are first overwritten after
+      // the package, piece by piece from where it was staged (W, S0 region,
+      // U, M, e^{G_C}); these are first overwritten after
       // the next chunk's first MMA, where thread kPub waits for the stores
       if (tid == kPub && ok) {
         uint8_t *pk = a.ring + ((size_t)u * kCoopRing + slot) * kCoopPkgBytes;
         bulk_s2g(pk + kPkW, sbase + Ly::kW, 16384);
-        bulk_s2g(pk + kPkKm, sbase + Ly::kScr, 16384);
+        bulk_s2g(pk + kPkKm, sbase + Ly::kS0 + 16384, 16384);
         bulk_s2g(pk + kPkU, sbase + Ly::kU, 16384);
         bulk_s2g(pk + kPkQ, sbase + Ly::kS0, 16384);
         bulk_s2g(pk + kPkM, sbase + Ly::kTM + 8192, 8192);
