@@ -8,8 +8,10 @@ One step is one ``kda_prefill_varlen`` call on the single-sequence prefill
 workload (B=1, T=8192, H=32, dk=dv=128, bf16, snapshots every 1024 tokens):
 the device-side plan kernel plus the chunked prefill kernel, which write the
 outputs, the 8 snapshots and the final state.  The same run also times the
-batched decode (256 sequences x 1 token) and the speculative-verify decode
-(64 x 8 tokens with per-token states) and reports them under "decode".
+batched decode (256 sequences x 1 token), the speculative-verify decode
+(64 x 8 tokens with per-token states) and the speculative verify with the
+previous step's commit folded in (64 x 8 tokens, kda_decode_spec) and
+reports them under "decode".
 Inputs are synthetic (seeded, see hybrid_linear_attention_delta_gb300/inputs.py).
 L2 is flushed (a 256 MiB write) between timed steps.  ``--impl reference``
 times the fp64 CPU oracle on a bounded sample of the same workload instead.
@@ -72,6 +74,21 @@ def prefill_algorithmic(w, lens, n_snaps, n_resumed, es):
     C = 64
     flops = T * H * (5 * 2 * C * dk + 3 * 2 * dk * dv)
     return nbytes, flops, T * H * per_tok
+
+
+def spec_algorithmic(w, N, accepted, es):
+    """Bytes of one speculative verify with commit: each touched state read
+    once, written once when its sequence accepted at least one token, the
+    replayed tokens' k, v, g, beta and the verified tokens' q, k, v, g, beta
+    and outputs."""
+    H, dk, dv = w.H, w.dk, w.dv
+    state = dk * dv * 4
+    n_write = int((accepted > 0).sum())
+    replayed = int(accepted.sum())
+    b = N * H * state + n_write * H * state
+    b += replayed * H * (2 * dk + dv + 1) * es
+    b += N * w.n_tok * H * (3 * dk + 2 * dv + 1) * es
+    return b
 
 
 def decode_algorithmic(w, N, n_tok, per_tok, es):
@@ -291,15 +308,27 @@ def bench_decode(name, args, torch, kda, inputs):
     ws = kda.workspace_for(N, H, pool.shape[0])
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
 
-    def call(events):
-        kda.kda_decode(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], slot_ids, pool, out,
-                       w.n_tok, per, workspace=ws, events=events)
+    if w.spec:
+        prev = {n: t.cuda() for n, t in b.extra["prev"].items()}
+        acc = b.extra["accepted"].cuda()
+
+        def call(events):
+            kda.kda_decode_spec(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], slot_ids,
+                                pool, out, w.n_tok, prev["k"], prev["v"], prev["g"],
+                                prev["beta"], acc, w.n_tok, workspace=ws, events=events)
+    else:
+        def call(events):
+            kda.kda_decode(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], slot_ids, pool,
+                           out, w.n_tok, per, workspace=ws, events=events)
 
     call_ms, kern_ms = time_calls(call, args.steps, args.warmup, flush, torch)
     st, bits = kda.kda_device_status(ws)
     if st != kda.KDA_OK:
         raise RuntimeError(f"decode device check failed: {st} bits={bits}")
-    nbytes = decode_algorithmic(w, N, w.n_tok, w.per_tok_states, dev["q"].element_size())
+    if w.spec:
+        nbytes = spec_algorithmic(w, N, b.extra["accepted"], dev["q"].element_size())
+    else:
+        nbytes = decode_algorithmic(w, N, w.n_tok, w.per_tok_states, dev["q"].element_size())
     return dict(w=w, N=N, call_ms=call_ms, kern_ms=kern_ms, nbytes=nbytes)
 
 
@@ -406,7 +435,7 @@ def main():
 
     dec = {}
     if not args.no_decode:
-        for name in ("decode_256x1", "verify_64x8"):
+        for name in ("decode_256x1", "verify_64x8", "spec_verify_64x8"):
             r = bench_decode(name, args, torch, kda, inputs)
             ks = statistics.mean(r["kern_ms"]) / 1e3
             cs = statistics.mean(r["call_ms"]) / 1e3

@@ -22,8 +22,10 @@ KDA_F32, KDA_BF16 = 0, 1
 KDA_ALGO_AUTO, KDA_ALGO_RECURRENT, KDA_ALGO_CHUNKED, KDA_ALGO_CHUNKED_PER_STATE, \
     KDA_ALGO_CHUNKED_COOP = range(5)
 
-EXPORTS = ("kda_prefill_varlen", "kda_decode", "kda_workspace_bytes", "kda_snapshot_count",
-           "kda_device_status", "kda_status_string", "kda_last_launch_count")
+EXPORTS = ("kda_prefill_varlen", "kda_prefill_varlen_retain", "kda_decode", "kda_decode_spec",
+           "kda_workspace_bytes",
+           "kda_snapshot_count", "kda_device_status", "kda_status_string",
+           "kda_last_launch_count")
 
 
 class KdaArgs(ctypes.Structure):
@@ -58,6 +60,8 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
         A = ctypes.POINTER(KdaArgs)
         L.kda_prefill_varlen.argtypes = [V, V, V, V, V, V, V, V, V, I32, V, A]
         L.kda_prefill_varlen.restype = ctypes.c_int
+        L.kda_prefill_varlen_retain.argtypes = [V, V, V, V, V, V, V, V, V, I32, V, A]
+        L.kda_prefill_varlen_retain.restype = ctypes.c_int
         L.kda_decode.argtypes = [V, V, V, V, V, V, V, V, I32, V, A]
         L.kda_decode.restype = ctypes.c_int
         L.kda_workspace_bytes.argtypes = [A]
@@ -72,6 +76,8 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
         L.kda_last_launch_count.restype = I32
         L.kda_decode_noalloc.argtypes = [V, V, V, V, V, V, V, V, I32, V, V, A]
         L.kda_decode_noalloc.restype = ctypes.c_int
+        L.kda_decode_spec.argtypes = [V, V, V, V, V, V, V, V, I32, V, V, V, V, V, I32, A]
+        L.kda_decode_spec.restype = ctypes.c_int
         if path:
             return L
         _lib = L
@@ -160,6 +166,23 @@ def kda_prefill_varlen(q, k, v, g, beta, cu_seqlens, init_slots, state_pool, out
         raise KdaError(st, "kda_prefill_varlen")
 
 
+def kda_prefill_varlen_retain(q, k, v, g, beta, cu_seqlens, init_slots, state_pool, out,
+                              snap_interval: int, snap_slots, *, workspace, stream=None,
+                              algo: int = KDA_ALGO_AUTO, events=None) -> None:
+    """kda_prefill_varlen with a retention map (see kda_prefill_varlen_retain
+    in include/kda.h): snap_slots[s] is the pool slot of snapshot s, or -1."""
+    a = make_args(B=cu_seqlens.numel() - 1, T_total=q.shape[0], H=q.shape[1], dk=q.shape[2],
+                  dv=v.shape[2], n_slots=state_pool.shape[0], dtype=_dtype_code(q), algo=algo,
+                  snaps_capacity=0 if snap_slots is None else snap_slots.numel(), stream=stream,
+                  workspace=workspace, events=events)
+    st = lib().kda_prefill_varlen_retain(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                         _ptr(cu_seqlens), _ptr(init_slots), _ptr(state_pool),
+                                         _ptr(out), int(snap_interval), _ptr(snap_slots),
+                                         ctypes.byref(a))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prefill_varlen_retain")
+
+
 def kda_decode(q, k, v, g, beta, slot_ids, state_pool, out, n_tok: int = 1,
                per_tok_states=None, *, workspace, stream=None, events=None) -> None:
     """In-place decode of n_tok tokens per sequence (see kda_decode in include/kda.h)."""
@@ -171,6 +194,32 @@ def kda_decode(q, k, v, g, beta, slot_ids, state_pool, out, n_tok: int = 1,
                           ctypes.byref(a))
     if st != KDA_OK:
         raise KdaError(st, "kda_decode")
+
+
+def kda_decode_spec(q, k, v, g, beta, slot_ids, state_pool, out, n_tok: int, k_prev=None,
+                    v_prev=None, g_prev=None, beta_prev=None, accepted_prev=None,
+                    n_prev: int = 0, *, workspace, stream=None, events=None,
+                    H: Optional[int] = None, dk: Optional[int] = None,
+                    dv: Optional[int] = None, dtype: Optional[int] = None) -> None:
+    """Speculative verify with the commit of the previous step folded in (see
+    kda_decode_spec in include/kda.h): replays accepted_prev[n] tokens of the
+    previous step onto slot_ids[n], writes that state, then writes the outputs
+    of this step's n_tok tokens without advancing the slot.  With n_tok == 0
+    (commit only) q, k, v, g, beta and out may be None and the shape keywords
+    H / dk / dv / dtype describe the call instead."""
+    ref = q if q is not None else k_prev
+    vref = v if v is not None else v_prev
+    a = make_args(B=slot_ids.numel(), T_total=slot_ids.numel() * int(n_tok),
+                  H=H or ref.shape[1], dk=dk or ref.shape[2], dv=dv or vref.shape[2],
+                  n_slots=state_pool.shape[0],
+                  dtype=dtype if dtype is not None else _dtype_code(ref),
+                  stream=stream, workspace=workspace, events=events)
+    st = lib().kda_decode_spec(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(slot_ids),
+                               _ptr(state_pool), _ptr(out), int(n_tok), _ptr(k_prev),
+                               _ptr(v_prev), _ptr(g_prev), _ptr(beta_prev), _ptr(accepted_prev),
+                               int(n_prev), ctypes.byref(a))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_spec")
 
 
 def kda_decode_noalloc(q, k, v, g, beta, slot_ids, state_pool, out, n_tok: int = 1,

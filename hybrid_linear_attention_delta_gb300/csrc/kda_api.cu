@@ -66,18 +66,27 @@ int64_t kda_snapshot_count(const int32_t *cu, int32_t B, int32_t snap_interval) 
   return n;
 }
 
-kda_status kda_prefill_varlen(const void *q, const void *k, const void *v, const void *g,
-                              const void *beta, const int32_t *cu_seqlens,
-                              const int32_t *init_slots, float *state_pool, void *out,
-                              int32_t snap_interval, float *snaps, const kda_args *a) {
+}  // extern "C"
+
+namespace {
+
+// Both prefill entry points: snapshots go to the dense buffer snaps, or, with
+// a retention map snap_slots, into the pool slots it names (exactly one of the
+// two is non-NULL when the call takes snapshots).
+kda_status prefill(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                   const int32_t *cu_seqlens, const int32_t *init_slots, float *state_pool,
+                   void *out, int32_t snap_interval, float *snaps, const int32_t *snap_slots,
+                   const kda_args *a) {
   g_last_launches = 0;
   kda_status st = check_common(a);
   if (st != KDA_OK) return st;
-  // snaps may be NULL with an interval only when its capacity is 0 (a batch
-  // whose sequences are all shorter than the interval)
+  // the snapshot target may be NULL with an interval only when its capacity
+  // is 0 (a batch whose sequences are all shorter than the interval)
+  const bool target = snaps || snap_slots;
   if (snap_interval < 0 || a->snaps_capacity < 0) return KDA_ERR_INVALID_ARG;
-  if (snap_interval == 0 && snaps) return KDA_ERR_INVALID_ARG;
-  if (snap_interval > 0 && !snaps && a->snaps_capacity > 0) return KDA_ERR_INVALID_ARG;
+  if (snaps && snap_slots) return KDA_ERR_INVALID_ARG;
+  if (snap_interval == 0 && target) return KDA_ERR_INVALID_ARG;
+  if (snap_interval > 0 && !target && a->snaps_capacity > 0) return KDA_ERR_INVALID_ARG;
   if (snaps && !aligned16(snaps)) return KDA_ERR_INVALID_ARG;
   if (a->algo < KDA_ALGO_AUTO || a->algo > KDA_ALGO_CHUNKED_COOP) return KDA_ERR_INVALID_ARG;
   if (a->B == 0) return a->T_total == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
@@ -91,9 +100,9 @@ kda_status kda_prefill_varlen(const void *q, const void *k, const void *v, const
   std::memset(&p, 0, sizeof(p));
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
   p.cu_seqlens = cu_seqlens; p.init_slots = init_slots;
-  p.pool = state_pool; p.out = out; p.snaps = snaps;
+  p.pool = state_pool; p.out = out; p.snaps = snaps; p.snap_slots = snap_slots;
   p.snap_interval = snap_interval;
-  p.snaps_capacity = snaps ? a->snaps_capacity : 0;
+  p.snaps_capacity = target ? a->snaps_capacity : 0;
   p.B = a->B; p.T_total = a->T_total; p.H = a->H; p.dk = a->dk; p.dv = a->dv;
   p.n_slots = a->n_slots; p.dtype = a->dtype;
   p.err = reinterpret_cast<uint32_t *>(ws);
@@ -127,6 +136,27 @@ kda_status kda_prefill_varlen(const void *q, const void *k, const void *v, const
   return st;
 }
 
+}  // namespace
+
+extern "C" {
+
+kda_status kda_prefill_varlen(const void *q, const void *k, const void *v, const void *g,
+                              const void *beta, const int32_t *cu_seqlens,
+                              const int32_t *init_slots, float *state_pool, void *out,
+                              int32_t snap_interval, float *snaps, const kda_args *a) {
+  return prefill(q, k, v, g, beta, cu_seqlens, init_slots, state_pool, out, snap_interval, snaps,
+                 nullptr, a);
+}
+
+kda_status kda_prefill_varlen_retain(const void *q, const void *k, const void *v, const void *g,
+                                     const void *beta, const int32_t *cu_seqlens,
+                                     const int32_t *init_slots, float *state_pool, void *out,
+                                     int32_t snap_interval, const int32_t *snap_slots,
+                                     const kda_args *a) {
+  return prefill(q, k, v, g, beta, cu_seqlens, init_slots, state_pool, out, snap_interval,
+                 nullptr, snap_slots, a);
+}
+
 kda_status kda_decode(const void *q, const void *k, const void *v, const void *g,
                       const void *beta, const int32_t *slot_ids, float *state_pool, void *out,
                       int32_t n_tok, float *per_tok_states, const kda_args *a) {
@@ -151,6 +181,49 @@ kda_status kda_decode(const void *q, const void *k, const void *v, const void *g
   p.claims = reinterpret_cast<uint32_t *>(ws + lay.claims_off);
   p.epoch = next_epoch();
   p.stream = static_cast<cudaStream_t>(a->stream);
+  const bool fast = a->dk == 128 && a->dv == 128;
+  record(a->ev_begin, p.stream);
+  st = from_cuda(fast ? kda::launch_decode128(p) : kda::launch_recurrent_decode(p));
+  record(a->ev_end, p.stream);
+  if (st == KDA_OK) g_last_launches = 1;
+  return st;
+}
+
+kda_status kda_decode_spec(const void *q, const void *k, const void *v, const void *g,
+                           const void *beta, const int32_t *slot_ids, float *state_pool,
+                           void *out, int32_t n_tok, const void *k_prev, const void *v_prev,
+                           const void *g_prev, const void *beta_prev,
+                           const int32_t *accepted_prev, int32_t n_prev, const kda_args *a) {
+  g_last_launches = 0;
+  kda_status st = check_common(a);
+  if (st != KDA_OK) return st;
+  if (n_tok < 0 || n_prev < 0 || (int64_t)a->B * n_tok != a->T_total) return KDA_ERR_INVALID_ARG;
+  if (a->B == 0) return KDA_OK;
+  if (!slot_ids || !state_pool || !aligned16(state_pool)) return KDA_ERR_INVALID_ARG;
+  if ((st = check_tokens(q, k, v, g, beta, out, a->T_total)) != KDA_OK) return st;
+  if (n_prev > 0) {
+    const void *ps[] = {k_prev, v_prev, g_prev, beta_prev};
+    for (const void *p : ps)
+      if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    if (!accepted_prev) return KDA_ERR_INVALID_ARG;
+  }
+
+  const kda::WorkspaceLayout lay(a->B, a->H, a->n_slots);
+  char *ws = static_cast<char *>(a->workspace);
+  kda::DecodePlan p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+  p.slot_ids = slot_ids; p.pool = state_pool; p.out = out; p.per_tok = nullptr;
+  p.N = a->B; p.n_tok = n_tok; p.H = a->H; p.dk = a->dk; p.dv = a->dv;
+  p.n_slots = a->n_slots; p.dtype = a->dtype;
+  p.err = reinterpret_cast<uint32_t *>(ws);
+  p.claims = reinterpret_cast<uint32_t *>(ws + lay.claims_off);
+  p.epoch = next_epoch();
+  p.stream = static_cast<cudaStream_t>(a->stream);
+  p.spec = 1;
+  p.n_prev = n_prev;
+  p.k_prev = k_prev; p.v_prev = v_prev; p.g_prev = g_prev; p.beta_prev = beta_prev;
+  p.accepted = accepted_prev;
   const bool fast = a->dk == 128 && a->dv == 128;
   record(a->ev_begin, p.stream);
   st = from_cuda(fast ? kda::launch_decode128(p) : kda::launch_recurrent_decode(p));

@@ -34,7 +34,8 @@
 //   MMA4  K-^T U       ;  O += M U
 //   out   o rows -> global bf16; S = Diag(e^{G_C}) S + Diag(e^{G_C - a}) K-^T U
 //         (= K_end^T U with K_end = K e^{G_C - G}) in registers;
-//         snapshot / final state -> global fp32
+//         snapshot (dense buffer or retained pool slot) / final state ->
+//         global fp32
 // All MMAs are M = 128 (rows 64..127 of the 64-row operands are ignored).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -94,6 +95,7 @@ struct ChunkArgs {
   float *pool;
   __nv_bfloat16 *out;
   float *snaps;
+  const int32_t *snap_slots;  // retention map, or NULL (dense snapshots)
   int64_t snaps_capacity;
   int32_t snap_interval;
   int32_t H, dv, n_dvb;
@@ -748,11 +750,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         snap_left = snap_every;
         const int64_t s = snap_next++;
         if (s < a.snaps_capacity) {
-          float4 *dst = reinterpret_cast<float4 *>(
-              a.snaps + (((s * H + h) * kDK + c) * dv) + dv0 + col0);
+          float *base = snapshot_base(a.snaps, a.snap_slots, a.pool, s, H, h, (int64_t)kDK * dv);
+          if (base) {
+            float4 *dst = reinterpret_cast<float4 *>(base + (int64_t)c * dv + dv0 + col0);
 #pragma unroll
-          for (int j = 0; j < NH / 4; ++j)
-            dst[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+            for (int j = 0; j < NH / 4; ++j)
+              dst[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+          }
         } else if (tid == 0) {
           raise_error(a.err, ERR_SNAP_CAPACITY);
         }
@@ -1342,9 +1346,13 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
         snap_left = snap_every;
         const int64_t s = snap_next++;
         if (s < a.c.snaps_capacity) {
-          float *d = a.c.snaps + (s * H + h) * kDK * dv + j;
+          float *base =
+              snapshot_base(a.c.snaps, a.c.snap_slots, a.c.pool, s, H, h, (int64_t)kDK * dv);
+          if (base) {
+            float *d = base + j;
 #pragma unroll
-          for (int c = 0; c < kDK; ++c) d[c * cs] = S[c];
+            for (int c = 0; c < kDK; ++c) d[c * cs] = S[c];
+          }
         } else if (j == 0) {
           raise_error(a.c.err, ERR_SNAP_CAPACITY);
         }
@@ -1505,6 +1513,7 @@ cudaError_t launch_dv(const PrefillPlan &p, const CUtensorMap &mq, const CUtenso
   a.pool = p.pool;
   a.out = static_cast<__nv_bfloat16 *>(p.out);
   a.snaps = p.snaps;
+  a.snap_slots = p.snap_slots;
   a.snaps_capacity = p.snaps_capacity;
   a.snap_interval = p.snap_interval;
   a.H = p.H;
@@ -1546,6 +1555,7 @@ cudaError_t launch_coop(const PrefillPlan &p, int grid, const CUtensorMap &mq,
   a.c.pool = p.pool;
   a.c.out = static_cast<__nv_bfloat16 *>(p.out);
   a.c.snaps = p.snaps;
+  a.c.snap_slots = p.snap_slots;
   a.c.snaps_capacity = p.snaps_capacity;
   a.c.snap_interval = p.snap_interval;
   a.c.H = p.H;

@@ -28,6 +28,7 @@ enum ErrBits : uint32_t {
   ERR_SNAP_CAPACITY = 8u,
   ERR_TIMEOUT = 16u,
   ERR_DECAY_RANGE = 32u,
+  ERR_BAD_ACCEPT = 64u,
 };
 
 struct SeqMeta {
@@ -90,6 +91,21 @@ __device__ __forceinline__ bool claim_state(uint32_t *claims, int64_t index, uin
   return atomicExch(claims + index, epoch) != epoch;
 }
 
+// Where snapshot s of head h is written: the dense snapshot buffer, or, when
+// the caller passed a retention map (snap_slots), the pool slot snap_slots[s]
+// (nullptr: this snapshot is not retained).  Slots in the map were range
+// checked and claimed by the plan kernel; a sequence with a bad one is
+// skipped before any kernel gets here.
+__device__ __forceinline__ float *snapshot_base(float *snaps, const int32_t *snap_slots,
+                                                float *pool, int64_t s, int H, int h,
+                                                int64_t state_elems) {
+  if (snap_slots) {
+    const int slot = snap_slots[s];
+    return slot >= 0 ? pool + ((int64_t)slot * H + h) * state_elems : nullptr;
+  }
+  return snaps + (s * H + h) * state_elems;
+}
+
 // ---------------------------------------------------------------- launchers
 struct PrefillPlan {
   const void *q, *k, *v, *g, *beta;
@@ -97,6 +113,10 @@ struct PrefillPlan {
   float *pool;
   void *out;
   float *snaps;
+  // retention map [snaps_capacity] (kda_prefill_varlen_retain): snapshot s
+  // goes to pool slot snap_slots[s], or nowhere when it is -1; NULL: the
+  // dense snaps buffer
+  const int32_t *snap_slots;
   int32_t snap_interval;
   int64_t snaps_capacity;
   int32_t B, T_total, H, dk, dv, n_slots, dtype;
@@ -123,6 +143,14 @@ struct DecodePlan {
   uint32_t *claims;
   uint32_t epoch;
   cudaStream_t stream;
+  // speculative verify with commit (spec != 0): sequence n first replays the
+  // accepted[n] leading tokens of the previous verify step (rows n * n_prev +
+  // j of k_prev, v_prev, g_prev, beta_prev), writes the slot once after them,
+  // then runs this step's n_tok tokens for their outputs only (the slot is not
+  // advanced past the committed state).  accepted may be NULL when n_prev == 0.
+  int32_t spec, n_prev;
+  const void *k_prev, *v_prev, *g_prev, *beta_prev;
+  const int32_t *accepted;
 };
 
 cudaError_t launch_meta(const PrefillPlan &p);

@@ -11,6 +11,9 @@
 //     duplicate destinations and sources that another sequence overwrites;
 //   * computes each sequence's first snapshot index (exclusive scan of
 //     floor(L_b / snap_interval)) and checks it against the snaps buffer;
+//   * with a retention map, range checks and claims the pool slot of every
+//     retained snapshot (one thread per snapshot), so that a snapshot slot
+//     shared with another snapshot, a destination or a source is refused;
 //   * orders sequences longest first, so the longest serial chains start
 //     first on a skewed varlen batch.
 #include "kda_internal.cuh"
@@ -66,20 +69,7 @@ __global__ void __launch_bounds__(kMetaThreads) meta_kernel(PrefillPlan p) {
   __threadfence_block();
   __syncthreads();
 
-  // 3. a source that another sequence of this call overwrites would race
-  for (int b = tid; b < B; b += kMetaThreads) {
-    SeqMeta m = p.meta[b];
-    if (m.ok && m.src >= 0 && m.src != m.dst) {
-      const uint32_t stamp = atomicAdd(p.claims + (int64_t)m.src * claim_stride, 0u);
-      if (stamp == p.epoch) {
-        raise_error(p.err, ERR_DUP_SLOT);
-        p.meta[b].ok = 0;
-      }
-    }
-  }
-  __syncthreads();
-
-  // 4. snapshot offsets: exclusive scan of floor(len / interval), tile by tile
+  // 3. snapshot offsets: exclusive scan of floor(len / interval), tile by tile
   if (tid == 0) carry = 0;
   __syncthreads();
   __shared__ long long scan[kMetaThreads];
@@ -108,7 +98,46 @@ __global__ void __launch_bounds__(kMetaThreads) meta_kernel(PrefillPlan p) {
     __syncthreads();
   }
 
-  // 5. cooperative-mode header: ticket and abort cleared, longest sequence in chunks
+  // 4. retention map: snapshot s belongs to the last sequence whose first
+  // snapshot index is <= s (that sequence has at least one snapshot); a slot
+  // out of range or already claimed in this call refuses the sequence
+  if (p.snap_slots) {
+    const long long n_snap = carry < p.snaps_capacity ? carry : p.snaps_capacity;
+    for (long long s = tid; s < n_snap; s += kMetaThreads) {
+      const int slot = p.snap_slots[s];
+      if (slot == -1) continue;
+      int lo = 0, hi = B - 1;
+      while (lo < hi) {  // largest b with snap_off[b] <= s
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.meta[mid].snap_off <= s) lo = mid; else hi = mid - 1;
+      }
+      if (slot < -1 || slot >= p.n_slots) {
+        raise_error(p.err, ERR_BAD_SLOT);
+        p.meta[lo].ok = 0;
+      } else if (!claim_state(p.claims, (int64_t)slot * claim_stride, p.epoch)) {
+        raise_error(p.err, ERR_DUP_SLOT);
+        p.meta[lo].ok = 0;
+      }
+    }
+    __threadfence_block();
+    __syncthreads();
+  }
+
+  // 5. a source that another sequence of this call overwrites (as its
+  // destination or a retained snapshot) would race
+  for (int b = tid; b < B; b += kMetaThreads) {
+    SeqMeta m = p.meta[b];
+    if (m.ok && m.src >= 0 && m.src != m.dst) {
+      const uint32_t stamp = atomicAdd(p.claims + (int64_t)m.src * claim_stride, 0u);
+      if (stamp == p.epoch) {
+        raise_error(p.err, ERR_DUP_SLOT);
+        p.meta[b].ok = 0;
+      }
+    }
+  }
+  __syncthreads();
+
+  // 6. cooperative-mode header: ticket and abort cleared, longest sequence in chunks
   if (p.coop_hdr) {
     int mx = 0;
     for (int b = tid; b < B; b += kMetaThreads) {
@@ -127,7 +156,7 @@ __global__ void __launch_bounds__(kMetaThreads) meta_kernel(PrefillPlan p) {
     }
   }
 
-  // 6. longest first (stable: ties keep batch order)
+  // 7. longest first (stable: ties keep batch order)
   for (int b = tid; b < B; b += kMetaThreads) {
     int rank = b;
     if (B <= kMaxSortedB) {

@@ -13,6 +13,10 @@ Recipe (the same for every workload; sizes come from ``WORKLOADS``):
 * All five are cast to the workload dtype (bf16 or fp32) at the end; the oracle
   reads the cast values back exactly.
 * Pool states ~ N(0, 0.1) (standard deviation 0.1), fp32.
+* Speculative verify with commit: the previous step's tokens are drawn with
+  the same recipe under the workload index + 100, and its accepted lengths
+  are integers uniform in [1, n_tok] (the first verified token is always
+  kept).
 * Each field has its own ``torch.Generator`` seeded with
   ``(20260000 + workload_index) * 100 + field_id`` so fields do not depend on
   the order they are drawn in (a varlen batch needs its lengths before the
@@ -29,7 +33,7 @@ from typing import List, Optional
 
 import torch
 
-F_Q, F_K, F_V, F_G, F_BETA, F_LENS, F_SLOTS, F_POOL, F_RESUME = range(9)
+F_Q, F_K, F_V, F_G, F_BETA, F_LENS, F_SLOTS, F_POOL, F_RESUME, F_ACCEPT = range(10)
 
 
 @dataclass(frozen=True)
@@ -50,6 +54,7 @@ class Workload:
     n_resume: int = 0             # how many sequences resume from a cached slot
     n_tok: int = 1                # decode tokens per sequence
     per_tok_states: bool = False
+    spec: bool = False            # decode: verify with commit of a previous step
     note: str = ""
 
 
@@ -70,6 +75,10 @@ WORKLOADS = {
     "verify_64x8": Workload("verify_64x8", 3, "decode", H=32, dk=128, dv=128, dtype="bf16",
                             B=64, n_slots=1024, n_tok=8, per_tok_states=True,
                             note="64 seqs x 8 tokens (7 draft + 1), per-token states"),
+    "spec_verify_64x8": Workload("spec_verify_64x8", 3, "decode", H=32, dk=128, dv=128,
+                                 dtype="bf16", B=64, n_slots=1024, n_tok=8, spec=True,
+                                 note="64 seqs x 8 tokens verified, commit of the previous "
+                                      "step's accepted tokens (1..8) in the same call"),
     "prefill_1m": Workload("prefill_1m", 4, "prefill", H=16, dk=128, dv=128, dtype="bf16", B=1,
                            T=1 << 20, snap_interval=32768,
                            note="B=1 T=2^20 H=16 dk=dv=128 bf16, snapshots every 32768"),
@@ -185,4 +194,9 @@ def make_batch(w: Workload, device="cpu", lengths: Optional[List[int]] = None,
     gen = _gen(w.index, F_SLOTS, "cpu")
     slot_ids = torch.randperm(w.n_slots, generator=gen)[:N].to(torch.int32)
     cu = torch.arange(N + 1, dtype=torch.int32) * w.n_tok
-    return Batch(cu_seqlens=cu, slot_ids=slot_ids, pool=pool, **tt)
+    extra = {}
+    if w.spec:
+        extra["prev"] = token_tensors(N * w.n_tok, H, w.dk, w.dv, dt, w.index + 100, device)
+        agen = _gen(w.index, F_ACCEPT, "cpu")
+        extra["accepted"] = torch.randint(1, w.n_tok + 1, (N,), generator=agen).to(torch.int32)
+    return Batch(cu_seqlens=cu, slot_ids=slot_ids, pool=pool, extra=extra, **tt)

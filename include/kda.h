@@ -140,6 +140,35 @@ kda_status kda_prefill_varlen(const void *q, const void *k, const void *v, const
                               int32_t snap_interval, float *snaps, const kda_args *a);
 
 /*
+ * kda_prefill_varlen with a snapshot retention map: the same computation, but
+ * each snapshot either goes straight into a pool slot or is not written.
+ *
+ * Retention follows "Kimi K3 + vLLM: Inside the Day-0 Production
+ * Integration", section "Interval-Based and Marconi-Style Retention": a
+ * serving scheduler keeps states at a fixed token interval (the prompt
+ * boundary always) or only for prefixes seen a second time, so most interval
+ * positions of a long prompt need no state.  The scheduler's decision, made
+ * before the call, is the map; the final state still always goes to dst.
+ *
+ * snap_slots [n_snaps] int32 (device)  for snapshot s, numbered as for the
+ *                                      snaps buffer of kda_prefill_varlen
+ *                                      (sequence-major, then position):
+ *                                      -1 = not retained, else the pool slot
+ *                                      that receives the state, written like a
+ *                                      final state ([H][dk][dv] fp32)
+ * a->snaps_capacity                    entries of snap_slots (>= n_snaps)
+ * All other arguments are those of kda_prefill_varlen.  A retained slot must
+ * be in [0, n_slots) and may not be any sequence's src or dst nor another
+ * retained snapshot's slot; a violation is a device-side error (bit 1 or 2)
+ * and the sequence that owns the offending snapshot is skipped.
+ */
+kda_status kda_prefill_varlen_retain(const void *q, const void *k, const void *v, const void *g,
+                                     const void *beta, const int32_t *cu_seqlens,
+                                     const int32_t *init_slots, float *state_pool, void *out,
+                                     int32_t snap_interval, const int32_t *snap_slots,
+                                     const kda_args *a);
+
+/*
  * Single- and multi-token decode in place on the state pool (the fused decode
  * step of "Kimi K3 on vLLM: Up to 370 Tokens/sec", section "Kimi Delta
  * Attention: a hybrid recurrent + full-attention stack", and the multi-token
@@ -159,6 +188,54 @@ kda_status kda_prefill_varlen(const void *q, const void *k, const void *v, const
 kda_status kda_decode(const void *q, const void *k, const void *v, const void *g,
                       const void *beta, const int32_t *slot_ids, float *state_pool, void *out,
                       int32_t n_tok, float *per_tok_states, const kda_args *a);
+
+/*
+ * Speculative verify with an in-kernel commit of the previous verify step.
+ *
+ * Under speculative decoding every step verifies 1 + d tokens per sequence
+ * (the last accepted token and d draft tokens; the DSpark speculator of
+ * "Kimi K3 on vLLM: Up to 370 Tokens/sec" proposes 7, the vLLM recipe page
+ * for Kimi-K3 configures 8).  How many of them
+ * are accepted is known only after the verify pass, so kda_decode must either
+ * dump the state after every verified token (per_tok_states) or advance the
+ * slot past tokens that may be rejected.  This call instead carries the
+ * commit into the next step: sequence n
+ *   1. reads state_pool[slot_ids[n]] -- the state before the previous verify
+ *      step's tokens;
+ *   2. replays the first accepted_prev[n] of those tokens (rows
+ *      n*n_prev + j, j < accepted_prev[n], of k_prev, v_prev, g_prev,
+ *      beta_prev -- the previous step's own k, v, g, beta, which the caller
+ *      keeps) and, if accepted_prev[n] > 0, writes the result into the slot:
+ *      the committed state;
+ *   3. runs this step's n_tok tokens (rows n*n_tok + j of q, k, v, g, beta)
+ *      from the committed state and writes their outputs o_t = S_t^T q_t to
+ *      out.  The slot is NOT advanced past the committed state: these tokens
+ *      are next call's "previous step".
+ * One state is read and at most one written per (sequence, head) and step,
+ * instead of n_tok + 1 writes with per-token states.
+ *
+ * q, k, g          [N*n_tok][H][dk]  dtype   this step's tokens (may be NULL when n_tok == 0)
+ * v, out           [N*n_tok][H][dv]  dtype
+ * beta             [N*n_tok][H]      dtype
+ * slot_ids         [N]               int32   distinct slots in [0, n_slots)
+ * state_pool       [n_slots][H][dk][dv] fp32 slot_ids[n] receives the committed state
+ * n_tok            >= 0 (0: commit only, nothing is verified)
+ * k_prev, g_prev   [N*n_prev][H][dk] dtype   the previous step's tokens (NULL when n_prev == 0)
+ * v_prev           [N*n_prev][H][dv] dtype
+ * beta_prev        [N*n_prev][H]     dtype
+ * accepted_prev    [N]               int32   in [0, n_prev]: tokens of the previous step
+ *                                            kept for sequence n (NULL when n_prev == 0);
+ *                                            a value outside the range is a device-side
+ *                                            error (bit 64) and that sequence's slot and
+ *                                            outputs are left unwritten
+ * n_prev           >= 0 (0: nothing to commit; the slot is only read)
+ * a->B = N, a->T_total = N * n_tok.  per-token states are not produced here.
+ */
+kda_status kda_decode_spec(const void *q, const void *k, const void *v, const void *g,
+                           const void *beta, const int32_t *slot_ids, float *state_pool,
+                           void *out, int32_t n_tok, const void *k_prev, const void *v_prev,
+                           const void *g_prev, const void *beta_prev,
+                           const int32_t *accepted_prev, int32_t n_prev, const kda_args *a);
 
 /*
  * kda_decode without a workspace, for callers that may not allocate device
@@ -208,7 +285,8 @@ int64_t kda_snapshot_count(const int32_t *cu_seqlens_host, int32_t B, int32_t sn
  * buffer too small, 16 wait timeout, 32 a channel's decay within half a
  * 64-token chunk exceeded 80 nats, beyond the chunked algorithm's exponent
  * range: its results are not reliable, run that batch with
- * KDA_ALGO_RECURRENT). */
+ * KDA_ALGO_RECURRENT; 64 an accepted length of kda_decode_spec outside
+ * [0, n_prev]). */
 kda_status kda_device_status(const kda_args *a, uint32_t *detail);
 
 /* Human-readable name of a status code (static string). */

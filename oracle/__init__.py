@@ -35,7 +35,9 @@ What is computed, and where it is stated:
   segment; the final (prompt-boundary) state is always kept.  Decode
   ("a fused CUDA kernel ... for decode", and the speculative-decoding verify
   path) applies the same step to one or several tokens in place on a pool slot
-  and can record the state after each token for rollback.
+  and can record the state after each token for rollback; ``decode_spec_pool``
+  is the speculative verify that commits the previous step's accepted tokens
+  before evaluating the new ones.
 
 Every function here has pins in ``tests/test_oracle_pins.py`` (closed forms,
 invariants, exact-rational brute force, sequential-vs-chunked agreement,
@@ -298,6 +300,25 @@ def prefill_pool(q, k, v, g, beta, cu_seqlens, init_slots, state_pool, snap_inte
     return res.out, after, res.snaps
 
 
+def prefill_pool_retain(q, k, v, g, beta, cu_seqlens, init_slots, state_pool, snap_interval,
+                        snap_slots, **kw):
+    """What ``kda_prefill_varlen_retain`` must produce.
+
+    The prefill of ``prefill_pool``; snapshot s (numbered as there) is then
+    written into pool slot snap_slots[s] when that is >= 0 and dropped when it
+    is -1 ("Interval-Based and Marconi-Style Retention" of the Day-0
+    integration page: the scheduler keeps only the states it will reuse; the
+    prompt-boundary state still goes to dst).  Returns (out, pool_after).
+    """
+    out, after, snaps = prefill_pool(q, k, v, g, beta, cu_seqlens, init_slots, state_pool,
+                                     snap_interval, **kw)
+    slots = np.asarray(snap_slots, dtype=np.int64).reshape(-1)
+    for s in range(min(len(slots), snaps.shape[0])):
+        if slots[s] >= 0:
+            after[slots[s]] = snaps[s]
+    return out, after
+
+
 def decode_pool(q, k, v, g, beta, slot_ids, state_pool, n_tok=1, per_tok_states=False, **kw):
     """What ``kda_decode`` must produce.
 
@@ -319,6 +340,54 @@ def decode_pool(q, k, v, g, beta, slot_ids, state_pool, n_tok=1, per_tok_states=
         after[slots[n]] = res.final[n]
     per = res.snaps.reshape(N, n_tok, H, dk, dv) if per_tok_states else None
     return res.out, after, per
+
+
+def decode_spec_pool(q, k, v, g, beta, slot_ids, state_pool, n_tok, k_prev=None, v_prev=None,
+                     g_prev=None, beta_prev=None, accepted_prev=None, n_prev=0, **kw):
+    """What ``kda_decode_spec`` must produce.
+
+    The speculative-verify protocol (the DSpark speculator's verify pass of
+    "Kimi K3 on vLLM: Up to 370 Tokens/sec"; the FLA decode path used under
+    speculative decoding, "Kimi K3 + vLLM: Inside the Day-0 Production
+    Integration") with the commit of the previous step done in the same call.
+    For sequence n with slot s = slot_ids[n] and a = accepted_prev[n]:
+      1. S = pool[s]; apply tokens j < a of the previous step (rows
+         n*n_prev + j of the *_prev arrays) with the same token step as
+         ``recurrence``; if a > 0 the slot becomes that committed state;
+      2. from the committed state, tokens j < n_tok of this step (rows
+         n*n_tok + j) produce their outputs; the slot keeps the committed
+         state.
+    Returns (out [N*n_tok, H, dv], pool_after).
+    """
+    pool = _f64(state_pool)
+    slots = np.asarray(slot_ids, dtype=np.int64).reshape(-1)
+    N = len(slots)
+    H, dk, dv = pool.shape[1:]
+    init = np.stack([pool[s] for s in slots]) if N else np.zeros((0, H, dk, dv))
+    committed = init.copy()
+    after = pool.copy()
+    if n_prev > 0:
+        acc = np.asarray(accepted_prev, dtype=np.int64).reshape(-1)
+        if np.any(acc < 0) or np.any(acc > n_prev):
+            raise ValueError("accepted lengths must lie in [0, n_prev]")
+        rows = np.concatenate([np.arange(n * n_prev, n * n_prev + acc[n]) for n in range(N)]
+                              + [np.zeros(0, dtype=np.int64)]).astype(np.int64)
+        if len(rows):
+            kp = _f64(k_prev)[rows]
+            cu = np.concatenate([[0], np.cumsum(acc)]).astype(np.int64)
+            # the replayed tokens have no outputs: any q serves, k is passed
+            res = run(kp, kp, _f64(v_prev)[rows], _f64(g_prev)[rows], _f64(beta_prev)[rows], cu,
+                      init, 0, **kw)
+            for n in range(N):
+                if acc[n] > 0:
+                    committed[n] = res.final[n]
+                    after[slots[n]] = res.final[n]
+    if n_tok > 0:
+        cu = np.arange(N + 1, dtype=np.int64) * n_tok
+        out = run(q, k, v, g, beta, cu, committed, 0, **kw).out
+    else:
+        out = np.zeros((0, H, dv))
+    return out, after
 
 
 def rel_l2(x, ref) -> float:

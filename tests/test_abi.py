@@ -98,10 +98,36 @@ def test_host_visible_errors_return_without_launch(lib):
     st = lib.kda_prefill_varlen(V(4100), fake, fake, fake, fake, fake, fake, fake, fake, 0,
                                 None, ctypes.byref(a))
     assert st == kda.KDA_ERR_INVALID_ARG
-    # decode: n_tok inconsistent with T_total
-    a = _args(B=4, T_total=7, workspace=V(1 << 20), workspace_bytes=1 << 20)
+    # decode: n_tok inconsistent with T_total (the workspace is large enough,
+    # so only that check can refuse the call)
+    a = _args(B=4, T_total=7, workspace=V(1 << 26), workspace_bytes=1 << 26)
+    assert lib.kda_workspace_bytes(ctypes.byref(a)) <= 1 << 26
     st = lib.kda_decode(fake, fake, fake, fake, fake, fake, fake, fake, 2, None, ctypes.byref(a))
     assert st == kda.KDA_ERR_INVALID_ARG
+    # speculative decode: negative counts, a previous step without its
+    # accepted lengths or tokens, a misaligned previous-step pointer
+    a = _args(B=4, T_total=8, workspace=V(1 << 26), workspace_bytes=1 << 26)
+    assert lib.kda_workspace_bytes(ctypes.byref(a)) <= 1 << 26
+    N = None
+    assert lib.kda_decode_spec(fake, fake, fake, fake, fake, fake, fake, fake, -1, N, N, N, N, N,
+                               0, ctypes.byref(a)) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode_spec(fake, fake, fake, fake, fake, fake, fake, fake, 2, N, N, N, N, N,
+                               -3, ctypes.byref(a)) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode_spec(fake, fake, fake, fake, fake, fake, fake, fake, 2, fake, fake, fake,
+                               fake, N, 4, ctypes.byref(a)) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode_spec(fake, fake, fake, fake, fake, fake, fake, fake, 2, fake, N, fake,
+                               fake, fake, 4, ctypes.byref(a)) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode_spec(fake, fake, fake, fake, fake, fake, fake, fake, 2, V(4100), fake,
+                               fake, fake, fake, 4, ctypes.byref(a)) == kda.KDA_ERR_INVALID_ARG
+    # n_tok inconsistent with T_total
+    assert lib.kda_decode_spec(fake, fake, fake, fake, fake, fake, fake, fake, 3, N, N, N, N, N, 0,
+                               ctypes.byref(a)) == kda.KDA_ERR_INVALID_ARG
+    # retention map: missing with a nonzero capacity, or given without an interval
+    a = _args(workspace=V(1 << 26), workspace_bytes=1 << 26, snaps_capacity=4)
+    assert lib.kda_prefill_varlen_retain(fake, fake, fake, fake, fake, fake, fake, fake, fake, 64,
+                                         None, ctypes.byref(a)) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_prefill_varlen_retain(fake, fake, fake, fake, fake, fake, fake, fake, fake, 0,
+                                         fake, ctypes.byref(a)) == kda.KDA_ERR_INVALID_ARG
     # forcing the chunked algorithm on an fp32 batch is unsupported (with a
     # workspace large enough for the cooperative mode's package ring)
     a = _args(algo=kda.KDA_ALGO_CHUNKED, workspace=V(1 << 26), workspace_bytes=1 << 26)
