@@ -202,6 +202,9 @@ cudaError_t launch(const RecArgs &a, int dk, int dv, int nseq, int dtype, cudaSt
   if (nseq == 0) return cudaSuccess;
   const int R = dk == 128 ? 2 : 1;
   const int ncol = (dv < 32 / R) ? dv : 32 / R;
+  // decode claims one word per (slot, head, column block); dk = dv = 128 (8
+  // blocks) always takes the 128 x 128 decode kernel instead
+  if (DECODE && dv / ncol > kClaimsPerState) return cudaErrorInvalidConfiguration;
   dim3 grid(nseq, a.H, dv / ncol), block(ncol * R);
 #define KDA_REC_CASE(DK, RR)                                                         \
   case DK:                                                                           \
