@@ -76,6 +76,14 @@ def prefill_algorithmic(w, lens, n_snaps, n_resumed, es):
     return nbytes, flops, T * H * per_tok
 
 
+# the kernel each decode workload runs (kda_decode.cu)
+DECODE_KERNEL = {
+    "decode_256x1": "decode128_single_kernel (one token per state)",
+    "verify_64x8": "decode128_kernel (staged tokens, per-token states, one CTA per state)",
+    "spec_verify_64x8": "decode128_kernel (speculative: replay + commit + verify, one CTA per state)",
+}
+
+
 def spec_algorithmic(w, N, accepted, es):
     """Bytes of one speculative verify with commit: each touched state read
     once, written once when its sequence accepted at least one token, the
@@ -447,7 +455,7 @@ def main():
                                       "unit": "GB/s", "frac": gbs / P["hbm_gbs"],
                                       "traffic": ncu_traffic("decode128_" + name,
                                                              ["kda_decode.cu"]),
-                                      "kernel": "decode128_kernel",
+                                      "kernel": DECODE_KERNEL[name],
                                       "peak_source": P["source"]}}
 
     if rank != 0:
