@@ -140,7 +140,8 @@ __device__ __forceinline__ float4 ld4s(const float *M, int r, int i) {
 // (fidx layout, fp32, zero on and above the diagonal).  X = (I + A)^{-1} is
 // built from 32 x 32 blocks:
 //  * the diagonal blocks X_00, X_11 by forward substitution, each column
-//    shared by two lanes of a warp (rows 0..15 and 16..31; threads 0..127);
+//    shared by two lanes of a warp (rows 0..15 and 16..31; threads 128..255,
+//    so that thread 0 can issue tensor-core work just before the solve);
 //  * the block below them, X_10 = -X_11 (A_10 X_00), as two 32 x 32 x 32
 //    products, each thread owning rows {p, p + 16} x columns {q, q + 16}
 //    (p = tid / 16, q = tid % 16).
@@ -151,22 +152,24 @@ __device__ __forceinline__ float4 ld4s(const float *M, int r, int i) {
 // x[m] is known it is folded into the running sums of every later row, and
 // x[m + 1] is one multiply-add away.  T is written as bf16
 // into rows 0..63 of the K-major [T; M] operand at tm; the threads without a
-// diagonal column zero its upper block (the rows also hold the decay prefix
-// scratch of the chunk's preparation) and then run side(tid - 128), work of
+// diagonal column (0..127) zero its upper block (the rows also hold the decay
+// prefix scratch of the chunk's preparation) and then run side(tid), work of
 // the caller that does not touch the solve's buffers.  Ends with T fenced
 // for the tensor cores and a barrier.
 template <class Side>
 __device__ __forceinline__ void solve_T(const float *L, const float *LT, float *XT, float *Xd,
                                         float *YT, const float *beta, uint8_t *tm, int tid,
                                         const Side &side) {
-  if (tid >= 128) {  // T's upper block: rows 0..31, 16-byte chunks 4..7
-    const int e = tid - 128;
+  if (tid < 128) {  // T's upper block: rows 0..31, 16-byte chunks 4..7
+    const int e = tid;
     *reinterpret_cast<uint4 *>(tm + sw128_chunk(e >> 2, 4 + (e & 3))) = make_uint4(0, 0, 0, 0);
     side(e);
   } else {
-    // warp w: block b = w / 2, columns 16 (w % 2) .. +15 of it; a column's
-    // rows 0..15 belong to lane c, rows 16..31 to lane c + 16 (c = lane % 16)
-    const int lane = tid & 31, w = tid >> 5, b = w >> 1, half = lane >> 4;
+    // warp w (of warps 4..7, counted from 0): block b = w / 2, columns
+    // 16 (w % 2) .. +15 of it; a column's rows 0..15 belong to lane c, rows
+    // 16..31 to lane c + 16 (c = lane % 16)
+    const int dt = tid - 128;
+    const int lane = dt & 31, w = dt >> 5, b = w >> 1, half = lane >> 4;
     const int j = 16 * (w & 1) + (lane & 15), base = 32 * b;
     const float *lt = LT + b * 1024 + 16 * half;
     float t[16], xo[16];  // running sums and values of this lane's rows 16 half + e
@@ -500,6 +503,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(misc + Ly::kSlot);
   const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+  // this thread's NH accumulator columns of a TMEM row, with a single wait
+  auto ld_row = [](uint32_t taddr, float (&v)[NH]) {
+    if constexpr (NH == 64) {
+      tmem_ld64(taddr, v);
+    } else {
+      tmem_ld32(taddr, v);
+    }
+  };
 
   // ---- state rows owned by this thread: row c, columns [col0, col0 + NH)
   const int c = quarter * 32 + lane;
@@ -678,18 +689,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // U (rows 0..63) -> bf16 MN-major operand (row = token)
     if (quarter < 2) {
       const int r = quarter * 32 + lane;
+      float v[NH];
+      ld_row(lane_base + 128 + col0, v);
 #pragma unroll
-      for (int p = 0; p < NH / 32; ++p) {
-        float v[32];
-        tmem_ld32(lane_base + 128 + col0 + p * 32, v);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int col = col0 + p * 32 + q4 * 8;
-          st_shared_v4(sbase + Ly::kU + (col >> 6) * 8192 + sw128_chunk(r, (col & 63) >> 3),
-                       pack_bf16x2(v[q4 * 8], v[q4 * 8 + 1]), pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]),
-                       pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]),
-                       pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]));
-        }
+      for (int q8 = 0; q8 < NH / 8; ++q8) {
+        const int col = col0 + q8 * 8;
+        st_shared_v4(sbase + Ly::kU + (col >> 6) * 8192 + sw128_chunk(r, (col & 63) >> 3),
+                     pack_bf16x2(v[q8 * 8], v[q8 * 8 + 1]), pack_bf16x2(v[q8 * 8 + 2], v[q8 * 8 + 3]),
+                     pack_bf16x2(v[q8 * 8 + 4], v[q8 * 8 + 5]),
+                     pack_bf16x2(v[q8 * 8 + 6], v[q8 * 8 + 7]));
       }
     }
     tc_fence_before();
@@ -719,31 +727,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (quarter < 2) {
       const int r = quarter * 32 + lane;
       __nv_bfloat16 *orow = a.out + ((int64_t)(t0 + r) * H + h) * dv + dv0 + col0;
+      float v[NH];
+      ld_row(lane_base + 384 + col0, v);
+      if (r < cl) {
+        uint4 *dst = reinterpret_cast<uint4 *>(orow);
 #pragma unroll
-      for (int p = 0; p < NH / 32; ++p) {
-        float v[32];
-        tmem_ld32(lane_base + 384 + col0 + p * 32, v);
-        if (r < cl) {
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + p * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            dst[q4] = make_uint4(pack_bf16x2(v[q4 * 8], v[q4 * 8 + 1]),
-                                 pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]),
-                                 pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]),
-                                 pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]));
-        }
+        for (int q8 = 0; q8 < NH / 8; ++q8)
+          dst[q8] = make_uint4(pack_bf16x2(v[q8 * 8], v[q8 * 8 + 1]),
+                               pack_bf16x2(v[q8 * 8 + 2], v[q8 * 8 + 3]),
+                               pack_bf16x2(v[q8 * 8 + 4], v[q8 * 8 + 5]),
+                               pack_bf16x2(v[q8 * 8 + 6], v[q8 * 8 + 7]));
       }
     }
     {
       // S = Diag(e^{G_C}) S + Diag(e^{G_C - a}) (K-^T U)   (K_end = K- e^{G_C - a})
       const float egc = expf(s_tot[c]), cke = expf(s_tot[c] - s_anc[c]);
+      float v[NH];
+      ld_row(lane_base + 256 + col0, v);
 #pragma unroll
-      for (int p = 0; p < NH / 32; ++p) {
-        float v[32];
-        tmem_ld32(lane_base + 256 + col0 + p * 32, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) S[p * 32 + j] = fmaf(egc, S[p * 32 + j], cke * v[j]);
-      }
+      for (int j = 0; j < NH; ++j) S[j] = fmaf(egc, S[j], cke * v[j]);
       // a snapshot after every snap_every full chunks (the interval is a
       // multiple of the chunk, so a ragged last chunk never ends on one)
       if (snap_every > 0 && --snap_left == 0 && cl == kC) {
@@ -1021,7 +1023,7 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
                reinterpret_cast<float *>(smem + Ly::kLT), sbase + Ly::kTM);
     tc_fence_before();
     __syncthreads();
-    // while threads 0..127 solve for T, threads 128..255 stage the package
+    // while threads 128..255 solve for T, threads 0..127 stage the package
     // operands that need only the prepared tiles: K^ = K- Diag(e^{G_C - a})
     // into the upper half of the S0 region and Q+' = Q+ Diag(e^{a}) into its
     // lower half (the previous package's stores finished before MMA1's wait)
