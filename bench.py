@@ -235,14 +235,31 @@ def bench_prefill(args, torch, kda, inputs, world, rank):
     T, H = dev["q"].shape[:2]
     out = torch.empty((T, H, w.dv), dtype=dev["q"].dtype, device="cuda")
     n_snaps = kda.kda_snapshot_count(b.cu_seqlens, w.snap_interval)
-    snaps = torch.empty((n_snaps, H, w.dk, w.dv), dtype=torch.float32, device="cuda")
     ws = kda.workspace_for(len(b.cu_seqlens) - 1, H, pool.shape[0])
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     launches = []
+    if args.retain:
+        # a retention map: every args.retain-th interval snapshot of each
+        # sequence kept, straight into a free pool slot; the rest dropped
+        smap_h = retention_map(b, w.snap_interval, args.retain, pool.shape[0])
+        smap = smap_h.cuda()
+        snaps = None
+        n_written = int((smap_h >= 0).sum())
+
+        def prefill(events=None):
+            kda.kda_prefill_varlen_retain(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], cu,
+                                          slots, pool, out, w.snap_interval, smap, workspace=ws,
+                                          events=events)
+    else:
+        snaps = torch.empty((n_snaps, H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+        n_written = n_snaps
+
+        def prefill(events=None):
+            kda.kda_prefill_varlen(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], cu, slots,
+                                   pool, out, w.snap_interval, snaps, workspace=ws, events=events)
 
     def call(events):
-        kda.kda_prefill_varlen(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], cu, slots,
-                               pool, out, w.snap_interval, snaps, workspace=ws, events=events)
+        prefill(events)
         launches.append(kda.kda_last_launch_count())
 
     call(None)
@@ -273,8 +290,7 @@ def bench_prefill(args, torch, kda, inputs, world, rank):
             dev[n].copy_(host[n], non_blocking=True)
         cu.copy_(host_cu, non_blocking=True)
         slots.copy_(host_slots, non_blocking=True)
-        kda.kda_prefill_varlen(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], cu, slots,
-                               pool, out, w.snap_interval, snaps, workspace=ws)
+        prefill()
         host_out.copy_(out, non_blocking=True)
 
     e2e_ms = []
@@ -296,10 +312,26 @@ def bench_prefill(args, torch, kda, inputs, world, rank):
     cu_h = b.cu_seqlens.tolist()
     lens = [cu_h[i + 1] - cu_h[i] for i in range(len(cu_h) - 1)]
     n_resumed = int((b.init_slots[:, 0] >= 0).sum())
-    nbytes, flops, _ = prefill_algorithmic(w, lens, n_snaps, n_resumed, dev["q"].element_size())
+    nbytes, flops, _ = prefill_algorithmic(w, lens, n_written, n_resumed,
+                                           dev["q"].element_size())
     return dict(w=w, T=T, B=len(lens), call_ms=call_ms, kern_ms=kern_ms, clocks=ck,
                 nbytes=nbytes, flops=flops, launches=timed_launches, e2e_ms=e2e_ms, h2d=h2d,
-                d2h=d2h, n_snaps=n_snaps, n_resumed=n_resumed)
+                d2h=d2h, n_snaps=n_written, n_resumed=n_resumed)
+
+
+def retention_map(b, interval, every, n_slots):
+    """int32 [n_snaps]: snapshot j of each sequence kept when (j + 1) % every
+    == 0, each into its own pool slot that no sequence reads or writes; -1
+    elsewhere (the scheduler's retention decision, taken before the call)."""
+    import torch
+    cu = b.cu_seqlens.tolist()
+    used = set(int(x) for x in b.init_slots.flatten().tolist() if x >= 0)
+    free = iter(s for s in range(n_slots) if s not in used)
+    out = []
+    for i in range(len(cu) - 1):
+        for j in range((cu[i + 1] - cu[i]) // interval):
+            out.append(next(free) if (j + 1) % every == 0 else -1)
+    return torch.tensor(out, dtype=torch.int32)
 
 
 def bench_decode(name, args, torch, kda, inputs):
@@ -411,6 +443,9 @@ def main():
     ap.add_argument("--workload", default=HEADLINE,
                     choices=["prefill_8k", "varlen_resume", "prefill_1m", "tiny_f32"],
                     help="prefill workload of a step (default: the 8k-token single sequence)")
+    ap.add_argument("--retain", type=int, default=0,
+                    help="keep every N-th interval snapshot in pool slots (retention map) "
+                         "instead of writing all of them to the snapshot buffer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="decode only (profiling runs)")
@@ -496,11 +531,14 @@ def main():
         "config": {"workload": f'{pre["w"].name}: {pre["w"].note}', "B": pre["B"],
                    "T": pre["T"], "H": pre["w"].H, "dk": pre["w"].dk, "dv": pre["w"].dv,
                    "snapshots": pre["n_snaps"], "resumed": pre["n_resumed"],
+                   **({"retention": f"every {args.retain}th interval snapshot kept in a pool "
+                                    "slot (kda_prefill_varlen_retain)"} if args.retain else {}),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "l2": "flushed between timed steps (256 MiB write)"},
         "roofline": {"bound": "hbm", "achieved": algo_gbs, "peak": P["hbm_gbs"], "unit": "GB/s",
                      "frac": algo_gbs / P["hbm_gbs"],
-                     "traffic": ncu_traffic("prefill_" + args.workload, [chunked, "kda_sm100.cuh"]),
+                     "traffic": None if args.retain else ncu_traffic("prefill_" + args.workload,
+                                                                     [chunked, "kda_sm100.cuh"]),
                      "kernel": kernel,
                      "kernel_ms": kern_s * 1e3, "algorithmic_bytes": pre["nbytes"],
                      "peak_source": P["source"],

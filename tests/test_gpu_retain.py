@@ -25,10 +25,12 @@ def _built():
 
 
 def _case(dtype, d, H, lens, n_slots, slots, index=120):
+    """d is dv; dk is 128 on the bf16 (chunked) path and d on the fp32 path."""
     cu = torch.zeros(len(lens) + 1, dtype=torch.int32)
     cu[1:] = torch.cumsum(torch.tensor(lens), 0).to(torch.int32)
-    tt = inputs.token_tensors(int(cu[-1]), H, d, d, inputs.torch_dtype(dtype), index)
-    pool = inputs.pool_states(n_slots, H, d, d, index)
+    dk = 128 if dtype == "bf16" else d
+    tt = inputs.token_tensors(int(cu[-1]), H, dk, d, inputs.torch_dtype(dtype), index)
+    pool = inputs.pool_states(n_slots, H, dk, d, index)
     return inputs.Batch(cu_seqlens=cu, init_slots=torch.tensor(slots, dtype=torch.int32),
                         pool=pool, **tt)
 
@@ -61,6 +63,7 @@ CASES = [
     (kda.KDA_ALGO_RECURRENT, "f32", 32, 3, 16),
     (kda.KDA_ALGO_CHUNKED_PER_STATE, "bf16", 128, 2, 64),
     (kda.KDA_ALGO_CHUNKED_COOP, "bf16", 128, 2, 64),
+    (kda.KDA_ALGO_CHUNKED_PER_STATE, "bf16", 64, 2, 128),   # dk = 128, dv = 64 below
 ]
 
 

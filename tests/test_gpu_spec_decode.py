@@ -84,6 +84,20 @@ def test_spec_decode_matches_oracle(dtype, d):
     assert_untouched(pool_d, before, committed)
 
 
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
+def test_spec_previous_and_current_steps_differ_in_length(dtype, d):
+    """7 tokens in the previous step (6 drafts + 1), 8 in this one: the
+    previous step's rows are read with their own stride."""
+    N, n_prev, n_tok, H, n_slots = 6, 7, 8, 2, 16
+    prev, cur, pool, slots, acc = _case(N, n_prev, n_tok, H, n_slots, dtype, d, index=103)
+    out, pool_d, (st, bits) = _gpu_spec(prev, cur, pool, slots, acc, n_prev, n_tok)
+    assert st == kda.KDA_OK and bits == 0
+    ro, rpool = _oracle_spec(prev, cur, pool, slots, acc, n_prev, n_tok)
+    assert rel(out, ro) <= TOL[dtype]
+    committed = [int(s) for s, a in zip(slots.tolist(), acc.tolist()) if a > 0]
+    assert rel(pool_d[committed], rpool[committed]) <= TOL[dtype]
+
+
 @pytest.mark.parametrize("d", [128, 64])
 def test_commit_equals_per_token_rollback_bit_exact(d):
     """A commit of a tokens writes exactly the state kda_decode reports after
