@@ -438,6 +438,24 @@ __device__ __forceinline__ void issue_mma2(uint32_t tmem, uint32_t tm, uint32_t 
   }
 }
 
+// The cooperative producer's MMA2: W = [T; M] K+ -> tmem[0, 128) (rows 0..63)
+// and U~^T = V^T T^T -> tmem[128, 192): TMEM lane = value column, TMEM
+// column = token (V as an MN-major A operand with M = 128 value columns, T
+// as the K-major B operand, N = K = 64 tokens), so that the package can carry
+// U~ transposed, one 128-byte row per value column.
+template <class Ly>
+__device__ __forceinline__ void issue_mma2_coop(uint32_t tmem, uint32_t tm, uint32_t sb) {
+  tc_fence_after();
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    const uint64_t td = sw128_desc(tm + kk * 32, 16, 1024);
+    mma_bf16(tmem + 0, td, sw128_desc(sb + kk * 2048, 16384, 1024), idesc_bf16(128, 128, 0, 1),
+             kk > 0);
+    mma_bf16(tmem + 128, sw128_desc(sb + Ly::kV + kk * 2048, 8192, 1024), td,
+             idesc_bf16(128, 64, 1, 0), kk > 0);
+  }
+}
+
 // W (rows 0..63 of tmem[0, 128)) as bf16 [token][channel] (K-major W, or the
 // MN-major view with K = token).
 __device__ __forceinline__ void extract_w(uint32_t lane_base, int quarter, int colhalf, int lane,
@@ -814,7 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // CTA feeds to its MMAs (U~ is read by its state warps), copied verbatim
 constexpr uint32_t kPkW = 0;        // W^ [64 tok][128 ch] bf16, K-major, 2 halves x 8 KiB
 constexpr uint32_t kPkKm = 16384;   // K^ [64 tok][128 ch] bf16, 2 halves x 8 KiB
-constexpr uint32_t kPkU = 32768;    // U~ [64 tok][128 dv] bf16, 2 halves x 8 KiB
+constexpr uint32_t kPkU = 32768;    // U~^T [128 dv][64 tok] bf16, 128-byte swizzled rows
 constexpr uint32_t kPkQ = 49152;    // Q+' [64 tok][128 ch] bf16, K-major, 2 halves x 8 KiB
 constexpr uint32_t kPkM = 65536;    // M [64 tok][64 tok] bf16, K-major, 8 KiB
 constexpr uint32_t kPkDec = 73728;  // f32 e^{G_C}[128]
@@ -1057,7 +1075,7 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
             reinterpret_cast<float *>(smem + Ly::kXd),
             reinterpret_cast<float *>(smem + Ly::kYt), s_beta, smem + Ly::kTM, tid, stage_kq);
     if (tid == 0) {
-      issue_mma2<Ly, 128>(tmem, sbase + Ly::kTM, sb);
+      issue_mma2_coop<Ly>(tmem, sbase + Ly::kTM, sb);
       mma_commit(bar_mma);
       s_item[2] = next >= 0 ? take_from(raw_ticket) : -1;
     }
@@ -1072,7 +1090,7 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     tc_fence_after();
     // The package is staged in shared memory in its final layout, outside
     // both input stages, then written out with bulk copies: W^ = W Diag(e^{a})
-    // in the W buffer, U~ in the U buffer, K^ and Q+' in the S0 region (staged
+    // in the W buffer, U~^T in the U buffer, K^ and Q+' in the S0 region (staged
     // during the solve), M where the solve left it and e^{G_C} in the
     // e^{G_C - a} vector.
     // the chunk two ahead goes to this chunk's stage: its k, v and g tiles are
@@ -1080,7 +1098,17 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     // rows to stage
     if (tid == kPub && after >= 0) issue_kvg(after, st);
     if (after >= 0) tma_pending[st] = true;
-    if (quarter < 2) {  // W^ and U~: rows 0..63 of tmem[0, 128) and [128, 256)
+    {  // U~^T: TMEM lane = value column c, this warp's 32 tokens -> row c of kU
+      const int c = quarter * 32 + lane;
+      float v[32];
+      tmem_ld32(lane_base + 128 + colhalf * 32, v);
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        const uint4 w = pack8(v + 8 * q8);
+        st_shared_v4(sbase + Ly::kU + sw128_chunk(c, colhalf * 4 + q8), w.x, w.y, w.z, w.w);
+      }
+    }
+    if (quarter < 2) {  // W^: rows 0..63 of tmem[0, 128)
       const int r = quarter * 32 + lane;
       float v[64];
       tmem_ld64(lane_base + colhalf * 64, v);
@@ -1097,12 +1125,6 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       for (int q8 = 0; q8 < 8; ++q8) {
         const uint4 w = pack8(v + 8 * q8);
         st_shared_v4(sbase + Ly::kW + colhalf * 8192 + sw128_chunk(r, q8), w.x, w.y, w.z, w.w);
-      }
-      tmem_ld64(lane_base + 128 + colhalf * 64, v);
-#pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
-        const uint4 w = pack8(v + 8 * q8);
-        st_shared_v4(sbase + Ly::kU + colhalf * 8192 + sw128_chunk(r, q8), w.x, w.y, w.z, w.w);
       }
     }
     if (tid < 128) s_cke[tid] = expf(s_tot[tid]);  // e^{G_C} for the package
@@ -1299,16 +1321,22 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
         break;
       }
       tc_fence_after();
-      {  // U^T = U~^T - X^T into tensor memory: column q holds tokens 2q (low half), 2q + 1
+      {  // U^T = U~^T - X^T into tensor memory: column q holds tokens 2q (low half), 2q + 1;
+         // row j of the package's U~^T holds this thread's 64 tokens
         float x[64];
         tmem_ld64(lane_base + 384, x);
-        const __nv_bfloat16 *ub = reinterpret_cast<const __nv_bfloat16 *>(
-            smem + b * kCoopPkgBytes + kPkU + (j >> 6) * 8192);
+        const uint32_t ub = sbase + b * (uint32_t)kCoopPkgBytes + kPkU;
         uint32_t r[32];
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-          r[q] = pack_bf16x2(__bfloat162float(ub[sw128_offset(2 * q, j & 63) >> 1]) - x[2 * q],
-                             __bfloat162float(ub[sw128_offset(2 * q + 1, j & 63) >> 1]) - x[2 * q + 1]);
+        for (int q8 = 0; q8 < 8; ++q8) {  // tokens 8 q8 .. 8 q8 + 7
+          const uint4 w = ld_shared_v4(ub + sw128_chunk(j, q8));
+          const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int t = 8 * q8 + 2 * e;
+            r[4 * q8 + e] = pack_bf16x2(bf16lo(wv[e]) - x[t], bf16hi(wv[e]) - x[t + 1]);
+          }
+        }
         tmem_st32(lane_base + 448, r);
         tmem_wait_st();
       }
