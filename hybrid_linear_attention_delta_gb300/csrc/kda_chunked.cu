@@ -994,13 +994,10 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
   // Thread kPub owns the copy engine: at the end of a chunk it requests the
   // tiles of the chunk two ahead, waits for the ring slot and stores the
   // package with bulk copies (shared -> global bulk writes run at about
-  // 29 B/cycle per SM, so the loads go first).  Once the next chunk's tiles
-  // have landed it waits until the stores are complete (their sources are
-  // then free) and publishes the package (ready flag), before that chunk's
-  // preparation: a chain CTA that has caught up with its producers waits for
-  // exactly this flag (waiting at the end of the chunk instead holds up the
-  // producer; waiting at the next chunk's first MMA publishes a whole
-  // preparation later).  Thread 0 issues the MMAs and takes tickets.
+  // 29 B/cycle per SM, so the loads go first).  At the next chunk's first MMA
+  // it waits until the stores are complete (their sources are then free) and
+  // publishes the package (ready flag).  Thread 0 issues the MMAs and takes
+  // tickets.
   constexpr int kPub = 64;
   bool pend = false;
   unsigned long long *pend_flag = nullptr, pend_tag = 0, slot_seen = 0;
@@ -1014,14 +1011,6 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     if (!cta_wait(bar_tma0 + 8 * st, uses[st] & 1)) { aborted = true; break; }
     ++uses[st];
     tma_pending[st] = false;
-    if (tid == kPub) {  // the previous package is complete (its sources are free): publish it
-      bulk_wait<0>();
-      if (pend) {
-        fence_proxy_async_all();
-        st_release_u64(pend_flag, pend_tag);
-        pend = false;
-      }
-    }
 
     prep_chunk<Ly, 128>(sb, cl, beta_n, s_gpart, s_beta, s_tot, s_anc,
                         tid, a.c.err);
@@ -1029,6 +1018,14 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       issue_mma1<Ly>(tmem + 256, sb);
       mma_commit(bar_mma);
       raw_ticket = next >= 0 ? (int)atomicAdd(a.hdr, 1u) : total;  // used at MMA2
+    }
+    if (tid == kPub) {  // the previous package is complete (its sources are free): publish it
+      bulk_wait<0>();
+      if (pend) {
+        fence_proxy_async_all();
+        st_release_u64(pend_flag, pend_tag);
+        pend = false;
+      }
     }
     mma_pending = true;
     if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
@@ -1143,9 +1140,8 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
         ok = coop_flag_wait(a.consumed + u * kCoopRing + slot, coop_tag(a.epoch, n - kCoopRing),
                             a.hdr + 1);
       // the package, piece by piece from where it was staged (W, S0 region,
-      // U, M, e^{G_C}); these are first overwritten after the next chunk's
-      // first MMA, and thread kPub waits for the stores before that chunk's
-      // preparation
+      // U, M, e^{G_C}); these are first overwritten after
+      // the next chunk's first MMA, where thread kPub waits for the stores
       if (tid == kPub && ok) {
         uint8_t *pk = a.ring + ((size_t)u * kCoopRing + slot) * kCoopPkgBytes;
         bulk_s2g(pk + kPkW, sbase + Ly::kW, 16384);
