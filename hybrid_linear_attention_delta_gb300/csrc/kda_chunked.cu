@@ -1443,8 +1443,11 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
     const uint8_t *ring_u = a.ring + (size_t)u * kCoopRing * kCoopPkgBytes;
     for (int n = 0; n < N; ++n) {
       const int b = n & 1;
-      if ((n > 1 && !mbar_wait(empty0 + 8 * b, ((n - 2) >> 1) & 1)) ||
-          !coop_flag_wait(ready + n % kCoopRing, coop_tag(a.epoch, n), a.hdr + 1)) {
+      // the ready flag first: reading it is an L2 round trip even when the
+      // package is long published, and that latency then overlaps the wait
+      // for the stage
+      if (!coop_flag_wait(ready + n % kCoopRing, coop_tag(a.epoch, n), a.hdr + 1) ||
+          (n > 1 && !mbar_wait(empty0 + 8 * b, ((n - 2) >> 1) & 1))) {
         failed = true;
         break;
       }
