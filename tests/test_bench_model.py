@@ -45,7 +45,7 @@ def test_decode_bytes():
 
 def test_speculative_verify_bytes():
     """One state read per (sequence, head); one write only where something was
-    accepted; the replayed tokens carry k, g, v, beta (769 bf16 values), the
+    accepted; the replayed tokens carry k, g, v, beta (385 bf16 values), the
     verified ones the full 1282 B."""
     w = inputs.WORKLOADS["spec_verify_64x8"]
     acc = torch.tensor([0, 3, 8, 1], dtype=torch.int32)
