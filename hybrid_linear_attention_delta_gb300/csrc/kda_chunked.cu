@@ -32,7 +32,7 @@
 //   MMA2  [T; M] K+ and [T; M] V        -> W, U~ (TMEM)
 //   MMA3  U~ -= W S0'  (O = Q+ S0' was issued before the solve)
 //   MMA4  K-^T U       ;  O += M U
-//   out   o rows -> global bf16; S = Diag(e^{G_C}) S + Diag(e^{G_C - a}) K-^T U
+//   out   o rows -> smem -> TMA store; S = Diag(e^{G_C}) S + Diag(e^{G_C - a}) K-^T U
 //         (= K_end^T U with K_end = K e^{G_C - G}) in registers;
 //         snapshot (dense buffer or retained pool slot) / final state ->
 //         global fp32
@@ -475,7 +475,7 @@ template <int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                   const ChunkArgs a) {
+                   const __grid_constant__ CUtensorMap tm_o, const ChunkArgs a) {
   using Ly = Layout<DV>;
   constexpr int NH = DV / 2;  // state columns per thread
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -513,6 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_g);
+    prefetch_tmap(&tm_o);
   }
   if (warp == 0) tmem_alloc(sbase + Ly::kMisc + Ly::kSlot, kTmemCols);
   // [T; M] starts at zero: the blocks of T above its diagonal are never written
@@ -633,6 +634,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_async_smem();
     }
+    // the previous chunk's outputs were stored from the W buffer, which the
+    // system L overwrites next
+    if (tid == 0) bulk_wait_read<0>();
     if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
     mma_phase ^= 1;
     mma_pending = false;
@@ -742,13 +746,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
 
     // ------------------------------------------------------------ outputs
+    // a whole chunk is staged in the W buffer (free since MMA3) as 128-byte
+    // swizzled halves of 64 value columns and leaves with TMA stores after
+    // the chunk's closing barrier; a ragged last chunk is written directly
+    // (a full box would run into the next sequence's rows)
     if (quarter < 2) {
       const int r = quarter * 32 + lane;
-      __nv_bfloat16 *orow = a.out + ((int64_t)(t0 + r) * H + h) * dv + dv0 + col0;
       float v[NH];
       ld_row(lane_base + 384 + col0, v);
-      if (r < cl) {
-        uint4 *dst = reinterpret_cast<uint4 *>(orow);
+      if (cl == kC) {
+#pragma unroll
+        for (int q8 = 0; q8 < NH / 8; ++q8) {
+          const int col = col0 + 8 * q8;
+          st_shared_v4(sbase + Ly::kW + (col >> 6) * 8192 + sw128_chunk(r, (col & 63) >> 3),
+                       pack_bf16x2(v[q8 * 8], v[q8 * 8 + 1]), pack_bf16x2(v[q8 * 8 + 2], v[q8 * 8 + 3]),
+                       pack_bf16x2(v[q8 * 8 + 4], v[q8 * 8 + 5]),
+                       pack_bf16x2(v[q8 * 8 + 6], v[q8 * 8 + 7]));
+        }
+        fence_async_smem();
+      } else if (r < cl) {
+        uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((int64_t)(t0 + r) * H + h) * dv + dv0 + col0);
 #pragma unroll
         for (int q8 = 0; q8 < NH / 8; ++q8)
           dst[q8] = make_uint4(pack_bf16x2(v[q8 * 8], v[q8 * 8 + 1]),
@@ -784,8 +801,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && cl == kC) {
+#pragma unroll
+      for (int j = 0; j < DV / 64; ++j)
+        tma_store_2d(&tm_o, sbase + Ly::kW + j * 8192, h * dv + dv0 + 64 * j, t0);
+      bulk_commit();
+    }
   }
 
+  if (tid == 0) bulk_wait<0>();  // every output store complete (and its source read)
   if (aborted) {
     if (tid == 0) raise_error(a.err, ERR_TIMEOUT);
     // drain what is still in flight (bounded), then release TMEM
@@ -1554,7 +1578,9 @@ cudaError_t launch_dv(const PrefillPlan &p, const CUtensorMap &mq, const CUtenso
   a.n_dvb = p.dv / DV;
   a.err = p.err;
   const unsigned grid = (unsigned)((int64_t)p.B * p.H * a.n_dvb);
-  chunked_kernel<DV><<<grid, kThreads, smem, p.stream>>>(mq, mk, mv, mg, a);
+  CUtensorMap mo;
+  if (!make_map(&mo, p.out, (uint64_t)p.H * p.dv, (uint64_t)p.T_total)) return cudaErrorInvalidValue;
+  chunked_kernel<DV><<<grid, kThreads, smem, p.stream>>>(mq, mk, mv, mg, mo, a);
   return cudaGetLastError();
 }
 
