@@ -37,6 +37,8 @@
 //         snapshot (dense buffer or retained pool slot) / final state ->
 //         global fp32
 // All MMAs are M = 128 (rows 64..127 of the 64-row operands are ignored).
+#include <cstring>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -100,6 +102,9 @@ struct ChunkArgs {
   int32_t snap_interval;
   int32_t H, dv, n_dvb;
   uint32_t *err;
+  // per-state kernel: snapshots leave through TMA stores (fp32 maps over the
+  // snapshot buffer and the pool are valid); else through direct stores
+  int32_t snap_tma;
 };
 
 // A CTA-uniform bounded wait: false (for every thread) if any thread gave up.
@@ -475,7 +480,9 @@ template <int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                   const __grid_constant__ CUtensorMap tm_o, const ChunkArgs a) {
+                   const __grid_constant__ CUtensorMap tm_o,
+                   const __grid_constant__ CUtensorMap tm_snap,
+                   const __grid_constant__ CUtensorMap tm_pool, const ChunkArgs a) {
   using Ly = Layout<DV>;
   constexpr int NH = DV / 2;  // state columns per thread
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -589,6 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int snap_every = a.snap_interval > 0 ? a.snap_interval / kC : 0;
   int snap_left = snap_every;
   int64_t snap_next = m.snap_off;
+  int64_t snap_y = -1;  // row of a snapshot staged for a TMA store this chunk
 #pragma unroll 1
   for (int n = 0; n < nchunks; ++n) {
     const int st = n & 1;
@@ -788,7 +796,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t s = snap_next++;
         if (s < a.snaps_capacity) {
           float *base = snapshot_base(a.snaps, a.snap_slots, a.pool, s, H, h, (int64_t)kDK * dv);
-          if (base) {
+          if (base && a.snap_tma) {
+            // staged in this chunk's input stage (dead since MMA4; its next
+            // load waits for the store) as 128-byte swizzled boxes of 32
+            // columns, then TMA-stored after the closing barrier
+#pragma unroll
+            for (int j = 0; j < NH / 4; ++j) {
+              const int col = col0 + 4 * j;
+              st_shared_v4(sb + (col >> 5) * 16384 + sw128_chunk(c, (col & 31) >> 2),
+                           __float_as_uint(S[4 * j]), __float_as_uint(S[4 * j + 1]),
+                           __float_as_uint(S[4 * j + 2]), __float_as_uint(S[4 * j + 3]));
+            }
+            fence_async_smem();
+            snap_y = a.snap_slots ? ((int64_t)a.snap_slots[s] * H + h) * kDK : (s * H + h) * kDK;
+          } else if (base) {
             float4 *dst = reinterpret_cast<float4 *>(base + (int64_t)c * dv + dv0 + col0);
 #pragma unroll
             for (int j = 0; j < NH / 4; ++j)
@@ -805,8 +826,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < DV / 64; ++j)
         tma_store_2d(&tm_o, sbase + Ly::kW + j * 8192, h * dv + dv0 + 64 * j, t0);
+      if (snap_y >= 0) {
+#pragma unroll
+        for (int j = 0; j < DV / 32; ++j)
+          tma_store_2d(a.snap_slots ? &tm_pool : &tm_snap, sb + j * 16384, dv0 + 32 * j,
+                       (int)snap_y);
+      }
       bulk_commit();
     }
+    snap_y = -1;
   }
 
   if (tid == 0) bulk_wait<0>();  // every output store complete (and its source read)
@@ -1552,6 +1580,21 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows)
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [rows][inner] with 128-byte swizzled boxes of 32 columns x 128 rows
+// (one (state, 32-column block) per box); false when it cannot be encoded or
+// its rows overflow the 32-bit TMA coordinate
+bool make_map_f32(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn || !base || rows == 0 || rows >= (1ull << 31)) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int DV>
 cudaError_t launch_dv(const PrefillPlan &p, const CUtensorMap &mq, const CUtensorMap &mk,
                       const CUtensorMap &mv, const CUtensorMap &mg) {
@@ -1578,9 +1621,16 @@ cudaError_t launch_dv(const PrefillPlan &p, const CUtensorMap &mq, const CUtenso
   a.n_dvb = p.dv / DV;
   a.err = p.err;
   const unsigned grid = (unsigned)((int64_t)p.B * p.H * a.n_dvb);
-  CUtensorMap mo;
+  CUtensorMap mo, msnap, mpool;
   if (!make_map(&mo, p.out, (uint64_t)p.H * p.dv, (uint64_t)p.T_total)) return cudaErrorInvalidValue;
-  chunked_kernel<DV><<<grid, kThreads, smem, p.stream>>>(mq, mk, mv, mg, mo, a);
+  std::memset(&msnap, 0, sizeof(msnap));
+  std::memset(&mpool, 0, sizeof(mpool));
+  const bool snap_ok = p.snaps_capacity > 0 && p.snaps &&
+                       make_map_f32(&msnap, p.snaps, (uint64_t)p.dv,
+                                    (uint64_t)p.snaps_capacity * p.H * kDK);
+  const bool pool_ok = make_map_f32(&mpool, p.pool, (uint64_t)p.dv, (uint64_t)p.n_slots * p.H * kDK);
+  a.snap_tma = (p.snap_slots ? pool_ok : snap_ok) ? 1 : 0;
+  chunked_kernel<DV><<<grid, kThreads, smem, p.stream>>>(mq, mk, mv, mg, mo, msnap, mpool, a);
   return cudaGetLastError();
 }
 
@@ -1621,6 +1671,7 @@ cudaError_t launch_coop(const PrefillPlan &p, int grid, const CUtensorMap &mq,
   a.c.dv = p.dv;
   a.c.n_dvb = 1;
   a.c.err = p.err;
+  a.c.snap_tma = 0;  // the chain CTAs store snapshots directly (coalesced columns)
   a.units = p.B * p.H;
   a.ring = p.coop_ring;
   a.ready = p.coop_flags;
