@@ -297,16 +297,27 @@ __global__ void __launch_bounds__(kThreads, 2) decode128_kernel(DecodePlan p) {
       // S' = Diag(a) S ; partial x = S'^T k and y = S'^T q over this warp's rows
       float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
       float kq = 0.f;  // k . q over this warp's rows (the same on every lane)
+      if (SPEC && t < acc) {  // a replayed token has no query: x only
 #pragma unroll
-      for (int m = 0; m < kRowsPerWarp; ++m) {
-        const int i = w * kRowsPerWarp + m;
-        const float ai = ta[tt][i], ki = tk[tt][i], qi = tq[tt][i];
-        kq = fmaf(ki, qi, kq);
-        s[m].x *= ai; s[m].y *= ai; s[m].z *= ai; s[m].w *= ai;
-        x.x = fmaf(ki, s[m].x, x.x); x.y = fmaf(ki, s[m].y, x.y);
-        x.z = fmaf(ki, s[m].z, x.z); x.w = fmaf(ki, s[m].w, x.w);
-        y.x = fmaf(qi, s[m].x, y.x); y.y = fmaf(qi, s[m].y, y.y);
-        y.z = fmaf(qi, s[m].z, y.z); y.w = fmaf(qi, s[m].w, y.w);
+        for (int m = 0; m < kRowsPerWarp; ++m) {
+          const int i = w * kRowsPerWarp + m;
+          const float ai = ta[tt][i], ki = tk[tt][i];
+          s[m].x *= ai; s[m].y *= ai; s[m].z *= ai; s[m].w *= ai;
+          x.x = fmaf(ki, s[m].x, x.x); x.y = fmaf(ki, s[m].y, x.y);
+          x.z = fmaf(ki, s[m].z, x.z); x.w = fmaf(ki, s[m].w, x.w);
+        }
+      } else {
+#pragma unroll
+        for (int m = 0; m < kRowsPerWarp; ++m) {
+          const int i = w * kRowsPerWarp + m;
+          const float ai = ta[tt][i], ki = tk[tt][i], qi = tq[tt][i];
+          kq = fmaf(ki, qi, kq);
+          s[m].x *= ai; s[m].y *= ai; s[m].z *= ai; s[m].w *= ai;
+          x.x = fmaf(ki, s[m].x, x.x); x.y = fmaf(ki, s[m].y, x.y);
+          x.z = fmaf(ki, s[m].z, x.z); x.w = fmaf(ki, s[m].w, x.w);
+          y.x = fmaf(qi, s[m].x, y.x); y.y = fmaf(qi, s[m].y, y.y);
+          y.z = fmaf(qi, s[m].z, y.z); y.w = fmaf(qi, s[m].w, y.w);
+        }
       }
       *reinterpret_cast<float4 *>(&redx[w][4 * l]) = x;
       *reinterpret_cast<float4 *>(&redy[w][4 * l]) = y;
