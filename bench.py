@@ -402,14 +402,14 @@ class OracleSample:
         self.cu = np.array([0, self.T], dtype=np.int64)
         self.tok_heads = sum(lens) * w.H    # of the whole workload
 
-    def run_heads(self, n):
+    def run_heads(self, n, threads=None):
         sub = {k: self.np.ascontiguousarray(a[:, :n]) for k, a in self.arrs.items()}
         t0 = time.perf_counter()
         self.oracle.run(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], self.cu, None,
-                        self.w.snap_interval, nthreads=self.cores)
+                        self.w.snap_interval, nthreads=threads or self.cores)
         return time.perf_counter() - t0
 
-    def measure(self, target_s, max_heads=None):
+    def measure(self, target_s, max_heads=None, one_core=False):
         """Returns a cpu_baseline dict whose value is the workload's tokens/s
         at the sampled token-head rate."""
         w = self.w
@@ -423,13 +423,19 @@ class OracleSample:
         rate = self.T * n / t                       # token-heads per second
         tokens = self.tok_heads / w.H
         value = rate / w.H                          # tokens/s of H-head work
-        return {"value": value, "unit": "tokens/s", "cores": self.cores, "kind": "oracle",
-                "sample": f"{n} of {w.H} heads x {self.T} tokens of {w.name} (C fp64, "
-                          f"{self.cores} threads over 16-column state blocks), {t:.2f} s "
-                          f"per pass, mean of {reps}; "
-                          f"value = tokens/s of all {w.H} heads at that rate "
-                          f"({tokens:.0f}-token workload)",
-                "seconds": t}
+        out = {"value": value, "unit": "tokens/s", "cores": self.cores, "kind": "oracle",
+               "sample": f"{n} of {w.H} heads x {self.T} tokens of {w.name} (C fp64, "
+                         f"{self.cores} threads over 16-column state blocks), {t:.2f} s "
+                         f"per pass, mean of {reps}; "
+                         f"value = tokens/s of all {w.H} heads at that rate "
+                         f"({tokens:.0f}-token workload)",
+               "seconds": t}
+        if one_core:  # the same oracle on one thread, one head
+            t1c = self.run_heads(1, threads=1)
+            out["one_core"] = {"value": self.T / t1c / w.H, "unit": "tokens/s", "cores": 1,
+                               "sample": f"1 head x {self.T} tokens, 1 thread, {t1c:.2f} s; "
+                                         f"value = tokens/s of all {w.H} heads at that rate"}
+        return out
 
 
 # ------------------------------------------------------------------ main
@@ -503,7 +509,7 @@ def main():
 
     cpu = None
     if not args.no_cpu_baseline:
-        cpu = OracleSample(args.workload).measure(target_s=12.0)
+        cpu = OracleSample(args.workload).measure(target_s=12.0, one_core=True)
         cpu.pop("seconds", None)
 
     algo_gbs = pre["nbytes"] / kern_s / 1e9
