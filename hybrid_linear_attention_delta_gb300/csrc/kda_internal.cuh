@@ -9,8 +9,8 @@
 //                            sequences of one call writing the same state
 //   when B*H <= kCoopMaxUnits, the cooperative prefill's section:
 //   [.., +256)               uint32 ticket, abort word, longest sequence in chunks
-//   [.., +align(B*H*8*16))   u64 ready[B*H][8], consumed[B*H][8] flags
-//   [.., +B*H*8*74752)       package ring, 8 chunk packages per (sequence, head)
+//   [.., +align(B*H*R*16))   u64 ready[B*H][R], consumed[B*H][R] flags (R = kCoopRing)
+//   [.., +B*H*R*74752)       package ring, R chunk packages per (sequence, head)
 #pragma once
 
 #include <cuda_bf16.h>
@@ -47,7 +47,10 @@ constexpr int kClaimsPerState = 4;  // one claim word per (slot, head, column bl
 // Cooperative prefill (few (sequence, head) pairs): per pair a ring of chunk
 // packages handed from producer CTAs to the pair's state-carrying CTA.
 constexpr int kCoopMaxUnits = 64;      // (sequence, head) pairs it serves at most
-constexpr int kCoopRing = 8;           // packages in flight per pair
+// packages in flight per pair: 6 measured 1% faster than 8 and 8% faster than 16 on
+// the 8k-token prefill (same box; a deeper ring lets the producers run ahead of all
+// pairs together, and its packages go cold in L2)
+constexpr int kCoopRing = 6;
 constexpr size_t kCoopPkgBytes = 74752;
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

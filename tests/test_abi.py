@@ -51,8 +51,8 @@ def test_snapshot_count_and_workspace_bytes(lib):
     n2 = kda.kda_workspace_bytes(16, 32, 1024)
     assert n1 % 256 == 0 and n2 % 256 == 0
     # few (sequence, head) pairs: room for the cooperative prefill's package
-    # ring (8 packages of 73 KiB per pair)
-    assert n1 >= 32 * 8 * 74752
+    # ring (6 packages of 73 KiB per pair)
+    assert n1 >= 32 * 6 * 74752
     # claims: one word per (slot, head, column block) of the pool; 512 pairs
     # use the per-state prefill, so no ring
     assert 1024 * 32 * 4 * 4 <= n2 < 1024 * 32 * 4 * 4 + 16 * 32 * 64 + 4096
