@@ -39,6 +39,11 @@ What is computed, and where it is stated:
   is the speculative verify that commits the previous step's accepted tokens
   before evaluating the new ones.
 
+* ``split_recurrence`` is the algebra of a sequence-split prefill (segments
+  from the zero state plus identity runs with v = 0, start states chained,
+  outputs corrected); the GPU library does not implement it yet, and it is
+  pinned against the sequential recurrence.
+
 Every function here has pins in ``tests/test_oracle_pins.py`` (closed forms,
 invariants, exact-rational brute force, sequential-vs-chunked agreement,
 C-vs-numpy agreement).
@@ -388,6 +393,39 @@ def decode_spec_pool(q, k, v, g, beta, slot_ids, state_pool, n_tok, k_prev=None,
     else:
         out = np.zeros((0, H, dv))
     return out, after
+
+
+def split_recurrence(q, k, v, g, beta, S0, splits):
+    """Sequence-split evaluation of ONE (sequence, head), the algebra of a
+    split prefill (a long prompt cut into segments that run in parallel;
+    "Kimi K3 on vLLM: Up to 370 Tokens/sec" motivates 1M-token contexts).
+
+    The token step is affine in the state: S_t = A_t S_{t-1} + b_t with
+    A_t = (I - beta_t k_t k_t^T) Diag(exp g_t) and b_t = beta_t k_t v_t^T.  So
+    a segment [s, e) maps its start state X to Phi X + L, where L is the
+    segment run from the zero state and Phi = A_{e-1} ... A_s is the same
+    segment run from the identity (a dk x dk state) with v := 0.  Its outputs
+    split the same way: o_t = L_t^T q_t + X^T (Phi_t^T q_t), and Phi_t^T q_t is
+    the identity run's own output.  Segment start states chain serially
+    (X_{i+1} = Phi_i X_i + L_i) and every segment's outputs are then corrected
+    independently.  ``splits`` are the cut points (0 < s_1 < ... < L).
+    Returns (o [L, dv], S_L), equal to ``recurrence`` up to rounding.
+    """
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(g)
+    beta = _f64(beta).reshape(-1)
+    L, dk = k.shape
+    dv = v.shape[1]
+    bounds = [0] + [int(x) for x in splits] + [L]
+    X = np.zeros((dk, dv)) if S0 is None else _f64(S0).copy()
+    o = np.zeros((L, dv))
+    for s0, s1 in zip(bounds[:-1], bounds[1:]):
+        sl = slice(s0, s1)
+        o_loc, L_end = recurrence(q[sl], k[sl], v[sl], g[sl], beta[sl], None)
+        o_hom, Phi = recurrence(q[sl], k[sl], np.zeros((s1 - s0, dk)), g[sl], beta[sl],
+                                np.eye(dk))
+        o[sl] = o_loc + o_hom @ X          # row t: L_t^T q_t + X^T Phi_t^T q_t
+        X = Phi @ X + L_end
+    return o, X
 
 
 def rel_l2(x, ref) -> float:

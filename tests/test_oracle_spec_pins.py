@@ -188,3 +188,38 @@ def test_retaining_nothing_equals_no_snapshots():
     o2, p2, _ = oracle.prefill_pool(q, k, v, g, beta, cu, init, pool, 0)
     np.testing.assert_array_equal(out, o2)
     np.testing.assert_array_equal(after, p2)
+
+
+# ---------------------------------------------------------------- sequence split
+
+def test_split_recurrence_equals_the_sequential_run():
+    """Cutting a sequence into segments (zero-state run plus identity run with
+    v = 0 per segment, start states chained, outputs corrected) reproduces the
+    token-by-token recurrence, with and without an initial state, for one and
+    for several cuts including cuts one token apart."""
+    rng = np.random.default_rng(31)
+    L, dk, dv = 40, 6, 5
+    q, k, v, g, beta = (a[:, 0] for a in _tokens(rng, L, 1, dk, dv))
+    S0 = 0.3 * rng.standard_normal((dk, dv))
+    o_ref, S_ref = oracle.recurrence(q, k, v, g, beta, S0)
+    for splits in ([20], [7, 8, 30], [1, 39], list(range(4, 40, 4))):
+        for init in (None, S0):
+            o, S = oracle.split_recurrence(q, k, v, g, beta, init, splits)
+            o_want, S_want = (o_ref, S_ref) if init is not None else \
+                oracle.recurrence(q, k, v, g, beta, None)
+            np.testing.assert_allclose(o, o_want, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(S, S_want, rtol=1e-12, atol=1e-12)
+
+
+def test_identity_run_is_the_product_of_the_token_maps():
+    """The identity run with v = 0 is the product of the token maps
+    A_t = (I - b_t k_t k_t^T) Diag(exp g_t), written out directly."""
+    rng = np.random.default_rng(32)
+    L, d = 9, 4
+    q, k, v, g, beta = (a[:, 0] for a in _tokens(rng, L, 1, d, d))
+    _, Phi = oracle.recurrence(q, k, np.zeros((L, d)), g, beta, np.eye(d))
+    P = np.eye(d)
+    for t in range(L):
+        A = (np.eye(d) - beta[t] * np.outer(k[t], k[t])) @ np.diag(np.exp(g[t]))
+        P = A @ P
+    np.testing.assert_allclose(Phi, P, rtol=1e-13, atol=1e-13)
