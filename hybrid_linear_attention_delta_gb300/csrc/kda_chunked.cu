@@ -889,8 +889,9 @@ constexpr uint32_t kPkQ = 49152;    // Q+' [64 tok][128 ch] bf16, K-major, 2 hal
 constexpr uint32_t kPkM = 65536;    // M [64 tok][64 tok] bf16, K-major, 8 KiB
 constexpr uint32_t kPkDec = 73728;  // f32 e^{G_C}[128]
 static_assert(kPkDec + 512 <= kCoopPkgBytes && kCoopPkgBytes % 1024 == 0, "package layout");
-// a package is fetched as kPkPieces bulk copies of kPkPiece bytes
-constexpr uint32_t kPkPieces = 4, kPkPiece = (uint32_t)kCoopPkgBytes / kPkPieces;
+// a package is fetched as kPkPieces bulk copies of kPkPiece bytes (8 measured
+// 0.3-0.6% faster than 4 in a same-box A/B)
+constexpr uint32_t kPkPieces = 8, kPkPiece = (uint32_t)kCoopPkgBytes / kPkPieces;
 static_assert(kPkPiece % 16 == 0 && kPkPiece * kPkPieces == kCoopPkgBytes, "bulk copy pieces");
 // chain CTA shared memory: two package stages, two output staging tiles
 // ([64 tok][128 dv] bf16 each, stored with one TMA box), mbarriers, TMEM slot
