@@ -326,11 +326,15 @@ def retention_map(b, interval, every, n_slots):
     import torch
     cu = b.cu_seqlens.tolist()
     used = set(int(x) for x in b.init_slots.flatten().tolist() if x >= 0)
-    free = iter(s for s in range(n_slots) if s not in used)
+    free = [s for s in range(n_slots) if s not in used]
     out = []
     for i in range(len(cu) - 1):
         for j in range((cu[i + 1] - cu[i]) // interval):
-            out.append(next(free) if (j + 1) % every == 0 else -1)
+            out.append(-1 if (j + 1) % every else (free.pop(0) if free else None))
+    if None in out:
+        raise ValueError(f"--retain {every}: the workload's pool has {n_slots} slots, too few "
+                         "free ones for the kept snapshots (use a workload with a slot pool, "
+                         "e.g. --workload varlen_resume)")
     return torch.tensor(out, dtype=torch.int32)
 
 

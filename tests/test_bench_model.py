@@ -72,3 +72,13 @@ def test_retention_map_keeps_every_nth_into_free_slots():
     assert len(kept) == len(set(kept))                  # distinct
     assert not set(kept) & {0, 1, 2, 3, 5}              # no source or destination
     assert all(0 <= s < 40 for s in kept)
+
+
+def test_retention_map_refuses_a_pool_without_room():
+    import pytest
+    cu = torch.tensor([0, 512], dtype=torch.int32)
+    slots = torch.tensor([[-1, 0]], dtype=torch.int32)
+    b = inputs.Batch(q=None, k=None, v=None, g=None, beta=None, cu_seqlens=cu,
+                     init_slots=slots)
+    with pytest.raises(ValueError):
+        bench.retention_map(b, 64, 2, 1)   # 4 kept snapshots, no free slot
