@@ -50,3 +50,19 @@ def test_two_gloo_ranks_take_the_slowest(tmp_path):
         assert step_s == 1.5            # max over ranks of 0.5 + rank
         assert e2e_s == 3.0             # max over ranks of 3 - rank
         assert tput == 8192 * 2 / 1.5   # both replicas' tokens over the slowest time
+
+
+def test_reference_arm_runs_on_rank_zero_only(capsys):
+    """Under torchrun the reference arm (the oracle on host cores) runs and
+    prints on rank 0 only; every other rank exits 0 without work or output."""
+    import argparse
+    import bench
+    args = argparse.Namespace(workload="tiny_f32", steps=1, warmup=0)
+    assert bench.reference_arm(args, 2, 1) == 0
+    assert capsys.readouterr().out == ""
+    assert bench.reference_arm(args, 2, 0) == 0
+    line = capsys.readouterr().out.strip().splitlines()[-1]
+    import json
+    d = json.loads(line)
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
