@@ -33,9 +33,11 @@
 //   MMA3  U~ -= W S0'  (O = Q+ S0' was issued before the solve)
 //   MMA4  K-^T U       ;  O += M U
 //   out   o rows -> smem -> TMA store; S = Diag(e^{G_C}) S + Diag(e^{G_C - a}) K-^T U
-//         (= K_end^T U with K_end = K e^{G_C - G}) in registers;
-//         snapshot (dense buffer or retained pool slot) / final state ->
-//         global fp32
+//         (= K_end^T U with K_end = K e^{G_C - G}) in registers; a snapshot
+//         -> the chunk's own (dead) input stage -> fp32 TMA store (dense
+//         buffer or retained pool slot); the final state -> global fp32
+// Below it, the cooperative mode for few (sequence, head) pairs splits the same
+// chunk pipeline between producer CTAs and one state-carrying CTA per pair.
 // All MMAs are M = 128 (rows 64..127 of the 64-row operands are ignored).
 #include <cstring>
 
