@@ -4,14 +4,18 @@ fractions, the fp64 CPU oracle timed beside it, and an end-to-end figure.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-One step is one ``kda_prefill_varlen`` call on the single-sequence prefill
-workload (B=1, T=8192, H=32, dk=dv=128, bf16, snapshots every 1024 tokens):
-the device-side plan kernel plus the chunked prefill kernel, which write the
-outputs, the 8 snapshots and the final state.  The same run also times the
-batched decode (256 sequences x 1 token), the speculative-verify decode
-(64 x 8 tokens with per-token states) and the speculative verify with the
-previous step's commit folded in (64 x 8 tokens, kda_decode_spec) and
-reports them under "decode".
+One step is one ``kda_prefill_varlen`` call on the long-context prefill
+workload (B=1, T=2^20, H=16, dk=dv=128, bf16, snapshots every 32768 tokens):
+the device-side plan kernel, the chunked prefill kernel, which writes the
+outputs, the 32 snapshots and the final state, and the exact-recomputation
+launch (which does nothing unless a gate left the chunked algorithm's range).
+The same run also times the single-sequence prefill (B=1, T=8192, H=32,
+snapshots every 1024) and the varlen batch with copy-on-write resume (16
+sequences, snapshots every 256) and reports them under "prefill", each with
+its own roofline, and the batched decode (256 sequences x 1 token), the
+speculative-verify decode (64 x 8 tokens with per-token states) and the
+speculative verify with the previous step's commit folded in (64 x 8 tokens,
+kda_decode_spec) under "decode".
 Inputs are synthetic (seeded, see hybrid_linear_attention_delta_gb300/inputs.py).
 L2 is flushed (a 256 MiB write) between timed steps.  ``--impl reference``
 times the fp64 CPU oracle on a bounded sample of the same workload instead.
@@ -37,7 +41,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "KDA prefill tokens/s & decode state GB/s on 1 GB300, % of tensor/HBM roofline"
-HEADLINE = "prefill_8k"
+HEADLINE = "prefill_1m"
+EXTRA_PREFILL = ("prefill_8k", "varlen_resume")
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -225,9 +230,13 @@ def job_throughput(tokens_per_rank, world, seconds):
     return tokens_per_rank * world / seconds
 
 
-def bench_prefill(args, torch, kda, inputs, world, rank):
-    w = inputs.WORKLOADS[args.workload]
-    b = inputs.make_batch(w, device="cuda")
+def bench_prefill(args, torch, kda, inputs, world, rank, workload, retain=0, e2e=True):
+    w = inputs.WORKLOADS[workload]
+    if args.tokens and workload == args.workload:
+        # a shortened single-sequence workload (profiling captures only)
+        b = inputs.make_batch(w, device="cuda", lengths=[args.tokens])
+    else:
+        b = inputs.make_batch(w, device="cuda")
     dev = {n: getattr(b, n) for n in ("q", "k", "v", "g", "beta")}
     cu = b.cu_seqlens.cuda()
     slots = b.init_slots.cuda()
@@ -238,10 +247,10 @@ def bench_prefill(args, torch, kda, inputs, world, rank):
     ws = kda.workspace_for(len(b.cu_seqlens) - 1, H, pool.shape[0])
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     launches = []
-    if args.retain:
-        # a retention map: every args.retain-th interval snapshot of each
+    if retain:
+        # a retention map: every retain-th interval snapshot of each
         # sequence kept, straight into a free pool slot; the rest dropped
-        smap_h = retention_map(b, w.snap_interval, args.retain, pool.shape[0])
+        smap_h = retention_map(b, w.snap_interval, retain, pool.shape[0])
         smap = smap_h.cuda()
         snaps = None
         n_written = int((smap_h >= 0).sum())
@@ -277,9 +286,12 @@ def bench_prefill(args, torch, kda, inputs, world, rank):
     ck = clocks.stop()
 
     # end to end through the same public call, host (pinned) buffers in and out
-    host = {n: t.cpu().pin_memory() for n, t in dev.items()}
+    host = {}
+    for n, t in (dev.items() if e2e else ()):
+        host[n] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        host[n].copy_(t)
     host_cu, host_slots = b.cu_seqlens.pin_memory(), b.init_slots.pin_memory()
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_out = torch.empty(out.shape if e2e else (0,), dtype=out.dtype, pin_memory=True)
     stream = torch.cuda.current_stream()
     h2d = sum(t.numel() * t.element_size() for t in host.values()) + \
         host_cu.numel() * 4 + host_slots.numel() * 4
@@ -294,10 +306,10 @@ def bench_prefill(args, torch, kda, inputs, world, rank):
         host_out.copy_(out, non_blocking=True)
 
     e2e_ms = []
-    for _ in range(0 if args.no_e2e else 2):
+    for _ in range(2 if e2e else 0):
         e2e_step()
     torch.cuda.synchronize()
-    for _ in range(0 if args.no_e2e else max(3, args.steps // 2)):
+    for _ in range(max(3, args.steps // 2) if e2e else 0):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -444,6 +456,33 @@ class OracleSample:
 
 # ------------------------------------------------------------------ main
 
+def prefill_kernel_name(pre):
+    if pre["w"].dtype != "bf16":
+        return "recurrent_kernel (token-recurrent fp32 prefill)"
+    if pre["B"] * pre["w"].H <= 64:
+        return "coop_kernel (cooperative chunked prefill)"
+    return "chunked_kernel (per-state chunked prefill)"
+
+
+def prefill_roofline(pre, kern_s, P, traffic_key):
+    """Roofline of a prefill call's main kernel: algorithmic bytes (and tensor
+    FLOP) over its CUDA-event time, against the measured HBM copy bandwidth
+    (and bf16 dense peak)."""
+    algo_gbs = pre["nbytes"] / kern_s / 1e9
+    algo_tflops = pre["flops"] / kern_s / 1e12
+    return {"bound": "hbm", "achieved": algo_gbs, "peak": P["hbm_gbs"], "unit": "GB/s",
+            "frac": algo_gbs / P["hbm_gbs"],
+            "traffic": None if traffic_key is None else ncu_traffic(
+                traffic_key, ["kda_chunked.cu", "kda_sm100.cuh"]),
+            "kernel": prefill_kernel_name(pre),
+            "kernel_ms": kern_s * 1e3, "algorithmic_bytes": pre["nbytes"],
+            "peak_source": P["source"],
+            "tensor": None if pre["w"].dtype != "bf16" else {
+                "achieved": algo_tflops, "unit": "TFLOP/s", "peak": P.get("bf16_tflops"),
+                "frac": algo_tflops / P.get("bf16_tflops", 1900.0),
+                "algorithmic_flops": pre["flops"]}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -452,12 +491,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=HEADLINE,
                     choices=["prefill_8k", "varlen_resume", "prefill_1m", "tiny_f32"],
-                    help="prefill workload of a step (default: the 8k-token single sequence)")
+                    help="prefill workload of a step (default: the 2^20-token single sequence)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="shorten the step's single-sequence workload to this many tokens "
+                         "(profiling captures of a smaller case; not a bench number)")
     ap.add_argument("--retain", type=int, default=0,
                     help="keep every N-th interval snapshot in pool slots (retention map) "
                          "instead of writing all of them to the snapshot buffer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other prefill workloads (reported under \"prefill\")")
     ap.add_argument("--no-prefill", action="store_true", help="decode only (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     args = ap.parse_args()
@@ -480,11 +524,25 @@ def main():
 
     P = peaks()
     if not args.no_prefill:
-        pre = bench_prefill(args, torch, kda, inputs, world, rank)
+        pre = bench_prefill(args, torch, kda, inputs, world, rank, args.workload,
+                            retain=args.retain, e2e=not args.no_e2e)
         step_s = statistics.mean(pre["call_ms"]) / 1e3
         kern_s = statistics.mean(pre["kern_ms"]) / 1e3
         e2e_s = statistics.mean(pre["e2e_ms"]) / 1e3 if pre["e2e_ms"] else float("nan")
         step_s, e2e_s, kern_s = reduce_over_ranks(torch, [step_s, e2e_s, kern_s], "cuda")
+
+    extra = {}
+    if not (args.no_prefill or args.no_extra or args.tokens):
+        for name in EXTRA_PREFILL:
+            if name == args.workload:
+                continue
+            r = bench_prefill(args, torch, kda, inputs, world, rank, name, e2e=False)
+            ks = statistics.mean(r["kern_ms"]) / 1e3
+            cs = statistics.mean(r["call_ms"]) / 1e3
+            extra[name] = {"workload": r["w"].note, "ms_per_call": cs * 1e3,
+                           "kernel_ms": ks * 1e3, "tokens_per_s": r["T"] / cs,
+                           "snapshots": r["n_snaps"], "resumed": r["n_resumed"],
+                           "roofline": prefill_roofline(r, ks, P, "prefill_" + name)}
 
     dec = {}
     if not args.no_decode:
@@ -516,15 +574,7 @@ def main():
         cpu = OracleSample(args.workload).measure(target_s=12.0, one_core=True)
         cpu.pop("seconds", None)
 
-    algo_gbs = pre["nbytes"] / kern_s / 1e9
-    algo_tflops = pre["flops"] / kern_s / 1e12
-    chunked = "kda_chunked.cu"
-    if pre["w"].dtype != "bf16":
-        kernel = "recurrent_kernel (token-recurrent fp32 prefill)"
-    elif pre["B"] * pre["w"].H <= 64:
-        kernel = "coop_kernel (cooperative chunked prefill)"
-    else:
-        kernel = "chunked_kernel (per-state chunked prefill)"
+    short = f" shortened to {args.tokens} tokens" if args.tokens else ""
     line = {
         "metric": METRIC,
         "value": job_throughput(pre["T"], world, step_s),
@@ -538,25 +588,15 @@ def main():
         "vs_baseline": None,
         "dtype": pre["w"].dtype,
         "data": "synthetic (seeded; q,k L2-normalised, g=-exp(N(-3,1)), beta=sigmoid(N(0,1)))",
-        "config": {"workload": f'{pre["w"].name}: {pre["w"].note}', "B": pre["B"],
+        "config": {"workload": f'{pre["w"].name}: {pre["w"].note}{short}', "B": pre["B"],
                    "T": pre["T"], "H": pre["w"].H, "dk": pre["w"].dk, "dv": pre["w"].dv,
                    "snapshots": pre["n_snaps"], "resumed": pre["n_resumed"],
                    **({"retention": f"every {args.retain}th interval snapshot kept in a pool "
                                     "slot (kda_prefill_varlen_retain)"} if args.retain else {}),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                   "l2": "flushed between timed steps (256 MiB write)"},
-        "roofline": {"bound": "hbm", "achieved": algo_gbs, "peak": P["hbm_gbs"], "unit": "GB/s",
-                     "frac": algo_gbs / P["hbm_gbs"],
-                     "traffic": None if args.retain else ncu_traffic("prefill_" + args.workload,
-                                                                     [chunked, "kda_sm100.cuh"]),
-                     "kernel": kernel,
-                     "kernel_ms": kern_s * 1e3, "algorithmic_bytes": pre["nbytes"],
-                     "peak_source": P["source"],
-                     "tensor": None if pre["w"].dtype != "bf16" else {
-                         "achieved": algo_tflops, "unit": "TFLOP/s",
-                         "peak": P.get("bf16_tflops"),
-                         "frac": algo_tflops / P.get("bf16_tflops", 1900.0),
-                         "algorithmic_flops": pre["flops"]}},
+                   "l2": "flushed between timed steps (256 MiB write); inputs exceed L2"},
+        "roofline": prefill_roofline(pre, kern_s, P, None if (args.retain or args.tokens)
+                                     else "prefill_" + args.workload),
         "cpu_baseline": cpu,
         "e2e": None if args.no_e2e else {"value": job_throughput(pre["T"], world, e2e_s),
                                          "unit": "tokens/s",
@@ -564,6 +604,7 @@ def main():
                                          "d2h_bytes_per_step": pre["d2h"]},
         "gpu_launches": pre["launches"],
         "clocks": pre["clocks"],
+        "prefill": extra,
         "decode": dec,
     }
     print(json.dumps(line), flush=True)

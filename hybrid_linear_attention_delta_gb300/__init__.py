@@ -223,11 +223,17 @@ def kda_decode_spec(q, k, v, g, beta, slot_ids, state_pool, out, n_tok: int, k_p
 
 
 def kda_decode_noalloc(q, k, v, g, beta, slot_ids, state_pool, out, n_tok: int = 1,
-                       per_tok_states=None, err_bits=None, *, stream=None) -> None:
+                       per_tok_states=None, err_bits=None, *, stream=None):
     """kda_decode for dk = dv = 128 without a workspace: for callers that may
     not allocate device memory (see kda_decode_noalloc in include/kda.h).
-    err_bits: optional int32/uint32 CUDA tensor of one element that collects
-    the device-side check bits."""
+    err_bits: int32/uint32 CUDA tensor of one element that collects the
+    device-side check bits (the caller clears it).  When it is not given, a
+    zeroed one is created on the device of ``out`` (the only allocation here,
+    from torch's cache, in Python, not in the library), so that a bad or
+    duplicate slot is never silently dropped.  Returns err_bits."""
+    if err_bits is None:
+        import torch
+        err_bits = torch.zeros(1, dtype=torch.int32, device=out.device)
     a = make_args(B=slot_ids.numel(), T_total=q.shape[0], H=q.shape[1], dk=q.shape[2],
                   dv=v.shape[2], n_slots=state_pool.shape[0], dtype=_dtype_code(q),
                   stream=stream)
@@ -236,6 +242,7 @@ def kda_decode_noalloc(q, k, v, g, beta, slot_ids, state_pool, out, n_tok: int =
                                   _ptr(per_tok_states), _ptr(err_bits), ctypes.byref(a))
     if st != KDA_OK:
         raise KdaError(st, "kda_decode_noalloc")
+    return err_bits
 
 
 def kda_device_status(workspace, stream=None):

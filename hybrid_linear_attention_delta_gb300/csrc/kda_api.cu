@@ -1,20 +1,44 @@
 // kda_api.cu -- the extern "C" entry points of libkda.so (declared in
 // include/kda.h): host-side argument checks, workspace carving, and the
 // stream-ordered launches.  No device memory is allocated here.
-#include <atomic>
 #include <cstring>
+#include <mutex>
+#include <set>
+#include <unordered_map>
+#include <utility>
 
 #include "kda_internal.cuh"
 
 namespace {
 
 thread_local int32_t g_last_launches = 0;
-std::atomic<uint32_t> g_epoch{0};
 
-uint32_t next_epoch() {
-  uint32_t e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
-  if (e == 0) e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;  // 0 marks "never claimed"
-  return e;
+// Epochs are counted per workspace: every stamp a call leaves in a workspace
+// (slot claims, rerun flags, cooperative ready / consumed flags) holds that
+// call's epoch, and a later call on the same workspace must never reuse it.
+// When a workspace's 32-bit count wraps, its stamp regions are zero-filled on
+// the call's stream (no allocation) before epoch 1 is handed out again.
+std::mutex g_epoch_mu;
+std::unordered_map<const void *, uint32_t> g_epochs;
+
+cudaError_t next_epoch(const kda_args *a, uint32_t *epoch) {
+  bool wrapped = false;
+  {
+    std::lock_guard<std::mutex> lock(g_epoch_mu);
+    uint32_t &count = g_epochs[a->workspace];
+    if (++count == 0) {  // 0 marks "never stamped"
+      count = 1;
+      wrapped = true;
+    }
+    *epoch = count;
+  }
+  if (!wrapped) return cudaSuccess;
+  // every stamp in the workspace may equal an epoch of the new cycle: clear
+  // everything but the sticky error word (stream-ordered, nothing allocated)
+  const size_t n = kda::WorkspaceLayout(a->B, a->H, a->n_slots).total;
+  return n > 256 ? cudaMemsetAsync(static_cast<char *>(a->workspace) + 256, 0, n - 256,
+                                   static_cast<cudaStream_t>(a->stream))
+                 : cudaSuccess;
 }
 
 bool dim_ok(int32_t d) { return d == 16 || d == 32 || d == 64 || d == 128; }
@@ -46,6 +70,23 @@ void record(void *ev, cudaStream_t s) {
 }
 
 }  // namespace
+
+namespace kda {
+
+cudaError_t set_smem_limit_once(const void *func, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void *, int>> done;  // (function, device)
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({func, dev})) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({func, dev});
+  return e;
+}
+
+}  // namespace kda
 
 extern "C" {
 
@@ -109,7 +150,8 @@ kda_status prefill(const void *q, const void *k, const void *v, const void *g, c
   p.meta = reinterpret_cast<kda::SeqMeta *>(ws + lay.meta_off);
   p.order = reinterpret_cast<int32_t *>(ws + lay.order_off);
   p.claims = reinterpret_cast<uint32_t *>(ws + lay.claims_off);
-  p.epoch = next_epoch();
+  p.rerun = reinterpret_cast<uint32_t *>(ws + lay.rerun_off);
+  if ((st = from_cuda(next_epoch(a, &p.epoch))) != KDA_OK) return st;
   p.stream = static_cast<cudaStream_t>(a->stream);
   if (lay.coop_units > 0) {
     p.coop_hdr = reinterpret_cast<uint32_t *>(ws + lay.coop_off);
@@ -132,7 +174,15 @@ kda_status prefill(const void *q, const void *k, const void *v, const void *g, c
   record(a->ev_begin, p.stream);
   st = from_cuda(chunked ? kda::launch_chunked_prefill(p, mode) : kda::launch_recurrent_prefill(p));
   record(a->ev_end, p.stream);
-  if (st == KDA_OK) g_last_launches = 2;
+  if (st != KDA_OK) return st;
+  g_last_launches = 2;
+  if (chunked) {
+    // units whose decay left the chunked algorithm's exponent range are
+    // recomputed by the exact token-recurrent kernel (every other CTA of this
+    // launch returns at once)
+    if ((st = from_cuda(kda::launch_recurrent_prefill(p, true))) != KDA_OK) return st;
+    g_last_launches = 3;
+  }
   return st;
 }
 
@@ -179,7 +229,7 @@ kda_status kda_decode(const void *q, const void *k, const void *v, const void *g
   p.n_slots = a->n_slots; p.dtype = a->dtype;
   p.err = reinterpret_cast<uint32_t *>(ws);
   p.claims = reinterpret_cast<uint32_t *>(ws + lay.claims_off);
-  p.epoch = next_epoch();
+  if ((st = from_cuda(next_epoch(a, &p.epoch))) != KDA_OK) return st;
   p.stream = static_cast<cudaStream_t>(a->stream);
   const bool fast = a->dk == 128 && a->dv == 128;
   record(a->ev_begin, p.stream);
@@ -218,7 +268,7 @@ kda_status kda_decode_spec(const void *q, const void *k, const void *v, const vo
   p.n_slots = a->n_slots; p.dtype = a->dtype;
   p.err = reinterpret_cast<uint32_t *>(ws);
   p.claims = reinterpret_cast<uint32_t *>(ws + lay.claims_off);
-  p.epoch = next_epoch();
+  if ((st = from_cuda(next_epoch(a, &p.epoch))) != KDA_OK) return st;
   p.stream = static_cast<cudaStream_t>(a->stream);
   p.spec = 1;
   p.n_prev = n_prev;

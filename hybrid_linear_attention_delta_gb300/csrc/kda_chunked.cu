@@ -104,6 +104,12 @@ struct ChunkArgs {
   int32_t snap_interval;
   int32_t H, dv, n_dvb;
   uint32_t *err;
+  // [B*H] by (longest-first rank * H + head): set to epoch for a unit whose
+  // decay left the chunked algorithm's exponent range; such a unit's final
+  // state is not written here (its source stays intact) and the exact
+  // token-recurrent kernel recomputes it after this kernel
+  uint32_t *rerun;
+  uint32_t epoch;
   // per-state kernel: snapshots leave through TMA stores (fp32 maps over the
   // snapshot buffer and the pool are valid); else through direct stores
   int32_t snap_tma;
@@ -289,8 +295,9 @@ __device__ __forceinline__ void solve_T(const float *L, const float *LT, float *
 // Thread: channels [8 cq, 8 cq + 8) x rows [4 rg, 4 rg + 4), 16-byte accesses.
 // Ends with the operand writes fenced for the tensor cores and a barrier.
 // A channel whose decay within one half of the chunk exceeds kMaxHalfDecay
-// nats would overflow e^{|G - a|} in fp32 / bf16; such a chunk raises
-// ERR_DECAY_RANGE (the token-recurrent algorithm has no such limit).
+// nats would overflow e^{|G - a|} in fp32 / bf16: the function then returns
+// true (on every thread), and the caller hands the whole (sequence, head) to
+// the token-recurrent kernel, which has no such limit.
 constexpr float kMaxHalfDecay = 80.f;
 
 // beta of row tid of a chunk (threads 0..63; zero past the chunk's end), read
@@ -300,9 +307,8 @@ __device__ __forceinline__ float load_beta(const __nv_bfloat16 *beta_t0, int H, 
 }
 
 template <class Ly, int VCOLS>
-__device__ __forceinline__ void prep_chunk(uint32_t sb, int cl, float beta_r, float *s_gpart,
-                                           float *s_beta, float *s_tot, float *s_anc, int tid,
-                                           uint32_t *err) {
+__device__ __forceinline__ bool prep_chunk(uint32_t sb, int cl, float beta_r, float *s_gpart,
+                                           float *s_beta, float *s_tot, float *s_anc, int tid) {
   const int cq = tid & 15, rg = tid >> 4;
   const uint32_t okq = (cq >> 3) * 16384, og = Ly::kG + (cq >> 3) * 8192;
   float gl[4][8];  // in-group inclusive cumulative decay
@@ -378,7 +384,7 @@ __device__ __forceinline__ void prep_chunk(uint32_t sb, int cl, float beta_r, fl
     st_shared_v4(sb + og + ck, km[0], km[1], km[2], km[3]);
   }
   fence_async_smem();
-  if (__syncthreads_or(out_of_range) && tid == 0) raise_error(err, ERR_DECAY_RANGE);
+  return __syncthreads_or(out_of_range) != 0;
 }
 
 // MMA1: [K+; Q+] K-^T -> d (64 columns: rows 0..63 A-raw, rows 64..127 Q+K-^T).
@@ -583,6 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t mma_phase = 0;
   bool mma_pending = false;
   bool aborted = false;
+  bool flagged = false;  // a chunk's decay left the exponent range: recomputed exactly later
   if (tid == 0 && nchunks > 0) issue_tma(0);
   tma_pending[0] = nchunks > 0;
 
@@ -622,8 +629,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_pending[st] = false;
 
     // ------------------------------------------------------------ prep
-    prep_chunk<Ly, DV>(sb, cl, beta_n, s_gpart, s_beta, s_tot, s_anc,
-                       tid, a.err);
+    if (prep_chunk<Ly, DV>(sb, cl, beta_n, s_gpart, s_beta, s_tot, s_anc, tid) && !flagged) {
+      flagged = true;
+      if (tid == 0) atomicExch(a.rerun + rank * H + h, a.epoch);
+    }
 
     // ------------------------------------------------------------ MMA1
     if (tid == 0) {
@@ -846,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s)
       if (tma_pending[s]) mbar_wait(bar_tma0 + 8 * s, tma_parity[s]);
     if (mma_pending) mbar_wait(bar_mma, mma_phase);
-  } else {
+  } else if (!flagged) {  // a flagged unit keeps its source for the exact recomputation
     float4 *dst = reinterpret_cast<float4 *>(
         a.pool + (((int64_t)m.dst * H + h) * kDK + c) * dv + dv0 + col0);
 #pragma unroll
@@ -1067,8 +1076,12 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     ++uses[st];
     tma_pending[st] = false;
 
-    prep_chunk<Ly, 128>(sb, cl, beta_n, s_gpart, s_beta, s_tot, s_anc,
-                        tid, a.c.err);
+    if (prep_chunk<Ly, 128>(sb, cl, beta_n, s_gpart, s_beta, s_tot, s_anc, tid) && tid == 0) {
+      // the flag is written before this chunk's package is published, so the
+      // pair's chain CTA sees it by the time it has taken its last package
+      atomicExch(a.c.rerun + u, a.epoch);
+      __threadfence();
+    }
     if (tid == 0) {
       issue_mma1<Ly>(tmem + 256, sb);
       mma_commit(bar_mma);
@@ -1444,7 +1457,10 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
       }
     }
     if (!failed && N > 0 && !retire(N - 1)) failed = true;
-    if (!failed && m.ok) {
+    // a unit flagged by a producer keeps its source for the exact recomputation
+    const bool flagged =
+        atomicAdd(a.c.rerun + u, 0u) == a.epoch;  // (all of its packages are consumed)
+    if (!failed && m.ok && !flagged) {
       float *d = a.c.pool + ((int64_t)m.dst * H + h) * kDK * dv + j;
 #pragma unroll
       for (int c = 0; c < kDK; ++c) d[c * cs] = S[c];
@@ -1602,13 +1618,8 @@ template <int DV>
 cudaError_t launch_dv(const PrefillPlan &p, const CUtensorMap &mq, const CUtensorMap &mk,
                       const CUtensorMap &mv, const CUtensorMap &mg) {
   constexpr uint32_t smem = Layout<DV>::kBytes;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(chunked_kernel<DV>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = set_smem_limit_once(reinterpret_cast<const void *>(chunked_kernel<DV>), smem);
+  if (e != cudaSuccess) return e;
   ChunkArgs a;
   a.beta = static_cast<const __nv_bfloat16 *>(p.beta);
   a.meta = p.meta;
@@ -1623,6 +1634,8 @@ cudaError_t launch_dv(const PrefillPlan &p, const CUtensorMap &mq, const CUtenso
   a.dv = p.dv;
   a.n_dvb = p.dv / DV;
   a.err = p.err;
+  a.rerun = p.rerun;
+  a.epoch = p.epoch;
   const unsigned grid = (unsigned)((int64_t)p.B * p.H * a.n_dvb);
   CUtensorMap mo, msnap, mpool;
   if (!make_map(&mo, p.out, (uint64_t)p.H * p.dv, (uint64_t)p.T_total)) return cudaErrorInvalidValue;
@@ -1640,13 +1653,8 @@ cudaError_t launch_dv(const PrefillPlan &p, const CUtensorMap &mq, const CUtenso
 // Grid of the cooperative kernel on the current device (0 when it cannot run
 // there: no cooperative launch, or fewer than 16 producer CTAs would remain).
 int coop_grid(int units) {
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(coop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kCoopSmem) != cudaSuccess)
-      return 0;
-    attr = true;
-  }
+  if (set_smem_limit_once(reinterpret_cast<const void *>(coop_kernel), kCoopSmem) != cudaSuccess)
+    return 0;
   int dev = 0, sms = 0, coop = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -1674,6 +1682,8 @@ cudaError_t launch_coop(const PrefillPlan &p, int grid, const CUtensorMap &mq,
   a.c.dv = p.dv;
   a.c.n_dvb = 1;
   a.c.err = p.err;
+  a.c.rerun = p.rerun;
+  a.c.epoch = p.epoch;
   a.c.snap_tma = 0;  // the chain CTAs store snapshots directly (coalesced columns)
   a.units = p.B * p.H;
   a.ring = p.coop_ring;

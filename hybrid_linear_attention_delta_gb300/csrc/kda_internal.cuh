@@ -7,6 +7,11 @@
 //   [.., +align(B*4))        int32 order[B]: sequences, longest first
 //   [.., +align(n_slots*H*4*4)) uint32 claims: epoch stamps that detect two
 //                            sequences of one call writing the same state
+//   [.., +align(B*H*4))      uint32 rerun[B*H] (prefill, indexed by longest-first
+//                            rank * H + head): the call's epoch when the chunked
+//                            kernel found a decay beyond its exponent range in
+//                            that (sequence, head); the exact token-recurrent
+//                            kernel then recomputes the unit in the same call
 //   when B*H <= kCoopMaxUnits, the cooperative prefill's section:
 //   [.., +256)               uint32 ticket, abort word, longest sequence in chunks
 //   [.., +align(B*H*R*16))   u64 ready[B*H][R], consumed[B*H][R] flags (R = kCoopRing)
@@ -27,7 +32,7 @@ enum ErrBits : uint32_t {
   ERR_BAD_CU = 4u,
   ERR_SNAP_CAPACITY = 8u,
   ERR_TIMEOUT = 16u,
-  ERR_DECAY_RANGE = 32u,
+  ERR_RESERVED_32 = 32u,  // no longer raised: such units are recomputed exactly
   ERR_BAD_ACCEPT = 64u,
 };
 
@@ -56,13 +61,15 @@ constexpr size_t kCoopPkgBytes = 74752;
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WorkspaceLayout {
-  size_t meta_off, order_off, claims_off, coop_off, coop_flags_off, coop_ring_off, total;
+  size_t meta_off, order_off, claims_off, rerun_off, coop_off, coop_flags_off, coop_ring_off,
+      total;
   int64_t coop_units;
   __host__ __device__ WorkspaceLayout(int64_t B, int64_t H, int64_t n_slots) {
     meta_off = 256;
     order_off = meta_off + align256((size_t)B * sizeof(SeqMeta));
     claims_off = order_off + align256((size_t)B * sizeof(int32_t));
-    coop_off = claims_off + align256((size_t)n_slots * H * kClaimsPerState * sizeof(uint32_t));
+    rerun_off = claims_off + align256((size_t)n_slots * H * kClaimsPerState * sizeof(uint32_t));
+    coop_off = rerun_off + align256((size_t)B * H * sizeof(uint32_t));
     coop_units = (B * H <= kCoopMaxUnits) ? B * H : 0;
     // header (ticket, abort, max chunks) | ready[u][ring] | consumed[u][ring] | ring
     coop_flags_off = coop_off + 256;
@@ -127,6 +134,9 @@ struct PrefillPlan {
   SeqMeta *meta;
   int32_t *order;
   uint32_t *claims;
+  // [B*H] per (longest-first rank, head): == epoch when the chunked kernel
+  // handed the unit to the exact recurrent kernel (decay beyond its range)
+  uint32_t *rerun;
   uint32_t epoch;
   cudaStream_t stream;
   // cooperative mode (null when the workspace has no room for it)
@@ -157,13 +167,18 @@ struct DecodePlan {
 };
 
 cudaError_t launch_meta(const PrefillPlan &p);
-cudaError_t launch_recurrent_prefill(const PrefillPlan &p);
+// rerun_only: recompute only the units that the chunked kernel flagged in
+// p.rerun with the call's epoch (every other CTA returns at once)
+cudaError_t launch_recurrent_prefill(const PrefillPlan &p, bool rerun_only = false);
 cudaError_t launch_recurrent_decode(const DecodePlan &p);
 cudaError_t launch_decode128(const DecodePlan &p);
 // The chunked tensor-core prefill: whether it applies to these shapes, whether
 // its cooperative mode can run, and the launch (mode: which variant).
 enum ChunkMode { kChunkAuto = 0, kChunkPerState = 1, kChunkCoop = 2 };
 bool chunked_supported(const PrefillPlan &p);
+// cudaFuncSetAttribute(func, MaxDynamicSharedMemorySize, bytes) once per
+// (function, device) in this process (thread-safe)
+cudaError_t set_smem_limit_once(const void *func, int bytes);
 bool coop_supported(const PrefillPlan &p);
 cudaError_t launch_chunked_prefill(const PrefillPlan &p, int mode);
 

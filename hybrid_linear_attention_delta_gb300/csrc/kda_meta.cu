@@ -137,8 +137,12 @@ __global__ void __launch_bounds__(kMetaThreads) meta_kernel(PrefillPlan p) {
   }
   __syncthreads();
 
-  // 6. cooperative-mode header: ticket and abort cleared, longest sequence in chunks
+  // 6. cooperative-mode header: ticket and abort cleared, longest sequence in
+  // chunks; ready / consumed flags cleared (the workspace may have held other
+  // data at their place in a call with other sizes)
   if (p.coop_hdr) {
+    const int nflags = 2 * p.B * p.H * kCoopRing;
+    for (int i = tid; i < nflags; i += kMetaThreads) p.coop_flags[i] = 0ull;
     int mx = 0;
     for (int b = tid; b < B; b += kMetaThreads) {
       const SeqMeta m = p.meta[b];

@@ -14,7 +14,6 @@
 // until the process exits.  Its device address is looked up once per device
 // with cudaGetSymbolAddress; the host symbol itself is only a stand-in and is
 // never given to a kernel.
-#include <atomic>
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -33,11 +32,14 @@ static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoallocScratchWords
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
 uint32_t *g_scratch_ptr[kMaxDevices] = {};
-std::atomic<uint32_t> g_noalloc_epoch{0};
+// per device: the epoch of the last call, the stamp its claims carry
+uint32_t g_epoch[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device (set up on the
-// first call per device).  nullptr when the lookup fails.
-uint32_t *scratch_on_current_device() {
+// first call per device) and the epoch of this call there; *wrapped is set
+// when that device's 32-bit epoch count has just wrapped, so that every stamp
+// left in its table could equal a new epoch.  nullptr when the lookup fails.
+uint32_t *scratch_on_current_device(uint32_t *epoch, bool *wrapped) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_setup_mu);
@@ -49,6 +51,9 @@ uint32_t *scratch_on_current_device() {
     }
     g_scratch_ptr[dev] = static_cast<uint32_t *>(ptr);
   }
+  *wrapped = ++g_epoch[dev] == 0;  // 0 marks "never claimed"
+  if (*wrapped) g_epoch[dev] = 1;
+  *epoch = g_epoch[dev];
   return g_scratch_ptr[dev];
 }
 
@@ -75,8 +80,15 @@ extern "C" kda_status kda_decode_noalloc(const void *q, const void *k, const voi
     if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
   if (!slot_ids || (per_tok_states && !aligned16(per_tok_states))) return KDA_ERR_INVALID_ARG;
 
-  uint32_t *scratch = scratch_on_current_device();
+  uint32_t epoch = 0;
+  bool wrapped = false;
+  uint32_t *scratch = scratch_on_current_device(&epoch, &wrapped);
   if (!scratch) return KDA_ERR_CUDA;
+  // after 2^32 - 1 calls on a device the claim table is cleared once, on the
+  // call's stream (a memset of the library's own array: nothing is allocated)
+  if (wrapped && cudaMemsetAsync(scratch, 0, kNoallocScratchWords * sizeof(uint32_t),
+                                 static_cast<cudaStream_t>(a->stream)) != cudaSuccess)
+    return KDA_ERR_CUDA;
 
   DecodePlan p = {};
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
@@ -85,9 +97,7 @@ extern "C" kda_status kda_decode_noalloc(const void *q, const void *k, const voi
   p.n_slots = a->n_slots; p.dtype = a->dtype;
   p.err = err_bits ? err_bits : scratch;
   p.claims = scratch + 64;
-  uint32_t e = g_noalloc_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
-  if (e == 0) e = g_noalloc_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
-  p.epoch = e;
+  p.epoch = epoch;
   p.stream = static_cast<cudaStream_t>(a->stream);
   return launch_decode128(p) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

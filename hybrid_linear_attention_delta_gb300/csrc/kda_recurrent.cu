@@ -43,6 +43,9 @@ struct RecArgs {
   uint32_t *err;
   uint32_t *claims;
   uint32_t epoch;
+  // prefill recomputation of the units the chunked kernel handed over:
+  // rerun[rank * H + h] == epoch selects a unit, every other CTA returns
+  const uint32_t *rerun;
 };
 
 // R lanes share one column (R = 2 for dk = 128 keeps the column in 64
@@ -88,6 +91,7 @@ __global__ void __launch_bounds__(32) recurrent_kernel(RecArgs a) {
     src = dst = slot;
     snap_off = (int64_t)n * a.n_tok;
   } else {
+    if (a.rerun && a.rerun[(int64_t)blockIdx.x * H + h] != a.epoch) return;
     const SeqMeta m = a.meta[a.order[blockIdx.x]];
     if (!m.ok) return;
     tok0 = m.tok0;
@@ -227,8 +231,9 @@ cudaError_t launch(const RecArgs &a, int dk, int dv, int nseq, int dtype, cudaSt
 
 }  // namespace
 
-cudaError_t launch_recurrent_prefill(const PrefillPlan &p) {
+cudaError_t launch_recurrent_prefill(const PrefillPlan &p, bool rerun_only) {
   RecArgs a = {};
+  a.rerun = rerun_only ? p.rerun : nullptr;
   a.q = p.q; a.k = p.k; a.v = p.v; a.g = p.g; a.beta = p.beta;
   a.pool = p.pool; a.out = p.out; a.snaps = p.snaps; a.snap_slots = p.snap_slots;
   a.snaps_capacity = p.snaps_capacity;

@@ -70,7 +70,15 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
  * grid in which the other SMs prepare chunks for the per-pair CTAs.  CHUNKED
  * lets the library choose the variant; CHUNKED_PER_STATE and CHUNKED_COOP
  * force one.  A forced choice that does not apply returns
- * KDA_ERR_UNSUPPORTED. */
+ * KDA_ERR_UNSUPPORTED.
+ *
+ * The chunked algorithm scales its operands by exp(+-(G_r - a)), G_r the
+ * in-chunk cumulative log-decay and a its value at mid-chunk, which stays
+ * within fp32 range while one channel's decay within half a chunk is at most
+ * 80 nats.  A (sequence, head) that goes beyond is recomputed in the same
+ * call, outputs, snapshots and final state, by the exact token-recurrent
+ * kernel (launched after every chunked prefill; its CTAs return at once when
+ * no unit needs it), so every finite gate gives the recurrence's result. */
 typedef enum {
   KDA_ALGO_AUTO = 0,
   KDA_ALGO_RECURRENT = 1,
@@ -256,12 +264,16 @@ kda_status kda_decode_spec(const void *q, const void *k, const void *v, const vo
  *
  * err_bits: NULL, or a caller-owned device uint32 that the kernel ORs the
  * device-side check bits into (same bits as kda_device_status reports); the
- * caller clears it.
+ * caller clears it.  With NULL the bits go to a word nobody reads: a slot id
+ * out of range or a duplicate slot then skips that sequence with no way for
+ * the caller to notice, so pass err_bits unless the slots are known valid.
  *
  * The first call on each device looks up the array's device address on the
  * current device (cudaGetSymbolAddress); make that first call before any
  * stream capture.  Every call shares the one array and leaves its contents
- * behind (claims are stamped per call, so nothing needs clearing); calls that
+ * behind (claims are stamped with a per-device call count, so nothing needs
+ * clearing; when that 32-bit count wraps, after 2^32 - 1 calls on a device,
+ * the call clears the array once with a memset on its stream); calls that
  * overlap on the GPU race on it and may miss a duplicate slot, so order them
  * on one stream.
  */
@@ -270,7 +282,14 @@ kda_status kda_decode_noalloc(const void *q, const void *k, const void *v, const
                               void *out, int32_t n_tok, float *per_tok_states, uint32_t *err_bits,
                               const kda_args *a);
 
-/* Workspace bytes the calls need for these sizes (uses B, H, n_slots). */
+/* Workspace bytes the calls need for these sizes (uses B, H, n_slots).
+ * The snapshot interval does not change the size: snapshot offsets live in
+ * the per-sequence plan, whose size depends on B only.
+ *
+ * Stamps that calls leave in a workspace carry a per-workspace call count;
+ * when that 32-bit count wraps (after 2^32 - 1 calls on one workspace) the
+ * call clears the workspace once (a memset on its stream, keeping the error
+ * word) before reusing the count. */
 size_t kda_workspace_bytes(const kda_args *a);
 
 /* Number of snapshots a prefill writes: sum over b of floor(L_b / snap_interval),
@@ -282,11 +301,12 @@ int64_t kda_snapshot_count(const int32_t *cu_seqlens_host, int32_t B, int32_t sn
  * last call to this function, and clears the record.  If detail is not NULL
  * it receives the raw error bits (1 slot out of range, 2 duplicate slot or a
  * source that is another sequence's destination, 4 bad cu_seqlens, 8 snapshot
- * buffer too small, 16 wait timeout, 32 a channel's decay within half a
- * 64-token chunk exceeded 80 nats, beyond the chunked algorithm's exponent
- * range: its results are not reliable, run that batch with
- * KDA_ALGO_RECURRENT; 64 an accepted length of kda_decode_spec outside
- * [0, n_prev]). */
+ * buffer too small, 16 wait timeout, 64 an accepted length of kda_decode_spec
+ * outside [0, n_prev]; bit 32 is not used).
+ *
+ * Only a->stream and a->workspace are read.  (The status word lives in the
+ * workspace, so the call takes the kda_args that name it rather than only a
+ * stream; several workspaces on one stream are queried separately.) */
 kda_status kda_device_status(const kda_args *a, uint32_t *detail);
 
 /* Human-readable name of a status code (static string). */

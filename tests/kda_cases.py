@@ -103,3 +103,37 @@ def worst_unit(x, ref, cu, H):
             if t1 > t0:
                 worst = max(worst, oracle.rel_l2(x[t0:t1, h], ref[t0:t1, h]))
     return worst
+
+
+def worst_state(x, ref):
+    """Worst relative L2 over the (index, head) blocks of [n, H, dk, dv] states
+    (final states of touched slots, snapshots or per-token states), so that one
+    bad (sequence, head) state is not diluted into a tensor-wide figure."""
+    x = np.asarray(x if not isinstance(x, torch.Tensor) else x.detach().float().cpu().numpy())
+    ref = np.asarray(ref)
+    worst = 0.0
+    for i in range(ref.shape[0]):
+        for h in range(ref.shape[1]):
+            worst = max(worst, oracle.rel_l2(x[i, h], ref[i, h]))
+    return worst
+
+
+class RelL2:
+    """Relative L2 accumulated over pieces of one tensor compared piece by
+    piece (sum of squared differences over sum of squared references)."""
+
+    def __init__(self):
+        self.num = 0.0
+        self.den = 0.0
+
+    def add(self, x, ref):
+        x = np.asarray(x if not isinstance(x, torch.Tensor) else x.detach().float().cpu().numpy(),
+                       dtype=np.float64)
+        ref = np.asarray(ref, dtype=np.float64)
+        self.num += float(np.sum((x - ref) ** 2))
+        self.den += float(np.sum(ref ** 2))
+        return oracle.rel_l2(x, ref)
+
+    @property
+    def value(self):
+        return (self.num / self.den) ** 0.5 if self.den > 0 else self.num ** 0.5

@@ -27,6 +27,16 @@ def test_prefill_bytes_and_flops_8k():
     assert flops == 8192 * 32 * 180_224 == 47_244_640_256
 
 
+def test_prefill_bytes_and_flops_1m():
+    """The headline workload: 2^20 tokens x 16 heads at 1282 B, plus 33 states
+    per head (32 snapshots and the final state)."""
+    w = inputs.WORKLOADS["prefill_1m"]
+    nbytes, flops, token_bytes = bench.prefill_algorithmic(w, [1 << 20], 32, 0, 2)
+    assert token_bytes == (1 << 20) * 16 * 1282 == 21_508_390_912
+    assert nbytes == 21_508_390_912 + 16 * 33 * STATE == 21_542_993_920
+    assert flops == (1 << 20) * 16 * 180_224 == 3_023_656_976_384
+
+
 def test_prefill_bytes_count_resumed_states():
     w = inputs.WORKLOADS["varlen_resume"]
     nbytes, _, _ = bench.prefill_algorithmic(w, [512, 1000], 5, 1, 2)

@@ -9,7 +9,7 @@ import torch
 import hybrid_linear_attention_delta_gb300 as kda
 from hybrid_linear_attention_delta_gb300 import inputs
 from kda_cases import (TOL, assert_untouched, gpu_decode, gpu_prefill, oracle_decode,
-                       oracle_prefill, rel, touched_slots, worst_unit)
+                       oracle_prefill, rel, touched_slots, worst_state, worst_unit)
 
 pytestmark = pytest.mark.gpu
 
@@ -144,6 +144,36 @@ def test_decode_full_size_256x32():
     ro, rpool, _ = oracle_decode(sub)
     assert rel(out, ro) <= TOL["bf16"]
     assert rel(pool[b.slot_ids.long()], rpool) <= TOL["bf16"]
+    assert_untouched(pool, before, touched_slots(b))
+
+
+def test_decode_verify_full_size_64x8():
+    """64 sequences x 8 tokens x 32 heads with per-token states on a 1024-slot
+    pool (the speculative-verify workload, 1 GiB of per-token states): every
+    output, every per-token state and every advanced slot against the oracle,
+    each (sequence, token, head) state and each (sequence, head) output block
+    within 2 tol; the slot holds the last per-token state bit for bit."""
+    w = inputs.WORKLOADS["verify_64x8"]
+    b = inputs.make_batch(w)
+    before = b.pool.clone()
+    out, pool, per, (st, bits) = gpu_decode(b, n_tok=w.n_tok, per_tok=True)
+    assert st == kda.KDA_OK and bits == 0
+    N, n_tok, H = w.B, w.n_tok, w.H
+    sub = inputs.Batch(q=b.q, k=b.k, v=b.v, g=b.g, beta=b.beta, cu_seqlens=b.cu_seqlens,
+                       slot_ids=torch.arange(N, dtype=torch.int32),
+                       pool=b.pool[b.slot_ids.long()])
+    ro, rpool, rper = oracle_decode(sub, n_tok, True)
+    tol = TOL["bf16"]
+    assert rel(out, ro) <= tol
+    assert worst_unit(out, ro, b.cu_seqlens.numpy(), H) <= 2 * tol
+    per_h = per.cpu()
+    assert rel(per_h, rper) <= tol
+    assert worst_state(per_h.reshape(N * n_tok, H, 128, 128),
+                       rper.reshape(N * n_tok, H, 128, 128)) <= 2 * tol
+    slots = b.slot_ids.long()
+    assert rel(pool[slots], rpool) <= tol
+    assert worst_state(pool[slots], rpool) <= 2 * tol
+    assert torch.equal(pool[slots].cpu(), per_h[:, -1])
     assert_untouched(pool, before, touched_slots(b))
 
 

@@ -53,10 +53,13 @@ def test_noalloc_decode_matches_workspace_decode_twice(n_tok, per_tok):
         kda.kda_decode_noalloc(tt["q"], tt["k"], tt["v"], tt["g"], tt["beta"], slots, pool_na,
                                o_na, n_tok, per_na, err)
         torch.cuda.synchronize()
+        # the same decode kernel runs on the same inputs: identical bits, and
+        # the bf16 tolerance the suite uses holds a fortiori
+        assert torch.equal(o_na.cpu(), o_ref.cpu()), step
+        assert torch.equal(pool_na.cpu(), pool_ref.cpu()), step
         assert rel(o_na, o_ref.float().cpu().numpy()) <= TOL["bf16"], step
-        assert rel(pool_na, pool_ref.cpu().numpy()) <= TOL["bf16"], step
         if per_tok:
-            assert rel(per_na, per_ref.cpu().numpy()) <= TOL["bf16"], step
+            assert torch.equal(per_na.cpu(), per_ref.cpu()), step
     assert int(err.item()) == 0
     assert kda.kda_device_status(ws)[0] == kda.KDA_OK
 
@@ -71,6 +74,10 @@ def test_noalloc_reports_duplicate_slots_and_rejects_oversize():
                            None, err)
     torch.cuda.synchronize()
     assert int(err.item()) & 2
+    # without an err_bits tensor the binding makes one and returns it
+    bits = kda.kda_decode_noalloc(tt["q"], tt["k"], tt["v"], tt["g"], tt["beta"], slots, pool,
+                                  out, 1)
+    assert int(bits.item()) & 2
     # a pool beyond the shared claim table (n_slots * H > 131072) is refused up front
     big = torch.empty((1, 1, 1, 1), device="cuda")
     a = kda.make_args(B=N, T_total=N, H=H, dk=128, dv=128, n_slots=70000,
