@@ -904,11 +904,12 @@ static_assert(kPkDec + 512 <= kCoopPkgBytes && kCoopPkgBytes % 1024 == 0, "packa
 // 0.3-0.6% faster than 4 in a same-box A/B)
 constexpr uint32_t kPkPieces = 8, kPkPiece = (uint32_t)kCoopPkgBytes / kPkPieces;
 static_assert(kPkPiece % 16 == 0 && kPkPiece * kPkPieces == kCoopPkgBytes, "bulk copy pieces");
-// chain CTA shared memory: two package stages, two output staging tiles
-// ([64 tok][128 dv] bf16 each, stored with one TMA box), mbarriers, TMEM slot
-constexpr uint32_t kChO = 2 * (uint32_t)kCoopPkgBytes;
-constexpr uint32_t kChMisc = kChO + 2 * 16384;
-constexpr uint32_t kChBytes = kChMisc + 128;
+// chain CTA shared memory: three package stages (a package copy from L2
+// takes about as long as a chunk's state step, so two stages leave the chain
+// waiting for its next package), mbarriers, TMEM slot
+constexpr int kChStages = 3;
+constexpr uint32_t kChMisc = kChStages * (uint32_t)kCoopPkgBytes;
+constexpr uint32_t kChBytes = kChMisc + 192;
 constexpr uint32_t kCoopSmem =
     Layout<128>::kBytes > kChBytes ? Layout<128>::kBytes : kChBytes;
 
@@ -1252,15 +1253,18 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
 //   warps 0-3 (state): thread j holds column j of S (row j of S^T) for all 128
 //     channels in fp32 registers.  Per chunk n it stores bf16(S^T) into TMEM
 //     buffer n & 1 (the A operand of the chunk's state-dependent MMAs),
-//     retires chunk n-1's outputs while those MMAs run, forms
+//     retires chunk n-1's outputs in two halves while X^T and acc^T run, forms
 //     U^T = U~^T - X^T (bf16, into TMEM), then applies
 //     S <- Diag(e^{G_C}) S + acc and writes snapshots.
-//   warp 4, one lane (MMA): per chunk, once S^T is stored, X^T = S^T W^^T
-//     (commit: X ready) and O^T = S^T Q+'^T; once the state warps stored
-//     U^T = U~^T - X^T, acc^T = U^T K^ (commit: acc ready) and O^T += U^T M^T
-//     (commit: outputs ready, stage free).
-//   warp 5, one lane (loader): waits until package n is in the ring, fetches
-//     it into stage n & 1 with bulk copies, and hands the ring slot back.
+//   warp 4, one lane (MMA): per chunk, once package n has landed it hands its
+//     ring slot back to the producers; once S^T is stored, X^T = S^T W^^T
+//     (commit: X ready); once the state warps stored U^T = U~^T - X^T,
+//     acc^T = U^T K^ (commit: acc ready), then the outputs O^T = S^T Q+'^T +
+//     U^T M^T (commit: outputs ready, stage free), so that the state step
+//     never queues behind output work on the tensor cores.
+//   warp 5, one lane (loader): waits until package n is in the ring and its
+//     stage n % 3 is free, and requests it with bulk copies; the next
+//     package's ready flag is read (acquire) while this one is in flight.
 // TMEM columns: acc^T [0, 128); O^T[b] [128 + 64 b, +64); S^T[b] as bf16
 // pairs [256 + 64 b, +64); X^T [384, 448); U^T as bf16 pairs [448, 480).
 // Every wait is bounded; a role that gives up raises the abort word and
@@ -1271,26 +1275,25 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
-// the four state warps of a chain CTA
-__device__ __forceinline__ void state_warps_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-__device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArgs &a, int u) {
+__device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_u32(smem);
   const int H = a.c.H, h = u % H, dv = a.c.dv;
   const SeqMeta m = a.c.meta[a.c.order[u / H]];
-  // mbarriers: full[2] (package landed), empty[2] (stage free: MMAs done and
+  // mbarriers: full[3] (package landed), empty[3] (stage free: MMAs done and
   // the state warps read its U~ and decays), sready[2] (S^T stored), xf
   // (X^T ready), uready (U^T stored), accf (acc^T ready), of[2] / oe[2] (O^T
   // ready / read), drain
   const uint32_t bars = sbase + kChMisc;
-  const uint32_t full0 = bars, empty0 = bars + 16, sready0 = bars + 32, accf = bars + 48,
-                 xf = bars + 56, of0 = bars + 64, oe0 = bars + 80, drain = bars + 96,
-                 uready = bars + 104;
+  const uint32_t full0 = bars, empty0 = bars + 24, sready0 = bars + 48, accf = bars + 64,
+                 xf = bars + 72, of0 = bars + 80, oe0 = bars + 96, drain = bars + 112,
+                 uready = bars + 120;
   if (tid == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kChStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1 + 4);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(sready0 + 8 * s, 4);
       mbar_init(of0 + 8 * s, 1);
       mbar_init(oe0 + 8 * s, 4);
@@ -1301,10 +1304,10 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
     mbar_init(drain, 1);
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(bars + 112, 512);
+  if (warp == 0) tmem_alloc(bars + 128, 512);
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kChMisc + 112);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kChMisc + 128);
   const int N = m.ok ? (m.len + kC - 1) / kC : 0;
   bool failed = false;
 
@@ -1321,47 +1324,35 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
 #pragma unroll
       for (int c = 0; c < kDK; ++c) S[c] = 0.f;
     }
-    // outputs of chunk n from O^T buffer n & 1: token t of the chunk is column t.
-    // A whole chunk goes through staging tile n & 1 and one TMA store; the
-    // ragged last chunk of a sequence is written directly, row by row.
-    auto retire = [&](int n) -> bool {
+    // outputs of chunk n from O^T buffer n & 1: token t of the chunk is
+    // column t, thread j holds value column j.  Stored directly: per token,
+    // the 128 threads write its 128 contiguous outputs (256 bytes).  Half
+    // `hf` (tokens 32 hf .. 32 hf + 31) at a time: the first half goes out
+    // while the next chunk's X^T runs on the tensor cores, the second while
+    // its acc^T runs; the buffer is handed back after the second.
+    auto retire = [&](int n, int hf) -> bool {
       const int b = n & 1;
-      if (!warp_wait(of0 + 8 * b, (n >> 1) & 1)) return false;
+      if (hf == 0 && !warp_wait(of0 + 8 * b, (n >> 1) & 1)) return false;
       tc_fence_after();
-      uint32_t v0[32], v1[32];
-      tmem_ld32_async(lane_base + 128 + 64 * b, v0);
-      tmem_ld32_async(lane_base + 128 + 64 * b + 32, v1);
+      uint32_t v[32];
+      tmem_ld32_async(lane_base + 128 + 64 * b + 32 * hf, v);
       tmem_wait_ld();
-      reg_fence(v0);
-      reg_fence(v1);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(oe0 + 8 * b);
-      const int cl = min(kC, m.len - n * kC);
-      if (cl == kC) {
-        if (tid == 0) bulk_wait_read<1>();  // chunk n-2's store has read tile b
-        state_warps_sync();
-        uint8_t *stg = smem + kChO + b * 16384 + 2 * j;
+      reg_fence(v);
+      if (hf == 1) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(oe0 + 8 * b);
+      }
+      const int cl = min(kC, m.len - n * kC) - 32 * hf;
+      const int64_t ts = (int64_t)H * dv;
+      __nv_bfloat16 *o = a.c.out + ((int64_t)(m.tok0 + n * kC + 32 * hf) * H + h) * dv + j;
+      if (cl >= 32) {
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          *reinterpret_cast<__nv_bfloat16 *>(stg + t * 256) = __float2bfloat16_rn(__uint_as_float(v0[t]));
-          *reinterpret_cast<__nv_bfloat16 *>(stg + (t + 32) * 256) =
-              __float2bfloat16_rn(__uint_as_float(v1[t]));
-        }
-        fence_async_smem();
-        state_warps_sync();
-        if (tid == 0) {
-          tma_store_2d(tm_o, sbase + kChO + b * 16384, h * dv, m.tok0 + n * kC);
-          bulk_commit();
-        }
+        for (int t = 0; t < 32; ++t) o[t * ts] = __float2bfloat16_rn(__uint_as_float(v[t]));
       } else {
-        const int64_t ts = (int64_t)H * dv;
-        __nv_bfloat16 *o = a.c.out + ((int64_t)(m.tok0 + n * kC) * H + h) * dv + j;
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          if (t < cl) o[t * ts] = __float2bfloat16_rn(__uint_as_float(v0[t]));
-          if (t + 32 < cl) o[(t + 32) * ts] = __float2bfloat16_rn(__uint_as_float(v1[t]));
-        }
+        for (int t = 0; t < 32; ++t)
+          if (t < cl) o[t * ts] = __float2bfloat16_rn(__uint_as_float(v[t]));
       }
       return true;
     };
@@ -1369,7 +1360,7 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
     int snap_left = snap_every;
     int64_t snap_next = m.snap_off;
     for (int n = 0; n < N; ++n) {
-      const int b = n & 1;
+      const int b = n & 1, st = n % kChStages;
       // bf16(S^T) -> S^T[b]: column q holds channels 2q (low half) and 2q + 1.
       // Buffer b was last read by chunk n-2's MMAs, which retire(n-2) waited for.
 #pragma unroll
@@ -1383,21 +1374,21 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sready0 + 8 * b);
-      if (n > 0 && !retire(n - 1)) { failed = true; break; }
-      if (!warp_wait(full0 + 8 * b, (n >> 1) & 1) || !warp_wait(xf, n & 1)) {
+      if (n > 0 && !retire(n - 1, 0)) { failed = true; break; }
+      if (!warp_wait(full0 + 8 * st, (n / kChStages) & 1) || !warp_wait(xf, n & 1)) {
         failed = true;
         break;
       }
       tc_fence_after();
+      const uint32_t sp = sbase + st * (uint32_t)kCoopPkgBytes;
       {  // U^T = U~^T - X^T into tensor memory: column q holds tokens 2q (low half), 2q + 1;
          // row j of the package's U~^T holds this thread's 64 tokens
         float x[64];
         tmem_ld64(lane_base + 384, x);
-        const uint32_t ub = sbase + b * (uint32_t)kCoopPkgBytes + kPkU;
         uint32_t r[32];
 #pragma unroll
         for (int q8 = 0; q8 < 8; ++q8) {  // tokens 8 q8 .. 8 q8 + 7
-          const uint4 w = ld_shared_v4(ub + sw128_chunk(j, q8));
+          const uint4 w = ld_shared_v4(sp + kPkU + sw128_chunk(j, q8));
           const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -1411,9 +1402,10 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(uready);
+      if (n > 0) retire(n - 1, 1);
       if (!warp_wait(accf, n & 1)) { failed = true; break; }
       tc_fence_after();
-      const float4 *egc = reinterpret_cast<const float4 *>(smem + b * kCoopPkgBytes + kPkDec);
+      const float4 *egc = reinterpret_cast<const float4 *>(smem + st * kCoopPkgBytes + kPkDec);
 #pragma unroll
       for (int p = 0; p < 2; ++p) {  // S = Diag(e^{G_C}) S + acc, 64 channels at a time
         uint32_t v[2][32];
@@ -1436,7 +1428,7 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * b);
+      if (lane == 0) mbar_arrive(empty0 + 8 * st);
       // a snapshot after every snap_every full chunks (the interval is a
       // multiple of the chunk, so a ragged last chunk never ends on one)
       const int cl = min(kC, m.len - n * kC);
@@ -1456,7 +1448,7 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
         }
       }
     }
-    if (!failed && N > 0 && !retire(N - 1)) failed = true;
+    if (!failed && N > 0 && !(retire(N - 1, 0) && retire(N - 1, 1))) failed = true;
     // a unit flagged by a producer keeps its source for the exact recomputation
     const bool flagged =
         atomicAdd(a.c.rerun + u, 0u) == a.epoch;  // (all of its packages are consumed)
@@ -1465,14 +1457,22 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
 #pragma unroll
       for (int c = 0; c < kDK; ++c) d[c * cs] = S[c];
     }
-    if (tid == 0) bulk_wait<0>();  // every output store complete
   } else if (warp == 4 && lane == 0) {
+    unsigned long long *consumed = a.consumed + u * kCoopRing;
     bool issued = false;
     for (int n = 0; n < N; ++n) {
-      const int b = n & 1;
-      const uint32_t sp = sbase + b * (uint32_t)kCoopPkgBytes;
-      if (!mbar_wait(full0 + 8 * b, (n >> 1) & 1) ||
-          (n > 1 && !mbar_wait(oe0 + 8 * b, ((n - 2) >> 1) & 1)) ||
+      const int b = n & 1, st = n % kChStages;
+      const uint32_t sp = sbase + st * (uint32_t)kCoopPkgBytes;
+      if (!mbar_wait(full0 + 8 * st, (n / kChStages) & 1)) {
+        failed = true;
+        break;
+      }
+      // the package has landed in shared memory (its ring slot has been read
+      // in full), so the slot can take another one; nothing of this thread
+      // needs ordering before the flag, and a release would stall the MMA
+      // issue for an L2 round trip
+      st_relaxed_u64(consumed + n % kCoopRing, coop_tag(a.epoch, n));
+      if ((n > 1 && !mbar_wait(oe0 + 8 * b, ((n - 2) >> 1) & 1)) ||
           !mbar_wait(sready0 + 8 * b, (n >> 1) & 1)) {
         failed = true;
         break;
@@ -1486,10 +1486,7 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
         mma_bf16_ts(xt, sa + kk * 8, sw128_desc(sp + kPkW + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
                     idesc_bf16(128, 64, 0, 0), kk > 0);
       mma_commit(xf);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // O^T = S^T Q+'^T
-        mma_bf16_ts(o, sa + kk * 8, sw128_desc(sp + kPkQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
-                    idesc_bf16(128, 64, 0, 0), kk > 0);
+      // the state step (acc^T) goes ahead of the outputs on the tensor cores
       if (!mbar_wait(uready, n & 1)) { failed = true; break; }
       tc_fence_after();
 #pragma unroll
@@ -1498,11 +1495,15 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
                     idesc_bf16(128, 128, 0, 1), kk > 0);
       mma_commit(accf);
 #pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // O^T = S^T Q+'^T
+        mma_bf16_ts(o, sa + kk * 8, sw128_desc(sp + kPkQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                    idesc_bf16(128, 64, 0, 0), kk > 0);
+#pragma unroll
       for (int kk = 0; kk < 4; ++kk)  // O^T += U^T M^T
         mma_bf16_ts(o, ut + kk * 8, sw128_desc(sp + kPkM + kk * 32, 16, 1024),
                     idesc_bf16(128, 64, 0, 0), 1);
       mma_commit(of0 + 8 * b);
-      mma_commit(empty0 + 8 * b);
+      mma_commit(empty0 + 8 * st);
     }
     if (issued) {  // every MMA done before the tensor memory is released
       mma_commit(drain);
@@ -1510,30 +1511,35 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
     }
   } else if (warp == 5 && lane == 0) {
     const unsigned long long *ready = a.ready + u * kCoopRing;
-    unsigned long long *consumed = a.consumed + u * kCoopRing;
     const uint8_t *ring_u = a.ring + (size_t)u * kCoopRing * kCoopPkgBytes;
+    // The ready flag of the next package is read (acquire) as soon as this
+    // one's copy is requested: that L2 round trip, often to the other die,
+    // then overlaps the wait for the next stage.
+    unsigned long long seen = N > 0 ? ld_acquire_u64(ready) : 0ull;
+    int issued = -1;  // last chunk whose copy was requested
     for (int n = 0; n < N; ++n) {
-      const int b = n & 1;
-      // the ready flag first: reading it is an L2 round trip even when the
-      // package is long published, and that latency then overlaps the wait
-      // for the stage
-      if (!coop_flag_wait(ready + n % kCoopRing, coop_tag(a.epoch, n), a.hdr + 1) ||
-          (n > 1 && !mbar_wait(empty0 + 8 * b, ((n - 2) >> 1) & 1))) {
+      const int st = n % kChStages;
+      const unsigned long long want = coop_tag(a.epoch, n);
+      if (seen < want && !coop_flag_wait(ready + n % kCoopRing, want, a.hdr + 1)) {
         failed = true;
         break;
       }
-      fence_proxy_async_all();  // the package was written with ordinary stores
+      if (n >= kChStages && !mbar_wait(empty0 + 8 * st, ((n - kChStages) / kChStages) & 1)) {
+        failed = true;
+        break;
+      }
+      fence_proxy_async_all();  // the package was written by another SM
       const uint8_t *src = ring_u + (size_t)(n % kCoopRing) * kCoopPkgBytes;
-      const uint32_t dst = sbase + b * (uint32_t)kCoopPkgBytes, bar = full0 + 8 * b;
+      const uint32_t dst = sbase + st * (uint32_t)kCoopPkgBytes, bar = full0 + 8 * st;
       mbar_expect_tx(bar, (uint32_t)kCoopPkgBytes);
       for (uint32_t q = 0; q < kPkPieces; ++q) bulk_g2s(dst + q * kPkPiece, src + q * kPkPiece, kPkPiece, bar);
-      if (!mbar_wait(bar, (n >> 1) & 1)) {
-        failed = true;
-        mbar_wait(bar, (n >> 1) & 1);  // the copy is still writing this CTA's memory
-        break;
-      }
-      st_release_u64(consumed + n % kCoopRing, coop_tag(a.epoch, n));
+      issued = n;
+      if (n + 1 < N) seen = ld_acquire_u64(ready + (n + 1) % kCoopRing);
     }
+    // copies still writing this CTA's shared memory finish before it exits
+    // (the last copy into each stage: earlier ones landed before it was reused)
+    for (int c = issued - kChStages + 1; c <= issued; ++c)
+      if (c >= 0) mbar_wait(full0 + 8 * (c % kChStages), (c / kChStages) & 1);
   }
   if (failed) coop_abort(a);
   tc_fence_before();
@@ -1547,14 +1553,14 @@ __device__ void coop_chain(uint8_t *smem, const CUtensorMap *tm_o, const CoopArg
 __global__ void __launch_bounds__(kThreads, 1)
     coop_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                const __grid_constant__ CUtensorMap tm_o, const CoopArgs a) {
+                const CoopArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023) {  // the swizzled layouts need a 1024-byte aligned base
     if (threadIdx.x == 0) coop_abort(a);
     return;
   }
   if ((int)blockIdx.x < a.units)
-    coop_chain(smem, &tm_o, a, blockIdx.x);
+    coop_chain(smem, a, blockIdx.x);
   else
     coop_producer(smem, &tm_q, &tm_k, &tm_v, &tm_g, a);
 }
@@ -1573,20 +1579,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2D map over a [rows][inner] bf16 array, 64 x 64 boxes, 128-byte swizzle.
-// Output map of the cooperative chain: [rows][inner] bf16, boxes of 64 rows x
-// 128 columns, unswizzled (the staging tile is plain row-major).
-bool make_store_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {128, 64};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -1691,10 +1683,8 @@ cudaError_t launch_coop(const PrefillPlan &p, int grid, const CUtensorMap &mq,
   a.consumed = p.coop_flags + (size_t)a.units * kCoopRing;
   a.hdr = p.coop_hdr;
   a.epoch = p.epoch;
-  CUtensorMap q = mq, k = mk, v = mv, g = mg, o;
-  if (!make_store_map(&o, p.out, (uint64_t)p.H * p.dv, (uint64_t)p.T_total))
-    return cudaErrorInvalidValue;
-  void *args[] = {&q, &k, &v, &g, &o, &a};
+  CUtensorMap q = mq, k = mk, v = mv, g = mg;
+  void *args[] = {&q, &k, &v, &g, &a};
   return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(coop_kernel), dim3(grid),
                                      dim3(kThreads), args, kCoopSmem, p.stream);
 }
