@@ -10,9 +10,10 @@ the device-side plan kernel, the chunked prefill kernel, which writes the
 outputs, the 32 snapshots and the final state, and the exact-recomputation
 launch (which does nothing unless a gate left the chunked algorithm's range).
 The same run also times the single-sequence prefill (B=1, T=8192, H=32,
-snapshots every 1024) and the varlen batch with copy-on-write resume (16
-sequences, snapshots every 256) and reports them under "prefill", each with
-its own roofline, and the batched decode (256 sequences x 1 token), the
+snapshots every 1024), the varlen batch with copy-on-write resume (16
+sequences, snapshots every 256) and three 32768-token sequences at H=32 (96
+(sequence, head) pairs, between the cooperative mode and a full GPU of
+per-state CTAs) and reports them under "prefill", each with its own roofline, and the batched decode (256 sequences x 1 token), the
 speculative-verify decode (64 x 8 tokens with per-token states) and the
 speculative verify with the previous step's commit folded in (64 x 8 tokens,
 kda_decode_spec) under "decode".
@@ -42,7 +43,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "KDA prefill tokens/s & decode state GB/s on 1 GB300, % of tensor/HBM roofline"
 HEADLINE = "prefill_1m"
-EXTRA_PREFILL = ("prefill_8k", "varlen_resume")
+EXTRA_PREFILL = ("prefill_8k", "varlen_resume", "prefill_3x32k")
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -490,7 +491,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=HEADLINE,
-                    choices=["prefill_8k", "varlen_resume", "prefill_1m", "tiny_f32"],
+                    choices=["prefill_8k", "varlen_resume", "prefill_1m", "prefill_3x32k",
+                             "tiny_f32"],
                     help="prefill workload of a step (default: the 2^20-token single sequence)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="shorten the step's single-sequence workload to this many tokens "

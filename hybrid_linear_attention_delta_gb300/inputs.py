@@ -82,6 +82,11 @@ WORKLOADS = {
     "prefill_1m": Workload("prefill_1m", 4, "prefill", H=16, dk=128, dv=128, dtype="bf16", B=1,
                            T=1 << 20, snap_interval=32768,
                            note="B=1 T=2^20 H=16 dk=dv=128 bf16, snapshots every 32768"),
+    # between the cooperative mode's 64 pairs and a full GPU of per-state CTAs
+    "prefill_3x32k": Workload("prefill_3x32k", 5, "prefill", H=32, dk=128, dv=128, dtype="bf16",
+                              B=3, T=32768, snap_interval=1024,
+                              note="B=3 x T=32768 H=32 dk=dv=128 bf16 (96 (sequence, head) "
+                                   "pairs), snapshots every 1024"),
 }
 
 

@@ -198,51 +198,73 @@ def test_prefill_8k_full():
     print(f"prefill_8k: out {e_out:.2e} state {e_state:.2e}")
 
 
-def test_varlen_resume_full():
-    """16 sequences, L ~ U[512, 32768], 8 resumed from a 1024-slot pool, snapshots
-    every 256, all 32 heads: every output, every snapshot and every touched final
-    state against the oracle.  The oracle runs one sequence at a time (all its
-    heads in parallel), so its fp64 copies stay a few GB; whole-tensor errors
-    are accumulated over the sequences, and every (sequence, head) block of the
-    outputs, snapshots and final states is bounded by 2 tol."""
-    w = inputs.WORKLOADS["varlen_resume"]
-    b = inputs.make_batch(w)
-    before = b.pool.clone()
-    out, pool, snaps, (st, bits) = gpu_prefill(b, w.snap_interval)
-    assert st == kda.KDA_OK and bits == 0
-    tol = TOL["bf16"]
+def _check_by_sequence(b, snap, out, pool, snaps, tol=TOL["bf16"]):
+    """The checks of _check for a large batch, with the oracle run one
+    sequence at a time (all its heads in parallel) so that its fp64 copies stay
+    a few GB: whole-tensor errors accumulated over the sequences within tol,
+    every (sequence, head) block of outputs, snapshots and final states within
+    2 tol.  Returns (out, snapshots, states, worst unit) errors."""
+    H = b.q.shape[1]
     cu = b.cu_seqlens.numpy()
-    off, n_total = oracle.snapshot_offsets(cu, w.snap_interval)
-    assert snaps.shape[0] == n_total
+    off, n_total = oracle.snapshot_offsets(cu, snap)
+    if snap:
+        assert snaps.shape[0] == n_total
     e_out, e_snap, e_state = RelL2(), RelL2(), RelL2()
     worst = 0.0
-    for s in range(w.B):
+    for s in range(len(cu) - 1):
         t0, t1 = int(cu[s]), int(cu[s + 1])
         sub = {n: getattr(b, n)[t0:t1] for n in ("q", "k", "v", "g", "beta")}
         src, dst = int(b.init_slots[s, 0]), int(b.init_slots[s, 1])
         init = None if src < 0 else b.pool[src][None]
         res = oracle.run(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], [0, t1 - t0],
-                         init, w.snap_interval)
+                         init, snap)
         o = out[t0:t1].float().cpu().numpy()
         e_out.add(o, res.out)
-        for h in range(w.H):
+        for h in range(H):
             worst = max(worst, oracle.rel_l2(o[:, h], res.out[:, h]))
         e_state.add(pool[dst].cpu(), res.final[0])
         worst = max(worst, worst_state(pool[dst:dst + 1], res.final))
-        n = (t1 - t0) // w.snap_interval
-        sn = snaps[off[s]:off[s] + n]
-        e_snap.add(sn.cpu(), res.snaps)
+        n = (t1 - t0) // snap if snap else 0
         if n:
+            sn = snaps[off[s]:off[s] + n]
+            e_snap.add(sn.cpu(), res.snaps)
             worst = max(worst, worst_state(sn, res.snaps))
-    print(f"varlen_resume: out {e_out.value:.2e} snaps {e_snap.value:.2e} "
-          f"states {e_state.value:.2e} worst unit {worst:.2e}")
-    assert e_out.value <= tol and e_snap.value <= tol and e_state.value <= tol
-    assert worst <= 2 * tol
+    assert e_out.value <= tol and e_state.value <= tol, (e_out.value, e_state.value)
+    assert e_snap.value <= tol, e_snap.value
+    assert worst <= 2 * tol, worst
+    return e_out.value, e_snap.value, e_state.value, worst
+
+
+def test_varlen_resume_full():
+    """16 sequences, L ~ U[512, 32768], 8 resumed from a 1024-slot pool, snapshots
+    every 256, all 32 heads: every output, every snapshot and every touched final
+    state against the oracle (per sequence; see _check_by_sequence); sources of
+    resumed sequences and untouched slots bit-identical."""
+    w = inputs.WORKLOADS["varlen_resume"]
+    b = inputs.make_batch(w)
+    before = b.pool.clone()
+    out, pool, snaps, (st, bits) = gpu_prefill(b, w.snap_interval)
+    assert st == kda.KDA_OK and bits == 0
+    e = _check_by_sequence(b, w.snap_interval, out, pool, snaps)
+    print("varlen_resume: out %.2e snaps %.2e states %.2e worst unit %.2e" % e)
     assert_untouched(pool, before, touched_slots(b))
     for s in range(w.B):
         src = int(b.init_slots[s, 0])
         if src >= 0:
             assert torch.equal(pool[src].cpu(), before[src])
+
+
+def test_prefill_3x32k_full():
+    """Three 32768-token sequences at H = 32: 96 (sequence, head) pairs, more
+    than the cooperative mode serves and fewer than the SMs, so the per-state
+    kernel runs one 128-column CTA per pair.  Every output, snapshot and final
+    state against the oracle (per sequence; see _check_by_sequence)."""
+    w = inputs.WORKLOADS["prefill_3x32k"]
+    b = inputs.make_batch(w)
+    out, pool, snaps, (st, bits) = gpu_prefill(b, w.snap_interval)
+    assert st == kda.KDA_OK and bits == 0
+    e = _check_by_sequence(b, w.snap_interval, out, pool, snaps)
+    print("prefill_3x32k: out %.2e snaps %.2e states %.2e worst unit %.2e" % e)
 
 
 @pytest.mark.slow
