@@ -39,6 +39,12 @@ What is computed, and where it is stated:
   is the speculative verify that commits the previous step's accepted tokens
   before evaluating the new ones.
 
+* ``short_conv``, ``l2_normalize`` and ``rms_norm_gated`` are the layer
+  around the recurrence that the pages' fused decode kernel folds into its
+  launch (the short causal convolution with its state, the output RMSNorm
+  and sigmoid gate); ``prefill_fused_pool`` / ``decode_fused_pool`` compose
+  them with the pool semantics above.
+
 * ``split_recurrence`` is the algebra of a sequence-split prefill (segments
   from the zero state plus identity runs with v = 0, start states chained,
   outputs corrected); the GPU library does not implement it yet, and it is
@@ -426,6 +432,136 @@ def split_recurrence(q, k, v, g, beta, S0, splits):
         o[sl] = o_loc + o_hom @ X          # row t: L_t^T q_t + X^T Phi_t^T q_t
         X = Phi @ X + L_end
     return o, X
+
+
+# ----------------------------------------------------------------------------
+# the fused layer around the recurrence: short causal convolution before it,
+# gated RMSNorm after it
+# ----------------------------------------------------------------------------
+#
+# "Kimi K3 + vLLM: Inside the Day-0 Production Integration": KDA keeps "a
+# short causal convolution state" beside its matrix state ("Kimi Delta
+# Attention: When Prefix Caching Meets Recurrent State"), both updated at
+# every token, and its fused decode kernel "folds causal convolution,
+# recurrent state update, gating, and RMSNorm into a single launch"
+# ("Separate Prefill/Decode Code Paths"); the vLLM recipe page for Kimi-K3
+# fuses "the KDA output RMSNorm and sigmoid gate" into one kernel.  The pages
+# fix none of the sizes; the readings taken here (conv width 4, depthwise over
+# the raw q, k and v channels, no activation unless asked for SiLU, q and k
+# L2-normalised after the conv with q scaled by 1/sqrt(dk), RMSNorm epsilon
+# 1e-6 with one weight per value column, the gate through a sigmoid after the
+# norm) are the plainest ones consistent with the rest of the path.
+
+CONV_WIDTH = 4
+RMS_EPS = 1e-6
+
+
+def short_conv(x, w, x_prev=None, act="none"):
+    """Causal depthwise convolution of ONE sequence over time.
+
+    x: [L, C] raw inputs; w: [C, W] taps (w[c, W-1] multiplies the current
+    token, w[c, i] the token W-1-i steps back); x_prev: [W-1, C] the W-1 raw
+    inputs before x in time order (the convolution state; zeros when None).
+    y[t, c] = act(sum_i w[c, i] * xx[t + i, c]) with xx = [x_prev; x].
+    Returns (y [L, C], new state = the last W-1 rows of xx)."""
+    x, w = _f64(x), _f64(w)
+    L, C = x.shape
+    W = w.shape[1]
+    prev = np.zeros((W - 1, C)) if x_prev is None else _f64(x_prev).reshape(W - 1, C)
+    xx = np.concatenate([prev, x], axis=0)
+    y = np.zeros((L, C))
+    for i in range(W):
+        y += w[:, i][None, :] * xx[i:i + L]
+    if act == "silu":
+        y = y / (1.0 + np.exp(-y))
+    elif act != "none":
+        raise ValueError(act)
+    return y, xx[L:].copy()
+
+
+def l2_normalize(x):
+    """Each row divided by its L2 norm (rows of zeros stay zero)."""
+    x = _f64(x)
+    n = np.linalg.norm(x, axis=-1, keepdims=True)
+    return x / np.where(n > 0, n, 1.0)
+
+
+def rms_norm_gated(o, w, gate, eps=RMS_EPS):
+    """y = o / sqrt(mean(o^2) + eps) * w * sigmoid(gate), over the last axis."""
+    o, w, gate = _f64(o), _f64(w), _f64(gate)
+    r = 1.0 / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
+    return o * r * w * (1.0 / (1.0 + np.exp(-gate)))
+
+
+def fused_inputs(xq, xk, xv, conv_w, conv_state=None, act="none"):
+    """The recurrence's q, k, v for ONE (sequence, head) from its raw inputs:
+    the short conv over the 2 dk + dv channels [q | k | v] (conv_w [2dk+dv, W],
+    conv_state [2dk+dv, W-1] channel-major or None), then q and k
+    L2-normalised, q scaled by 1/sqrt(dk).  Returns (q, k, v, new conv state
+    [2dk+dv, W-1])."""
+    xq, xk, xv = _f64(xq), _f64(xk), _f64(xv)
+    dk = xq.shape[1]
+    x = np.concatenate([xq, xk, xv], axis=1)
+    prev = None if conv_state is None else _f64(conv_state).T
+    y, st = short_conv(x, conv_w, prev, act)
+    q = l2_normalize(y[:, :dk]) / np.sqrt(dk)
+    k = l2_normalize(y[:, dk:2 * dk])
+    return q, k, y[:, 2 * dk:], st.T.copy()
+
+
+def prefill_fused_pool(xq, xk, xv, g, beta, gate, conv_w, norm_w, cu_seqlens, init_slots,
+                       state_pool, conv_pool, snap_interval=0, act="none", **kw):
+    """What ``kda_prefill_varlen_fused`` must produce: per sequence b and head h,
+    the conv starts from conv_pool[src_b, h] (zeros when src_b < 0), its new
+    state goes to conv_pool[dst_b, h]; the conv outputs feed ``prefill_pool``
+    (matrix states, snapshots, copy-on-write exactly as there); the outputs
+    pass through ``rms_norm_gated``.  xq, xk, g: [T, H, dk]; xv, gate:
+    [T, H, dv]; conv_w: [H, 2dk+dv, W]; norm_w: [dv]; conv_pool:
+    [n_slots, H, 2dk+dv, W-1].  Returns (out, pool_after, conv_after, snaps)."""
+    xq, xk, xv = _f64(xq), _f64(xk), _f64(xv)
+    cw, cpool = _f64(conv_w), _f64(conv_pool)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    slots = np.asarray(init_slots, dtype=np.int64).reshape(-1, 2)
+    T, H, dk = xq.shape
+    dv = xv.shape[2]
+    q, k, v = np.zeros((T, H, dk)), np.zeros((T, H, dk)), np.zeros((T, H, dv))
+    conv_after = cpool.copy()
+    for b in range(len(cu) - 1):
+        t0, t1 = int(cu[b]), int(cu[b + 1])
+        src, dst = int(slots[b, 0]), int(slots[b, 1])
+        for h in range(H):
+            st0 = cpool[src, h] if src >= 0 else None
+            qb, kb, vb, st = fused_inputs(xq[t0:t1, h], xk[t0:t1, h], xv[t0:t1, h], cw[h], st0,
+                                          act)
+            q[t0:t1, h], k[t0:t1, h], v[t0:t1, h] = qb, kb, vb
+            conv_after[dst, h] = st
+    o, after, snaps = prefill_pool(q, k, v, g, beta, cu, slots, state_pool, snap_interval, **kw)
+    return rms_norm_gated(o, norm_w, gate), after, conv_after, snaps
+
+
+def decode_fused_pool(xq, xk, xv, g, beta, gate, conv_w, norm_w, slot_ids, state_pool,
+                      conv_pool, n_tok=1, act="none", **kw):
+    """What ``kda_decode_fused`` must produce: sequence n owns rows
+    [n n_tok, (n+1) n_tok) and slot slot_ids[n] of both pools; its conv runs
+    from conv_pool[slot] and the slot's conv state advances in place like the
+    matrix state.  Returns (out, pool_after, conv_after)."""
+    xq, xk, xv = _f64(xq), _f64(xk), _f64(xv)
+    cw, cpool = _f64(conv_w), _f64(conv_pool)
+    slots = np.asarray(slot_ids, dtype=np.int64).reshape(-1)
+    N = len(slots)
+    T, H, dk = xq.shape
+    dv = xv.shape[2]
+    q, k, v = np.zeros((T, H, dk)), np.zeros((T, H, dk)), np.zeros((T, H, dv))
+    conv_after = cpool.copy()
+    for n in range(N):
+        r0, r1 = n * n_tok, (n + 1) * n_tok
+        for h in range(H):
+            qb, kb, vb, st = fused_inputs(xq[r0:r1, h], xk[r0:r1, h], xv[r0:r1, h], cw[h],
+                                          cpool[slots[n], h], act)
+            q[r0:r1, h], k[r0:r1, h], v[r0:r1, h] = qb, kb, vb
+            conv_after[slots[n], h] = st
+    o, after, _ = decode_pool(q, k, v, g, beta, slots, state_pool, n_tok, False, **kw)
+    return rms_norm_gated(o, norm_w, gate), after, conv_after
 
 
 def rel_l2(x, ref) -> float:
