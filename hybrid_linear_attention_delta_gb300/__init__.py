@@ -23,6 +23,7 @@ KDA_ALGO_AUTO, KDA_ALGO_RECURRENT, KDA_ALGO_CHUNKED, KDA_ALGO_CHUNKED_PER_STATE,
     KDA_ALGO_CHUNKED_COOP = range(5)
 
 EXPORTS = ("kda_prefill_varlen", "kda_prefill_varlen_retain", "kda_decode", "kda_decode_spec",
+           "kda_prefill_varlen_fused", "kda_decode_fused", "kda_fused_scratch_bytes",
            "kda_workspace_bytes",
            "kda_snapshot_count", "kda_device_status", "kda_status_string",
            "kda_last_launch_count")
@@ -36,6 +37,17 @@ class KdaArgs(ctypes.Structure):
                 ("snaps_capacity", ctypes.c_int64), ("stream", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("ev_begin", ctypes.c_void_p), ("ev_end", ctypes.c_void_p)]
+
+
+class KdaFusedArgs(ctypes.Structure):
+    """Mirror of ``kda_fused_args`` in include/kda.h."""
+    _fields_ = [("gate", ctypes.c_void_p), ("conv_w", ctypes.c_void_p),
+                ("norm_w", ctypes.c_void_p), ("conv_pool", ctypes.c_void_p),
+                ("conv_width", ctypes.c_int32), ("conv_act", ctypes.c_int32),
+                ("norm_eps", ctypes.c_float), ("reserved", ctypes.c_int32)]
+
+
+CONV_ACT = {"none": 0, "silu": 1}
 
 
 class KdaError(RuntimeError):
@@ -78,6 +90,14 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
         L.kda_decode_noalloc.restype = ctypes.c_int
         L.kda_decode_spec.argtypes = [V, V, V, V, V, V, V, V, I32, V, V, V, V, V, I32, A]
         L.kda_decode_spec.restype = ctypes.c_int
+        F = ctypes.POINTER(KdaFusedArgs)
+        L.kda_prefill_varlen_fused.argtypes = [V, V, V, V, V, V, V, V, V, I32, V, F, V,
+                                               ctypes.c_size_t, A]
+        L.kda_prefill_varlen_fused.restype = ctypes.c_int
+        L.kda_decode_fused.argtypes = [V, V, V, V, V, V, V, V, I32, V, F, A]
+        L.kda_decode_fused.restype = ctypes.c_int
+        L.kda_fused_scratch_bytes.argtypes = [A]
+        L.kda_fused_scratch_bytes.restype = ctypes.c_size_t
         if path:
             return L
         _lib = L
@@ -243,6 +263,69 @@ def kda_decode_noalloc(q, k, v, g, beta, slot_ids, state_pool, out, n_tok: int =
     if st != KDA_OK:
         raise KdaError(st, "kda_decode_noalloc")
     return err_bits
+
+
+def _fused_args(gate, conv_w, norm_w, conv_pool, conv_act="none", norm_eps=1e-6):
+    for t in (conv_w, norm_w):
+        if t is not None and t.dtype.is_floating_point and t.element_size() != 4:
+            raise TypeError("conv_w and norm_w are fp32")
+    return KdaFusedArgs(gate=_ptr(gate), conv_w=_ptr(conv_w), norm_w=_ptr(norm_w),
+                        conv_pool=_ptr(conv_pool), conv_width=conv_w.shape[-1],
+                        conv_act=CONV_ACT[conv_act], norm_eps=float(norm_eps), reserved=0)
+
+
+def kda_fused_scratch_bytes(T_total: int, H: int, dk: int, dv: int, dtype: int) -> int:
+    a = KdaArgs(T_total=T_total, H=H, dk=dk, dv=dv, dtype=dtype)
+    return int(lib().kda_fused_scratch_bytes(ctypes.byref(a)))
+
+
+def kda_prefill_varlen_fused(xq, xk, xv, g, beta, gate, conv_w, norm_w, cu_seqlens, init_slots,
+                             state_pool, conv_pool, out, snap_interval: int = 0, snaps=None, *,
+                             workspace, scratch=None, conv_act="none", norm_eps=1e-6,
+                             stream=None, algo: int = KDA_ALGO_AUTO, events=None):
+    """The prefill with the short convolution before it and the gated RMSNorm
+    after it (see kda_prefill_varlen_fused in include/kda.h).  xq, xk, xv are
+    the raw inputs; conv_w [H, 2dk+dv, 4] and norm_w [dv] fp32; conv_pool
+    [n_slots, H, 2dk+dv, 3] in the input dtype.  scratch: a uint8 CUDA tensor
+    of kda_fused_scratch_bytes(...) bytes (made here when not given).
+    Returns the scratch tensor."""
+    import torch
+    dt = _dtype_code(xq)
+    T, H, dk = xq.shape
+    dv = xv.shape[2]
+    if scratch is None:
+        n = kda_fused_scratch_bytes(T, H, dk, dv, dt)
+        scratch = torch.empty(max(n, 16), dtype=torch.uint8, device=xq.device)
+    a = make_args(B=cu_seqlens.numel() - 1, T_total=T, H=H, dk=dk, dv=dv,
+                  n_slots=state_pool.shape[0], dtype=dt, algo=algo,
+                  snaps_capacity=0 if snaps is None else snaps.shape[0], stream=stream,
+                  workspace=workspace, events=events)
+    f = _fused_args(gate, conv_w, norm_w, conv_pool, conv_act, norm_eps)
+    st = lib().kda_prefill_varlen_fused(_ptr(xq), _ptr(xk), _ptr(xv), _ptr(g), _ptr(beta),
+                                        _ptr(cu_seqlens), _ptr(init_slots), _ptr(state_pool),
+                                        _ptr(out), int(snap_interval), _ptr(snaps),
+                                        ctypes.byref(f), _ptr(scratch),
+                                        scratch.numel() * scratch.element_size(),
+                                        ctypes.byref(a))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prefill_varlen_fused")
+    return scratch
+
+
+def kda_decode_fused(xq, xk, xv, g, beta, gate, conv_w, norm_w, slot_ids, state_pool, conv_pool,
+                     out, n_tok: int = 1, per_tok_states=None, *, workspace, conv_act="none",
+                     norm_eps=1e-6, stream=None, events=None) -> None:
+    """Decode with the short convolution and the gated RMSNorm in one launch
+    (see kda_decode_fused in include/kda.h); dk = dv = 128."""
+    a = make_args(B=slot_ids.numel(), T_total=xq.shape[0], H=xq.shape[1], dk=xq.shape[2],
+                  dv=xv.shape[2], n_slots=state_pool.shape[0], dtype=_dtype_code(xq),
+                  stream=stream, workspace=workspace, events=events)
+    f = _fused_args(gate, conv_w, norm_w, conv_pool, conv_act, norm_eps)
+    st = lib().kda_decode_fused(_ptr(xq), _ptr(xk), _ptr(xv), _ptr(g), _ptr(beta), _ptr(slot_ids),
+                                _ptr(state_pool), _ptr(out), int(n_tok), _ptr(per_tok_states),
+                                ctypes.byref(f), ctypes.byref(a))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_fused")
 
 
 def kda_device_status(workspace, stream=None):

@@ -111,13 +111,51 @@ int64_t kda_snapshot_count(const int32_t *cu, int32_t B, int32_t snap_interval) 
 
 namespace {
 
-// Both prefill entry points: snapshots go to the dense buffer snaps, or, with
+// The fused layer's arguments: host checks and the device-side view.
+kda_status check_fused(const kda_fused_args *f, const kda_args *a, const void *xq, const void *xk,
+                       const void *xv, kda::FusedParams *fp) {
+  if (!f || !f->conv_w || !f->norm_w || !f->conv_pool) return KDA_ERR_INVALID_ARG;
+  if (f->conv_width != kda::kConvW) return KDA_ERR_UNSUPPORTED;
+  if (f->conv_act != 0 && f->conv_act != 1) return KDA_ERR_INVALID_ARG;
+  if (!(f->norm_eps >= 0.f)) return KDA_ERR_INVALID_ARG;
+  if (2 * a->dk + a->dv > 384) return KDA_ERR_UNSUPPORTED;
+  if (a->T_total > 0) {
+    const void *ps[] = {xq, xk, xv, f->gate};
+    for (const void *p : ps)
+      if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  }
+  fp->xq = xq; fp->xk = xk; fp->xv = xv; fp->gate = f->gate;
+  fp->conv_w = f->conv_w; fp->norm_w = f->norm_w; fp->conv_pool = f->conv_pool;
+  fp->act = f->conv_act; fp->eps = f->norm_eps;
+  return KDA_OK;
+}
+
+size_t elem_size(int32_t dtype) { return dtype == KDA_BF16 ? 2 : 4; }
+
+// Scratch of the fused prefill: q, k, v (convolved) and o, each 256-byte aligned.
+struct FusedScratch {
+  size_t q, k, v, o, total;
+  FusedScratch(const kda_args *a) {
+    const size_t es = elem_size(a->dtype), T = (size_t)(a->T_total > 0 ? a->T_total : 0);
+    const size_t nk = T * a->H * a->dk * es, nv = T * a->H * a->dv * es;
+    q = 0;
+    k = kda::align256(nk);
+    v = k + kda::align256(nk);
+    o = v + kda::align256(nv);
+    total = o + kda::align256(nv);
+  }
+};
+
+// Every prefill entry point: snapshots go to the dense buffer snaps, or, with
 // a retention map snap_slots, into the pool slots it names (exactly one of the
-// two is non-NULL when the call takes snapshots).
+// two is non-NULL when the call takes snapshots).  With fused (not NULL), q,
+// k, v are the raw inputs, which the convolution turns into scratch; the
+// recurrence writes its outputs into scratch and the gated RMSNorm into out.
 kda_status prefill(const void *q, const void *k, const void *v, const void *g, const void *beta,
                    const int32_t *cu_seqlens, const int32_t *init_slots, float *state_pool,
                    void *out, int32_t snap_interval, float *snaps, const int32_t *snap_slots,
-                   const kda_args *a) {
+                   const kda_args *a, const kda_fused_args *fused = nullptr,
+                   void *scratch = nullptr, size_t scratch_bytes = 0) {
   g_last_launches = 0;
   kda_status st = check_common(a);
   if (st != KDA_OK) return st;
@@ -134,6 +172,19 @@ kda_status prefill(const void *q, const void *k, const void *v, const void *g, c
   if (!cu_seqlens || !init_slots || !state_pool || !aligned16(state_pool))
     return KDA_ERR_INVALID_ARG;
   if ((st = check_tokens(q, k, v, g, beta, out, a->T_total)) != KDA_OK) return st;
+  kda::FusedParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  void *o_final = out;
+  if (fused) {
+    if ((st = check_fused(fused, a, q, k, v, &fp)) != KDA_OK) return st;
+    const FusedScratch sc(a);
+    if (!scratch || !aligned16(scratch) || scratch_bytes < sc.total) return KDA_ERR_INVALID_ARG;
+    char *b = static_cast<char *>(scratch);
+    q = b + sc.q;
+    k = b + sc.k;
+    v = b + sc.v;
+    out = b + sc.o;
+  }
 
   const kda::WorkspaceLayout lay(a->B, a->H, a->n_slots);
   char *ws = static_cast<char *>(a->workspace);
@@ -171,17 +222,26 @@ kda_status prefill(const void *q, const void *k, const void *v, const void *g, c
 
   if ((st = from_cuda(kda::launch_meta(p))) != KDA_OK) return st;
   g_last_launches = 1;
+  if (fused) {  // the convolution, then the new convolution states
+    if ((st = from_cuda(kda::launch_conv_prefill(p, fp))) != KDA_OK) return st;
+    if ((st = from_cuda(kda::launch_conv_state(p, fp))) != KDA_OK) return st;
+    g_last_launches += 2;
+  }
   record(a->ev_begin, p.stream);
   st = from_cuda(chunked ? kda::launch_chunked_prefill(p, mode) : kda::launch_recurrent_prefill(p));
   record(a->ev_end, p.stream);
   if (st != KDA_OK) return st;
-  g_last_launches = 2;
+  ++g_last_launches;
   if (chunked) {
     // units whose decay left the chunked algorithm's exponent range are
     // recomputed by the exact token-recurrent kernel (every other CTA of this
     // launch returns at once)
     if ((st = from_cuda(kda::launch_recurrent_prefill(p, true))) != KDA_OK) return st;
-    g_last_launches = 3;
+    ++g_last_launches;
+  }
+  if (fused) {  // the gated RMSNorm of the recurrence's outputs
+    if ((st = from_cuda(kda::launch_rms_gate(p, fp, out, o_final))) != KDA_OK) return st;
+    ++g_last_launches;
   }
   return st;
 }
@@ -205,6 +265,59 @@ kda_status kda_prefill_varlen_retain(const void *q, const void *k, const void *v
                                      const kda_args *a) {
   return prefill(q, k, v, g, beta, cu_seqlens, init_slots, state_pool, out, snap_interval,
                  nullptr, snap_slots, a);
+}
+
+kda_status kda_prefill_varlen_fused(const void *xq, const void *xk, const void *xv,
+                                    const void *g, const void *beta, const int32_t *cu_seqlens,
+                                    const int32_t *init_slots, float *state_pool, void *out,
+                                    int32_t snap_interval, float *snaps, const kda_fused_args *f,
+                                    void *scratch, size_t scratch_bytes, const kda_args *a) {
+  if (!f) {
+    g_last_launches = 0;
+    return KDA_ERR_INVALID_ARG;
+  }
+  return prefill(xq, xk, xv, g, beta, cu_seqlens, init_slots, state_pool, out, snap_interval,
+                 snaps, nullptr, a, f, scratch, scratch_bytes);
+}
+
+size_t kda_fused_scratch_bytes(const kda_args *a) {
+  if (!a || a->T_total < 0 || a->H <= 0 || a->dk <= 0 || a->dv <= 0) return 0;
+  return FusedScratch(a).total;
+}
+
+kda_status kda_decode_fused(const void *xq, const void *xk, const void *xv, const void *g,
+                            const void *beta, const int32_t *slot_ids, float *state_pool,
+                            void *out, int32_t n_tok, float *per_tok_states,
+                            const kda_fused_args *f, const kda_args *a) {
+  g_last_launches = 0;
+  kda_status st = check_common(a);
+  if (st != KDA_OK) return st;
+  if (a->dk != 128 || a->dv != 128) return KDA_ERR_UNSUPPORTED;
+  if (n_tok < 1 || (int64_t)a->B * n_tok != a->T_total) return KDA_ERR_INVALID_ARG;
+  if (a->B == 0) return KDA_OK;
+  if (!slot_ids || !state_pool || !aligned16(state_pool)) return KDA_ERR_INVALID_ARG;
+  if (per_tok_states && !aligned16(per_tok_states)) return KDA_ERR_INVALID_ARG;
+  if ((st = check_tokens(xq, xk, xv, g, beta, out, a->T_total)) != KDA_OK) return st;
+  kda::FusedParams fp;
+  if ((st = check_fused(f, a, xq, xk, xv, &fp)) != KDA_OK) return st;
+
+  const kda::WorkspaceLayout lay(a->B, a->H, a->n_slots);
+  char *ws = static_cast<char *>(a->workspace);
+  kda::DecodePlan p;
+  std::memset(&p, 0, sizeof(p));
+  p.g = g; p.beta = beta;
+  p.slot_ids = slot_ids; p.pool = state_pool; p.out = out; p.per_tok = per_tok_states;
+  p.N = a->B; p.n_tok = n_tok; p.H = a->H; p.dk = a->dk; p.dv = a->dv;
+  p.n_slots = a->n_slots; p.dtype = a->dtype;
+  p.err = reinterpret_cast<uint32_t *>(ws);
+  p.claims = reinterpret_cast<uint32_t *>(ws + lay.claims_off);
+  if ((st = from_cuda(next_epoch(a, &p.epoch))) != KDA_OK) return st;
+  p.stream = static_cast<cudaStream_t>(a->stream);
+  record(a->ev_begin, p.stream);
+  st = from_cuda(kda::launch_decode_fused(p, fp));
+  record(a->ev_end, p.stream);
+  if (st == KDA_OK) g_last_launches = 1;
+  return st;
 }
 
 kda_status kda_decode(const void *q, const void *k, const void *v, const void *g,

@@ -166,7 +166,30 @@ struct DecodePlan {
   const int32_t *accepted;
 };
 
+// The layer around the recurrence (kda_prefill_varlen_fused / kda_decode_fused):
+// the short causal convolution of the raw q, k, v channels with its state in
+// a slot-indexed pool, and the gated RMSNorm of the outputs.
+struct FusedParams {
+  const void *xq, *xk, *xv;  // raw inputs [T][H][dk], [T][H][dk], [T][H][dv]
+  const void *gate;          // [T][H][dv] output gate logits
+  const float *conv_w;       // [H][2 dk + dv][kConvW] taps, channel order q | k | v
+  const float *norm_w;       // [dv]
+  void *conv_pool;           // [n_slots][H][2 dk + dv][kConvW - 1], oldest first
+  int32_t act;               // 0: none, 1: SiLU
+  float eps;
+};
+constexpr int kConvW = 4;
+
 cudaError_t launch_meta(const PrefillPlan &p);
+// prefill side, in stream order: the convolution of p's batch into q, k, v
+// (p.q, p.k, p.v point at the caller's scratch), then the new convolution
+// states (after it, so that src == dst is safe), and, after the prefill, the
+// gated RMSNorm of o (scratch) into out
+cudaError_t launch_conv_prefill(const PrefillPlan &p, const FusedParams &f);
+cudaError_t launch_conv_state(const PrefillPlan &p, const FusedParams &f);
+cudaError_t launch_rms_gate(const PrefillPlan &p, const FusedParams &f, const void *o, void *out);
+// decode: one launch per call, dk = dv = 128 (p.q/k/v unused: f.xq/xk/xv)
+cudaError_t launch_decode_fused(const DecodePlan &p, const FusedParams &f);
 // rerun_only: recompute only the units that the chunked kernel flagged in
 // p.rerun with the call's epoch (every other CTA returns at once)
 cudaError_t launch_recurrent_prefill(const PrefillPlan &p, bool rerun_only = false);

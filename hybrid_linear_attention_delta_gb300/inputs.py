@@ -21,6 +21,12 @@ Recipe (the same for every workload; sizes come from ``WORKLOADS``):
   ``(20260000 + workload_index) * 100 + field_id`` so fields do not depend on
   the order they are drawn in (a varlen batch needs its lengths before the
   token tensors).
+* The layer around the recurrence (short convolution, gated RMSNorm;
+  ``fused_tensors``): the raw inputs are q, k, v drawn as above (the
+  convolution mixes them, and q and k are normalised again after it), the
+  gate logits ~ N(0, 1) per (token, head, value column), the convolution taps
+  ~ N(0, 0.5^2) per (head, channel, tap), the RMSNorm weight 1 + N(0, 0.1^2)
+  per value column, and the slots' convolution states ~ N(0, 1) raw inputs.
 * Large tensors are drawn in token blocks on ``device`` (the CPU by default;
   the benchmark and the full-size tests draw on the GPU for speed).
 """
@@ -34,6 +40,7 @@ from typing import List, Optional
 import torch
 
 F_Q, F_K, F_V, F_G, F_BETA, F_LENS, F_SLOTS, F_POOL, F_RESUME, F_ACCEPT = range(10)
+F_GATE, F_CONVW, F_NORMW, F_CONVPOOL = range(10, 14)
 
 
 @dataclass(frozen=True)
@@ -205,3 +212,23 @@ def make_batch(w: Workload, device="cpu", lengths: Optional[List[int]] = None,
         agen = _gen(w.index, F_ACCEPT, "cpu")
         extra["accepted"] = torch.randint(1, w.n_tok + 1, (N,), generator=agen).to(torch.int32)
     return Batch(cu_seqlens=cu, slot_ids=slot_ids, pool=pool, extra=extra, **tt)
+
+
+def fused_tensors(T: int, H: int, dk: int, dv: int, dtype: torch.dtype, index: int,
+                  n_slots: int, device="cpu", conv_width: int = 4):
+    """gate [T, H, dv] (dtype), conv_w [H, 2dk+dv, W] fp32, norm_w [dv] fp32,
+    conv_pool [n_slots, H, 2dk+dv, W-1] (dtype), per the recipe above."""
+    dev = torch.device(device)
+    C = 2 * dk + dv
+    gate = torch.empty((T, H, dv), dtype=dtype, device=dev)
+    gen = _gen(index, F_GATE, dev)
+    block = 1 << 15
+    for t0 in range(0, T, block):
+        t1 = min(T, t0 + block)
+        gate[t0:t1] = torch.randn((t1 - t0, H, dv), generator=gen, device=dev).to(dtype)
+    conv_w = torch.randn((H, C, conv_width), generator=_gen(index, F_CONVW, dev),
+                         device=dev) * 0.5
+    norm_w = 1.0 + 0.1 * torch.randn((dv,), generator=_gen(index, F_NORMW, dev), device=dev)
+    conv_pool = torch.randn((n_slots, H, C, conv_width - 1),
+                            generator=_gen(index, F_CONVPOOL, dev), device=dev).to(dtype)
+    return {"gate": gate, "conv_w": conv_w, "norm_w": norm_w, "conv_pool": conv_pool}

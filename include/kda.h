@@ -282,6 +282,79 @@ kda_status kda_decode_noalloc(const void *q, const void *k, const void *v, const
                               void *out, int32_t n_tok, float *per_tok_states, uint32_t *err_bits,
                               const kda_args *a);
 
+/*
+ * The layer around the recurrence: short causal convolution in, gated RMSNorm
+ * out ("Kimi K3 + vLLM: Inside the Day-0 Production Integration": a KDA layer
+ * keeps "a short causal convolution state" beside its matrix state, section
+ * "Kimi Delta Attention: When Prefix Caching Meets Recurrent State", and its
+ * fused decode kernel folds the causal convolution, the recurrent state
+ * update, the gating and the RMSNorm into one launch, section "Separate
+ * Prefill/Decode Code Paths"; the vLLM recipe page for Kimi-K3 fuses the KDA
+ * output RMSNorm and its sigmoid gate).  Per (sequence, head), token t:
+ *
+ *     y~_t[c] = act(sum_i conv_w[h][c][i] * x[t - (W-1) + i][c])   c over [q | k | v]
+ *     q_t = y~_q / |y~_q| / sqrt(dk),  k_t = y~_k / |y~_k|,  v_t = y~_v
+ *     (the recurrence of kda_prefill_varlen / kda_decode on q, k, v, g, beta)
+ *     out_t = o_t / sqrt(mean(o_t^2) + norm_eps) * norm_w * sigmoid(gate_t)
+ *
+ * where x are the raw (pre-convolution) inputs, W = conv_width taps, and the
+ * W-1 inputs before a segment come from the slot's convolution state (zeros
+ * for a sequence without a source slot).
+ */
+typedef struct {
+  const void *gate;     /* [T][H][dv] a->dtype: output gate logits */
+  const float *conv_w;  /* [H][2 dk + dv][conv_width] fp32: taps per channel, channels in
+                           the order q (dk), k (dk), v (dv); tap conv_width-1 multiplies
+                           the current token, tap i the token conv_width-1-i steps back */
+  const float *norm_w;  /* [dv] fp32: RMSNorm weight, shared by the heads */
+  void *conv_pool;      /* [n_slots][H][2 dk + dv][conv_width - 1] a->dtype: per channel
+                           its last conv_width-1 raw inputs, oldest first (channel-major,
+                           the "DS" layout); indexed by the same slots as state_pool */
+  int32_t conv_width;   /* 4 (the only width supported) */
+  int32_t conv_act;     /* 0: no activation after the convolution, 1: SiLU */
+  float norm_eps;       /* RMSNorm epsilon, >= 0 */
+  int32_t reserved;     /* 0 */
+} kda_fused_args;
+
+/* Scratch bytes kda_prefill_varlen_fused needs for these sizes (uses T_total,
+ * H, dk, dv, dtype): the convolved q, k, v and the recurrence's outputs. */
+size_t kda_fused_scratch_bytes(const kda_args *a);
+
+/*
+ * kda_prefill_varlen with the layer around it.  xq, xk [T][H][dk] and xv
+ * [T][H][dv] are the raw inputs; the convolution of sequence b starts from
+ * conv_pool[src_b] (zeros when src_b = -1) and its new state (the last
+ * conv_width-1 raw inputs of [old state; segment]) goes to conv_pool[dst_b],
+ * copy-on-write exactly like state_pool.  out [T][H][dv] receives the gated
+ * RMSNorm of the recurrence's outputs; snapshots and final states are those
+ * of the recurrence on the convolved q, k, v (the convolution state at a
+ * snapshot is the W-1 raw inputs before that position, which the caller
+ * holds).  scratch: device memory of at least kda_fused_scratch_bytes(a)
+ * bytes, 16-byte aligned, caller-owned, not shared by concurrent calls.
+ * Six kernels in stream order: plan, convolution, convolution states,
+ * prefill, exact recomputation (as in kda_prefill_varlen), gated RMSNorm.
+ * Same shapes and errors as kda_prefill_varlen.
+ */
+kda_status kda_prefill_varlen_fused(const void *xq, const void *xk, const void *xv,
+                                    const void *g, const void *beta, const int32_t *cu_seqlens,
+                                    const int32_t *init_slots, float *state_pool, void *out,
+                                    int32_t snap_interval, float *snaps, const kda_fused_args *f,
+                                    void *scratch, size_t scratch_bytes, const kda_args *a);
+
+/*
+ * kda_decode with the layer around it, in ONE kernel launch (dk = dv = 128):
+ * per token the convolution from the slot's convolution state, the
+ * normalisation of q and k, the recurrence step in place on the slot and the
+ * gated RMSNorm of the output; the slot's convolution state advances with
+ * its matrix state.  per_tok_states as in kda_decode (the convolution state
+ * after token j is the last conv_width-1 raw inputs up to j, which the caller
+ * holds).  Arguments otherwise as kda_decode, raw inputs in place of q, k, v.
+ */
+kda_status kda_decode_fused(const void *xq, const void *xk, const void *xv, const void *g,
+                            const void *beta, const int32_t *slot_ids, float *state_pool,
+                            void *out, int32_t n_tok, float *per_tok_states,
+                            const kda_fused_args *f, const kda_args *a);
+
 /* Workspace bytes the calls need for these sizes (uses B, H, n_slots).
  * The snapshot interval does not change the size: snapshot offsets live in
  * the per-sequence plan, whose size depends on B only.

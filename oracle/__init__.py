@@ -479,6 +479,19 @@ def short_conv(x, w, x_prev=None, act="none"):
     return y, xx[L:].copy()
 
 
+def round_to(x, dtype):
+    """Round-to-nearest-even of fp64 values to the significand of `dtype`
+    ('bf16': 8 significant bits, 'f32': 24), kept in fp64; None leaves x as it
+    is.  (The normal range only: the values here are far from over- and
+    underflow.)"""
+    x = _f64(x)
+    if dtype is None:
+        return x
+    bits = {"bf16": 8, "f32": 24}[dtype]
+    m, e = np.frexp(x)                      # x = m 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(np.ldexp(m, bits)), e - bits)   # rint: ties to even
+
+
 def l2_normalize(x):
     """Each row divided by its L2 norm (rows of zeros stay zero)."""
     x = _f64(x)
@@ -493,24 +506,27 @@ def rms_norm_gated(o, w, gate, eps=RMS_EPS):
     return o * r * w * (1.0 / (1.0 + np.exp(-gate)))
 
 
-def fused_inputs(xq, xk, xv, conv_w, conv_state=None, act="none"):
+def fused_inputs(xq, xk, xv, conv_w, conv_state=None, act="none", operand_dtype=None):
     """The recurrence's q, k, v for ONE (sequence, head) from its raw inputs:
     the short conv over the 2 dk + dv channels [q | k | v] (conv_w [2dk+dv, W],
     conv_state [2dk+dv, W-1] channel-major or None), then q and k
-    L2-normalised, q scaled by 1/sqrt(dk).  Returns (q, k, v, new conv state
-    [2dk+dv, W-1])."""
+    L2-normalised, q scaled by 1/sqrt(dk).  The recurrence takes q, k, v in
+    the call's element type, as every call of the library does
+    (``operand_dtype`` 'bf16' / 'f32': rounded to it, ties to even; None:
+    exact).  Returns (q, k, v, new conv state [2dk+dv, W-1])."""
     xq, xk, xv = _f64(xq), _f64(xk), _f64(xv)
     dk = xq.shape[1]
     x = np.concatenate([xq, xk, xv], axis=1)
     prev = None if conv_state is None else _f64(conv_state).T
     y, st = short_conv(x, conv_w, prev, act)
-    q = l2_normalize(y[:, :dk]) / np.sqrt(dk)
-    k = l2_normalize(y[:, dk:2 * dk])
-    return q, k, y[:, 2 * dk:], st.T.copy()
+    q = round_to(l2_normalize(y[:, :dk]) / np.sqrt(dk), operand_dtype)
+    k = round_to(l2_normalize(y[:, dk:2 * dk]), operand_dtype)
+    return q, k, round_to(y[:, 2 * dk:], operand_dtype), st.T.copy()
 
 
 def prefill_fused_pool(xq, xk, xv, g, beta, gate, conv_w, norm_w, cu_seqlens, init_slots,
-                       state_pool, conv_pool, snap_interval=0, act="none", **kw):
+                       state_pool, conv_pool, snap_interval=0, act="none", operand_dtype=None,
+                       **kw):
     """What ``kda_prefill_varlen_fused`` must produce: per sequence b and head h,
     the conv starts from conv_pool[src_b, h] (zeros when src_b < 0), its new
     state goes to conv_pool[dst_b, h]; the conv outputs feed ``prefill_pool``
@@ -532,7 +548,7 @@ def prefill_fused_pool(xq, xk, xv, g, beta, gate, conv_w, norm_w, cu_seqlens, in
         for h in range(H):
             st0 = cpool[src, h] if src >= 0 else None
             qb, kb, vb, st = fused_inputs(xq[t0:t1, h], xk[t0:t1, h], xv[t0:t1, h], cw[h], st0,
-                                          act)
+                                          act, operand_dtype)
             q[t0:t1, h], k[t0:t1, h], v[t0:t1, h] = qb, kb, vb
             conv_after[dst, h] = st
     o, after, snaps = prefill_pool(q, k, v, g, beta, cu, slots, state_pool, snap_interval, **kw)
@@ -540,7 +556,7 @@ def prefill_fused_pool(xq, xk, xv, g, beta, gate, conv_w, norm_w, cu_seqlens, in
 
 
 def decode_fused_pool(xq, xk, xv, g, beta, gate, conv_w, norm_w, slot_ids, state_pool,
-                      conv_pool, n_tok=1, act="none", **kw):
+                      conv_pool, n_tok=1, act="none", operand_dtype=None, **kw):
     """What ``kda_decode_fused`` must produce: sequence n owns rows
     [n n_tok, (n+1) n_tok) and slot slot_ids[n] of both pools; its conv runs
     from conv_pool[slot] and the slot's conv state advances in place like the
@@ -557,7 +573,7 @@ def decode_fused_pool(xq, xk, xv, g, beta, gate, conv_w, norm_w, slot_ids, state
         r0, r1 = n * n_tok, (n + 1) * n_tok
         for h in range(H):
             qb, kb, vb, st = fused_inputs(xq[r0:r1, h], xk[r0:r1, h], xv[r0:r1, h], cw[h],
-                                          cpool[slots[n], h], act)
+                                          cpool[slots[n], h], act, operand_dtype)
             q[r0:r1, h], k[r0:r1, h], v[r0:r1, h] = qb, kb, vb
             conv_after[slots[n], h] = st
     o, after, _ = decode_pool(q, k, v, g, beta, slots, state_pool, n_tok, False, **kw)

@@ -90,7 +90,8 @@ def assert_untouched(pool_after: torch.Tensor, pool_before: torch.Tensor, touche
     idx = torch.nonzero(keep).flatten()
     a = pool_after.detach().cpu()[idx]
     bb = pool_before.detach().cpu()[idx]
-    assert torch.equal(a.view(torch.int32), bb.view(torch.int32)), "untouched slots changed"
+    assert torch.equal(a.contiguous().view(torch.uint8), bb.contiguous().view(torch.uint8)), \
+        "untouched slots changed"
 
 
 def worst_unit(x, ref, cu, H):

@@ -135,3 +135,33 @@ def test_host_visible_errors_return_without_launch(lib):
                                 ctypes.byref(a))
     assert st == kda.KDA_ERR_UNSUPPORTED
     assert lib.kda_last_launch_count() == 0
+
+
+def test_fused_calls_host_visible_errors_and_scratch_size(lib):
+    """The convolution + gated-RMSNorm entry points refuse bad arguments on the
+    host before any launch; the prefill's scratch holds q, k, v and o."""
+    V = ctypes.c_void_p
+    fake = V(4096)
+    a = _args(workspace=V(1 << 26), workspace_bytes=1 << 26)
+    # T = 64, H = 2, dk = dv = 16, fp32: four 8 KiB regions
+    assert lib.kda_fused_scratch_bytes(ctypes.byref(a)) == 4 * 64 * 2 * 16 * 4
+    f = kda.KdaFusedArgs(gate=fake, conv_w=fake, norm_w=fake, conv_pool=fake, conv_width=4,
+                         conv_act=0, norm_eps=1e-6)
+    pre = lambda f_, scratch, n: lib.kda_prefill_varlen_fused(
+        fake, fake, fake, fake, fake, fake, fake, fake, fake, 0, None,
+        None if f_ is None else ctypes.byref(f_), scratch, n, ctypes.byref(a))
+    assert pre(None, fake, 1 << 20) == kda.KDA_ERR_INVALID_ARG
+    assert pre(f, fake, 16) == kda.KDA_ERR_INVALID_ARG          # scratch too small
+    assert pre(f, None, 1 << 20) == kda.KDA_ERR_INVALID_ARG     # no scratch
+    f3 = kda.KdaFusedArgs(gate=fake, conv_w=fake, norm_w=fake, conv_pool=fake, conv_width=3)
+    assert pre(f3, fake, 1 << 20) == kda.KDA_ERR_UNSUPPORTED    # only 4 taps
+    fa = kda.KdaFusedArgs(gate=fake, conv_w=fake, norm_w=fake, conv_pool=fake, conv_width=4,
+                          conv_act=7)
+    assert pre(fa, fake, 1 << 20) == kda.KDA_ERR_INVALID_ARG    # unknown activation
+    fn = kda.KdaFusedArgs(gate=None, conv_w=fake, norm_w=fake, conv_pool=fake, conv_width=4)
+    assert pre(fn, fake, 1 << 20) == kda.KDA_ERR_INVALID_ARG    # no gate
+    # the fused decode runs dk = dv = 128 only
+    ad = _args(B=4, T_total=4, workspace=V(1 << 26), workspace_bytes=1 << 26)
+    assert lib.kda_decode_fused(fake, fake, fake, fake, fake, fake, fake, fake, 1, None,
+                                ctypes.byref(f), ctypes.byref(ad)) == kda.KDA_ERR_UNSUPPORTED
+    assert lib.kda_last_launch_count() == 0

@@ -12,6 +12,7 @@ convolution state and the matrix state handed over together)."""
 import numpy as np
 import pytest
 import scipy.special
+import torch
 
 import oracle
 
@@ -213,3 +214,47 @@ def test_fused_with_identity_conv_and_open_gate_is_the_plain_recurrence_normed()
     rms = np.sqrt(np.mean(o_ref ** 2, axis=-1, keepdims=True) + oracle.RMS_EPS)
     np.testing.assert_allclose(o, o_ref / rms, rtol=1e-11, atol=1e-13)
     np.testing.assert_allclose(p, p_ref, rtol=1e-12)
+
+
+# ------------------------------------------------------------------ operand rounding
+
+def test_round_to_matches_torch_casts_and_bounds():
+    """On values that fp32 holds exactly, rounding to bf16 is torch's fp32 ->
+    bf16 cast (round to nearest, ties to even); rounding to f32 is numpy's
+    cast; both are idempotent, with relative error at most the unit roundoff
+    (2^-8 for 8 significant bits)."""
+    rng = _rng(11)
+    x32 = (rng.standard_normal(4096) * np.exp(rng.uniform(-20, 20, 4096))).astype(np.float32)
+    x32[:8] = [1.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -1.0 - 2.0 ** -8, 0.0, 3.0, 2.0 ** -9, 7.0]
+    ref = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.round_to(x32.astype(np.float64), "bf16")
+    np.testing.assert_array_equal(got, ref)
+    np.testing.assert_array_equal(oracle.round_to(got, "bf16"), got)
+    x = rng.standard_normal(1000)
+    np.testing.assert_array_equal(oracle.round_to(x, "f32"), x.astype(np.float32).astype(np.float64))
+    r = oracle.round_to(x, "bf16")
+    assert np.all(np.abs(r - x) <= 2.0 ** -8 * np.abs(x))   # unit roundoff of 8 bits
+    np.testing.assert_array_equal(oracle.round_to(x, None), x)
+
+
+def test_fused_operand_rounding_is_the_only_difference():
+    """With operand_dtype the recurrence sees q, k, v rounded to bf16, and
+    nothing else changes: the result equals the plain prefill of the rounded
+    exact operands."""
+    xq, xk, xv, g, beta, gate, cw, nw, pool, cpool = _fused_case(12, [9, 5])
+    cu, slots = [0, 9, 14], [[2, 1], [-1, 3]]
+    o, p, c, _ = oracle.prefill_fused_pool(xq, xk, xv, g, beta, gate, cw, nw, cu, slots, pool,
+                                           cpool, operand_dtype="bf16")
+    H, dk = xq.shape[1], xq.shape[2]
+    q, k, v = np.zeros_like(xq), np.zeros_like(xk), np.zeros_like(xv)
+    for b, (t0, t1) in enumerate([(0, 9), (9, 14)]):
+        src = slots[b][0]
+        for h in range(H):
+            qb, kb, vb, _ = oracle.fused_inputs(xq[t0:t1, h], xk[t0:t1, h], xv[t0:t1, h], cw[h],
+                                                cpool[src, h] if src >= 0 else None)
+            q[t0:t1, h] = oracle.round_to(qb, "bf16")
+            k[t0:t1, h] = oracle.round_to(kb, "bf16")
+            v[t0:t1, h] = oracle.round_to(vb, "bf16")
+    o_ref, p_ref, _ = oracle.prefill_pool(q, k, v, g, beta, cu, slots, pool)
+    np.testing.assert_allclose(o, oracle.rms_norm_gated(o_ref, nw, gate), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(p, p_ref, rtol=1e-12, atol=1e-14)
