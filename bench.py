@@ -85,6 +85,7 @@ def prefill_algorithmic(w, lens, n_snaps, n_resumed, es):
 # the kernel each decode workload runs (kda_decode.cu)
 DECODE_KERNEL = {
     "decode_256x1": "decode128_single_kernel (one token per state)",
+    "decode_fused_256x1": "decode_fused_kernel (convolution + recurrence + gated RMSNorm)",
     "verify_64x8": "decode128_kernel (staged tokens, per-token states, one CTA per state)",
     "spec_verify_64x8": "decode128_kernel (speculative: replay + commit + verify, one CTA per state)",
 }
@@ -103,6 +104,17 @@ def spec_algorithmic(w, N, accepted, es):
     b += replayed * H * (2 * dk + dv + 1) * es
     b += N * w.n_tok * H * (3 * dk + 2 * dv + 1) * es
     return b
+
+
+def fused_decode_algorithmic(w, N, n_tok, es, conv_width=4):
+    """Bytes of one fused decode call: each state read and written once, each
+    convolution state ((2 dk + dv) x (W-1) raw inputs) read and written once,
+    and per token-head the raw q, k, v, g, beta, gate in and the output out:
+    (2 dk + dv) + dk + 1 + dv + dv elements (769 at dk = dv = 128)."""
+    H, dk, dv = w.H, w.dk, w.dv
+    state = dk * dv * 4
+    conv = (2 * dk + dv) * (conv_width - 1) * es
+    return N * H * (2 * state + 2 * conv + n_tok * ((2 * dk + dv) + dk + 1 + 2 * dv) * es)
 
 
 def decode_algorithmic(w, N, n_tok, per_tok, es):
@@ -231,11 +243,15 @@ def job_throughput(tokens_per_rank, world, seconds):
     return tokens_per_rank * world / seconds
 
 
-def bench_prefill(args, torch, kda, inputs, world, rank, workload, retain=0, e2e=True):
+def bench_prefill(args, torch, kda, inputs, world, rank, workload, retain=0, e2e=True,
+                  fused=False):
     w = inputs.WORKLOADS[workload]
     if args.tokens and workload == args.workload:
         # a shortened single-sequence workload (profiling captures only)
         b = inputs.make_batch(w, device="cuda", lengths=[args.tokens])
+    elif args.seqs and workload == args.workload:
+        # the first sequences of a varlen workload (profiling captures only)
+        b = inputs.make_batch(w, device="cuda", lengths=inputs.seq_lengths(w)[:args.seqs])
     else:
         b = inputs.make_batch(w, device="cuda")
     dev = {n: getattr(b, n) for n in ("q", "k", "v", "g", "beta")}
@@ -260,6 +276,20 @@ def bench_prefill(args, torch, kda, inputs, world, rank, workload, retain=0, e2e
             kda.kda_prefill_varlen_retain(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], cu,
                                           slots, pool, out, w.snap_interval, smap, workspace=ws,
                                           events=events)
+    elif fused:
+        # the layer around the recurrence: dev q, k, v serve as the raw inputs
+        snaps = torch.empty((n_snaps, H, w.dk, w.dv), dtype=torch.float32, device="cuda")
+        n_written = n_snaps
+        ft = inputs.fused_tensors(T, H, w.dk, w.dv, dev["q"].dtype, w.index, pool.shape[0],
+                                  device="cuda")
+        scratch = torch.empty(kda.kda_fused_scratch_bytes(T, H, w.dk, w.dv, kda.KDA_BF16),
+                              dtype=torch.uint8, device="cuda")
+
+        def prefill(events=None):
+            kda.kda_prefill_varlen_fused(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"],
+                                         ft["gate"], ft["conv_w"], ft["norm_w"], cu, slots, pool,
+                                         ft["conv_pool"], out, w.snap_interval, snaps,
+                                         workspace=ws, scratch=scratch, events=events)
     else:
         snaps = torch.empty((n_snaps, H, w.dk, w.dv), dtype=torch.float32, device="cuda")
         n_written = n_snaps
@@ -352,7 +382,8 @@ def retention_map(b, interval, every, n_slots):
 
 
 def bench_decode(name, args, torch, kda, inputs):
-    w = inputs.WORKLOADS[name]
+    fused = name.startswith("decode_fused")
+    w = inputs.WORKLOADS["decode_256x1" if fused else name]
     b = inputs.make_batch(w, device="cuda")
     dev = {n: getattr(b, n) for n in ("q", "k", "v", "g", "beta")}
     slot_ids = b.slot_ids.cuda()
@@ -365,7 +396,15 @@ def bench_decode(name, args, torch, kda, inputs):
     ws = kda.workspace_for(N, H, pool.shape[0])
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
 
-    if w.spec:
+    if fused:
+        ft = inputs.fused_tensors(N * w.n_tok, H, w.dk, w.dv, dev["q"].dtype, w.index, w.n_slots,
+                                  device="cuda")
+
+        def call(events):
+            kda.kda_decode_fused(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], ft["gate"],
+                                 ft["conv_w"], ft["norm_w"], slot_ids, pool, ft["conv_pool"], out,
+                                 w.n_tok, workspace=ws, events=events)
+    elif w.spec:
         prev = {n: t.cuda() for n, t in b.extra["prev"].items()}
         acc = b.extra["accepted"].cuda()
 
@@ -382,7 +421,9 @@ def bench_decode(name, args, torch, kda, inputs):
     st, bits = kda.kda_device_status(ws)
     if st != kda.KDA_OK:
         raise RuntimeError(f"decode device check failed: {st} bits={bits}")
-    if w.spec:
+    if fused:
+        nbytes = fused_decode_algorithmic(w, N, w.n_tok, dev["q"].element_size())
+    elif w.spec:
         nbytes = spec_algorithmic(w, N, b.extra["accepted"], dev["q"].element_size())
     else:
         nbytes = decode_algorithmic(w, N, w.n_tok, w.per_tok_states, dev["q"].element_size())
@@ -497,6 +538,9 @@ def main():
     ap.add_argument("--tokens", type=int, default=0,
                     help="shorten the step's single-sequence workload to this many tokens "
                          "(profiling captures of a smaller case; not a bench number)")
+    ap.add_argument("--seqs", type=int, default=0,
+                    help="keep only the first N sequences of the step's varlen workload "
+                         "(profiling captures of a smaller case; not a bench number)")
     ap.add_argument("--retain", type=int, default=0,
                     help="keep every N-th interval snapshot in pool slots (retention map) "
                          "instead of writing all of them to the snapshot buffer")
@@ -534,7 +578,7 @@ def main():
         step_s, e2e_s, kern_s = reduce_over_ranks(torch, [step_s, e2e_s, kern_s], "cuda")
 
     extra = {}
-    if not (args.no_prefill or args.no_extra or args.tokens):
+    if not (args.no_prefill or args.no_extra or args.tokens or args.seqs):
         for name in EXTRA_PREFILL:
             if name == args.workload:
                 continue
@@ -545,10 +589,30 @@ def main():
                            "kernel_ms": ks * 1e3, "tokens_per_s": r["T"] / cs,
                            "snapshots": r["n_snaps"], "resumed": r["n_resumed"],
                            "roofline": prefill_roofline(r, ks, P, "prefill_" + name)}
+        # the layer around the recurrence on the 8k-token workload: the whole
+        # call (plan, convolution, convolution states, prefill, recomputation
+        # check, gated RMSNorm), its bytes those of the layer's inputs and
+        # outputs (raw q, k, v, g, beta, gate in; the normed output out)
+        r = bench_prefill(args, torch, kda, inputs, world, rank, "prefill_8k", e2e=False,
+                          fused=True)
+        ks = statistics.mean(r["kern_ms"]) / 1e3
+        cs = statistics.mean(r["call_ms"]) / 1e3
+        w8 = r["w"]
+        fb = r["T"] * w8.H * (3 * w8.dk + 1 + 3 * w8.dv) * 2 + \
+            w8.H * w8.dk * w8.dv * 4 * (1 + r["n_snaps"]) + \
+            2 * w8.H * (2 * w8.dk + w8.dv) * 3 * 2
+        extra["prefill_8k_fused"] = {
+            "workload": w8.note + "; with the short convolution and the gated RMSNorm",
+            "ms_per_call": cs * 1e3, "prefill_kernel_ms": ks * 1e3,
+            "tokens_per_s": r["T"] / cs, "launches": r["launches"] // max(args.steps, 1),
+            "call_GBps": fb / cs / 1e9, "algorithmic_bytes": fb,
+            "roofline": {"bound": "hbm", "achieved": fb / cs / 1e9, "peak": P["hbm_gbs"],
+                         "unit": "GB/s", "frac": fb / cs / 1e9 / P["hbm_gbs"], "traffic": None,
+                         "kernel": "whole call (6 kernels)", "peak_source": P["source"]}}
 
     dec = {}
     if not args.no_decode:
-        for name in ("decode_256x1", "verify_64x8", "spec_verify_64x8"):
+        for name in ("decode_256x1", "verify_64x8", "spec_verify_64x8", "decode_fused_256x1"):
             r = bench_decode(name, args, torch, kda, inputs)
             ks = statistics.mean(r["kern_ms"]) / 1e3
             cs = statistics.mean(r["call_ms"]) / 1e3
@@ -576,7 +640,8 @@ def main():
         cpu = OracleSample(args.workload).measure(target_s=12.0, one_core=True)
         cpu.pop("seconds", None)
 
-    short = f" shortened to {args.tokens} tokens" if args.tokens else ""
+    short = (f" shortened to {args.tokens} tokens" if args.tokens else
+             f" (first {args.seqs} sequences only)" if args.seqs else "")
     line = {
         "metric": METRIC,
         "value": job_throughput(pre["T"], world, step_s),
@@ -597,7 +662,8 @@ def main():
                                     "slot (kda_prefill_varlen_retain)"} if args.retain else {}),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "l2": "flushed between timed steps (256 MiB write); inputs exceed L2"},
-        "roofline": prefill_roofline(pre, kern_s, P, None if (args.retain or args.tokens)
+        "roofline": prefill_roofline(pre, kern_s, P,
+                                     None if (args.retain or args.tokens or args.seqs)
                                      else "prefill_" + args.workload),
         "cpu_baseline": cpu,
         "e2e": None if args.no_e2e else {"value": job_throughput(pre["T"], world, e2e_s),

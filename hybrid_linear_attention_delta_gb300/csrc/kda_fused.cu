@@ -51,8 +51,11 @@ __device__ __forceinline__ int seq_of(const int32_t *cu, int B, int64_t t) {
 }
 
 // One CTA: kConvTile packed tokens x one head; thread c: channel c of the
-// head's 2 dk + dv.  Writes q, k, v (the recurrence's inputs) for tokens of
-// sequences the plan accepted.
+// head's 2 dk + dv.  The tile's raw inputs are loaded together first; the
+// convolution then runs token by token with the channel's last inputs in
+// registers.  |q~| and |k~| of each token are reduced by one warp per (token,
+// part) in a fixed order (deterministic).  Writes q, k, v (the recurrence's
+// inputs) for tokens of sequences the plan accepted.
 template <typename T>
 __global__ void __launch_bounds__(kMaxConvC) conv_prefill_kernel(PrefillPlan p, FusedParams f) {
   const int c = threadIdx.x, h = blockIdx.y, H = p.H, dk = p.dk, dv = p.dv;
@@ -63,6 +66,12 @@ __global__ void __launch_bounds__(kMaxConvC) conv_prefill_kernel(PrefillPlan p, 
   __shared__ float sinv[2][kConvTile];     // 1 / |q~|, 1 / |k~| per token
   __shared__ int sb0;
   if (c == 0) sb0 = seq_of(p.cu_seqlens, p.B, t0);
+  float xs[kConvTile];
+  if (c < C) {
+#pragma unroll
+    for (int tt = 0; tt < kConvTile; ++tt)
+      xs[tt] = tt < n ? raw_input<T>(f, t0 + tt, H, h, dk, dv, c) : 0.f;
+  }
   __syncthreads();
   float y[kConvTile];
   int ok_mask = 0;  // bit tt: token t0 + tt belongs to an accepted sequence
@@ -72,19 +81,20 @@ __global__ void __launch_bounds__(kMaxConvC) conv_prefill_kernel(PrefillPlan p, 
     for (int i = 0; i < kConvW; ++i) w[i] = f.conv_w[((int64_t)h * C + c) * kConvW + i];
     int b = sb0;
     int64_t start = p.cu_seqlens[b], end = p.cu_seqlens[b + 1];
+    int ok = p.meta[b].ok;
     float hist[kConvW - 1];
     // the kConvW - 1 raw inputs before token t of sequence b, from the
     // sequence itself or from its starting convolution state
     auto init_hist = [&](int64_t t) {
-      const SeqMeta m = p.meta[b];
+      const int src = p.meta[b].src;
       const T *cp = static_cast<const T *>(f.conv_pool);
 #pragma unroll
       for (int i = 0; i < kConvW - 1; ++i) {
         const int64_t pos = t - start - (kConvW - 1) + i;
         if (pos >= 0)
           hist[i] = raw_input<T>(f, start + pos, H, h, dk, dv, c);
-        else if (m.src >= 0)
-          hist[i] = to_f32(cp[(((int64_t)m.src * H + h) * C + c) * (kConvW - 1) +
+        else if (src >= 0)
+          hist[i] = to_f32(cp[(((int64_t)src * H + h) * C + c) * (kConvW - 1) +
                               (kConvW - 1 + pos)]);
         else
           hist[i] = 0.f;
@@ -102,28 +112,33 @@ __global__ void __launch_bounds__(kMaxConvC) conv_prefill_kernel(PrefillPlan p, 
           start = p.cu_seqlens[b];
           end = p.cu_seqlens[b + 1];
         }
+        ok = p.meta[b].ok;
         init_hist(t);
       }
-      const float x = raw_input<T>(f, t, H, h, dk, dv, c);
-      float acc = w[kConvW - 1] * x;
+      float acc = w[kConvW - 1] * xs[tt];
 #pragma unroll
       for (int i = 0; i < kConvW - 1; ++i) acc = fmaf(w[i], hist[i], acc);
 #pragma unroll
       for (int i = 0; i + 1 < kConvW - 1; ++i) hist[i] = hist[i + 1];
-      hist[kConvW - 2] = x;
+      hist[kConvW - 2] = xs[tt];
       y[tt] = act_f(acc, f.act);
-      if (p.meta[b].ok) ok_mask |= 1 << tt;
+      if (ok) ok_mask |= 1 << tt;
       if (c < 2 * dk) ss[tt][c] = y[tt] * y[tt];
     }
   }
   __syncthreads();
-  // |q~| and |k~| of each token, summed over the channels in order
-  if (c < 2 * kConvTile) {
-    const int tt = c >> 1, part = c & 1;
-    float sum = 0.f;
-    if (tt < n)
-      for (int i = 0; i < dk; ++i) sum += ss[tt][part * dk + i];
-    sinv[part][tt] = sum > 0.f ? rsqrtf(sum) : 0.f;
+  // |q~| and |k~| of each token: warp w takes (token, part) pairs w, w + warps,
+  // ...; lane i sums channels i, i + 32, ... of the part, then a fixed tree
+  {
+    const int warp = c >> 5, lane = c & 31, nwarps = blockDim.x >> 5;
+    for (int pr = warp; pr < 2 * n; pr += nwarps) {
+      const int tt = pr >> 1, part = pr & 1;
+      float sum = 0.f;
+      for (int i = lane; i < dk; i += 32) sum += ss[tt][part * dk + i];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      if (lane == 0) sinv[part][tt] = sum > 0.f ? rsqrtf(sum) : 0.f;
+    }
   }
   __syncthreads();
   if (c >= C) return;
@@ -169,34 +184,50 @@ __global__ void __launch_bounds__(kMaxConvC) conv_state_kernel(PrefillPlan p, Fu
     cp[(((int64_t)m.dst * H + h) * C + c) * (kConvW - 1) + i] = from_f32<T>(ns[i]);
 }
 
-// One warp per (token, head) row of dv outputs: y = o / rms(o) * w * sigmoid(gate).
-// Rows of sequences the plan did not accept are not written.
+// y = o / rms(o) * w * sigmoid(gate) per (token, head) row of dv outputs.
+// One warp takes kRmsRows consecutive rows and issues all their loads (o,
+// gate and the row's sequence check) before it reduces; rows of sequences
+// the plan did not accept are not written.
+constexpr int kRmsRows = 4;
+
 template <typename T>
 __global__ void __launch_bounds__(256) rms_gate_kernel(PrefillPlan p, FusedParams f, const T *o,
                                                        T *out) {
   const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t row0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * kRmsRows;
   const int H = p.H, dv = p.dv;
-  if (row >= (int64_t)p.T_total * H) return;
-  const int64_t t = row / H;
-  if (!p.meta[seq_of(p.cu_seqlens, p.B, t)].ok) return;
-  const T *orow = o + row * dv;
-  const T *grow = static_cast<const T *>(f.gate) + row * dv;
-  float v[4];
-  float ss = 0.f;
+  const int64_t rows = (int64_t)p.T_total * H;
+  const T *gate = static_cast<const T *>(f.gate);
+  float v[kRmsRows][4], gt[kRmsRows][4];
+  int ok[kRmsRows];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int j = lane + 32 * e;
-    v[e] = j < dv ? to_f32(orow[j]) : 0.f;
-    ss = fmaf(v[e], v[e], ss);
+  for (int r = 0; r < kRmsRows; ++r) {
+    const int64_t row = row0 + r;
+    ok[r] = row < rows;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = lane + 32 * e;
+      const bool in = ok[r] && j < dv;
+      v[r][e] = in ? to_f32(o[row * dv + j]) : 0.f;
+      gt[r][e] = in ? to_f32(gate[row * dv + j]) : 0.f;
+    }
+    if (ok[r]) ok[r] = p.meta[seq_of(p.cu_seqlens, p.B, row / H)].ok;
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  const float r = rsqrtf(ss / (float)dv + f.eps);
+  for (int r = 0; r < kRmsRows; ++r) {
+    float ss = 0.f;
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int j = lane + 32 * e;
-    if (j < dv) out[row * dv + j] = from_f32<T>(v[e] * r * f.norm_w[j] * sigmoid_f(to_f32(grow[j])));
+    for (int e = 0; e < 4; ++e) ss = fmaf(v[r][e], v[r][e], ss);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (!ok[r]) continue;
+    const float rr = rsqrtf(ss / (float)dv + f.eps);
+    const int64_t row = row0 + r;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = lane + 32 * e;
+      if (j < dv) out[row * dv + j] = from_f32<T>(v[r][e] * rr * f.norm_w[j] * sigmoid_f(gt[r][e]));
+    }
   }
 }
 
@@ -399,7 +430,7 @@ cudaError_t launch_conv_state(const PrefillPlan &p, const FusedParams &f) {
 cudaError_t launch_rms_gate(const PrefillPlan &p, const FusedParams &f, const void *o, void *out) {
   const int64_t rows = (int64_t)p.T_total * p.H;
   if (rows == 0) return cudaSuccess;
-  const unsigned grid = (unsigned)((rows + 7) / 8);
+  const unsigned grid = (unsigned)((rows + 8 * kRmsRows - 1) / (8 * kRmsRows));
   if (p.dtype == KDA_BF16)
     rms_gate_kernel<__nv_bfloat16><<<grid, 256, 0, p.stream>>>(
         p, f, static_cast<const __nv_bfloat16 *>(o), static_cast<__nv_bfloat16 *>(out));
