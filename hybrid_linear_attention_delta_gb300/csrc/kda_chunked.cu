@@ -1258,10 +1258,11 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
 //     S <- Diag(e^{G_C}) S + acc and writes snapshots.
 //   warp 4, one lane (MMA): per chunk, once package n has landed it hands its
 //     ring slot back to the producers; once S^T is stored, X^T = S^T W^^T
-//     (commit: X ready); once the state warps stored U^T = U~^T - X^T,
-//     acc^T = U^T K^ (commit: acc ready), then the outputs O^T = S^T Q+'^T +
-//     U^T M^T (commit: outputs ready, stage free), so that the state step
-//     never queues behind output work on the tensor cores.
+//     (commit: X ready) and O^T = S^T Q+'^T (it runs while the state warps
+//     form U^T); once they stored U^T = U~^T - X^T, acc^T = U^T K^ (commit:
+//     acc ready) and O^T += U^T M^T (commit: outputs ready, stage free).
+//     (Same-box A/B on the 2^20-token prefill: 23.2 ms in this order, 24.6 ms
+//     with acc^T ahead of O^T = S^T Q+'^T.)
 //   warp 5, one lane (loader): waits until package n is in the ring and its
 //     stage n % 3 is free, and requests it with bulk copies; the next
 //     package's ready flag is read (acquire) while this one is in flight.
@@ -1486,7 +1487,10 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u) {
         mma_bf16_ts(xt, sa + kk * 8, sw128_desc(sp + kPkW + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
                     idesc_bf16(128, 64, 0, 0), kk > 0);
       mma_commit(xf);
-      // the state step (acc^T) goes ahead of the outputs on the tensor cores
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // O^T = S^T Q+'^T
+        mma_bf16_ts(o, sa + kk * 8, sw128_desc(sp + kPkQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
+                    idesc_bf16(128, 64, 0, 0), kk > 0);
       if (!mbar_wait(uready, n & 1)) { failed = true; break; }
       tc_fence_after();
 #pragma unroll
@@ -1494,10 +1498,6 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u) {
         mma_bf16_ts(tmem, ut + kk * 8, sw128_desc(sp + kPkKm + kk * 2048, 8192, 1024),
                     idesc_bf16(128, 128, 0, 1), kk > 0);
       mma_commit(accf);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // O^T = S^T Q+'^T
-        mma_bf16_ts(o, sa + kk * 8, sw128_desc(sp + kPkQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
-                    idesc_bf16(128, 64, 0, 0), kk > 0);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)  // O^T += U^T M^T
         mma_bf16_ts(o, ut + kk * 8, sw128_desc(sp + kPkM + kk * 32, 16, 1024),
