@@ -58,9 +58,10 @@ __device__ __forceinline__ int seq_of(const int32_t *cu, int B, int64_t t) {
 // inputs) for tokens of sequences the plan accepted.
 template <typename T>
 __global__ void __launch_bounds__(kMaxConvC) conv_prefill_kernel(PrefillPlan p, FusedParams f) {
-  const int c = threadIdx.x, h = blockIdx.y, H = p.H, dk = p.dk, dv = p.dv;
+  // heads fastest: the CTAs resident together read whole token rows
+  const int c = threadIdx.x, H = p.H, h = (int)(blockIdx.x % (unsigned)H), dk = p.dk, dv = p.dv;
   const int C = 2 * dk + dv;
-  const int64_t t0 = (int64_t)blockIdx.x * kConvTile;
+  const int64_t t0 = (int64_t)(blockIdx.x / (unsigned)H) * kConvTile;
   const int n = (int)min((int64_t)kConvTile, (int64_t)p.T_total - t0);
   __shared__ float ss[kConvTile][256];     // squares of the q and k channels
   __shared__ float sinv[2][kConvTile];     // 1 / |q~|, 1 / |k~| per token
@@ -185,61 +186,74 @@ __global__ void __launch_bounds__(kMaxConvC) conv_state_kernel(PrefillPlan p, Fu
 }
 
 // y = o / rms(o) * w * sigmoid(gate) per (token, head) row of dv outputs.
-// One warp takes kRmsRows consecutive rows and issues all their loads (o,
-// gate and the row's sequence check) before it reduces; rows of sequences
-// the plan did not accept are not written.
+// One warp takes kRmsRows consecutive rows, lane i elements [E i, E i + E)
+// of each (E = max(dv / 32, 1): one vector load per row and tensor; lanes
+// past dv idle), and issues all their loads before it reduces.  The rows' sequences come from one search
+// and a forward walk; rows of sequences the plan did not accept are not
+// written.
 constexpr int kRmsRows = 4;
 
-template <typename T>
+template <typename T, int E>
+struct alignas(E * sizeof(T)) VecT {
+  T x[E];
+};
+
+template <typename T, int E>
 __global__ void __launch_bounds__(256) rms_gate_kernel(PrefillPlan p, FusedParams f, const T *o,
                                                        T *out) {
+  using V = VecT<T, E>;
   const int lane = threadIdx.x & 31;
   const int64_t row0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * kRmsRows;
   const int H = p.H, dv = p.dv;
   const int64_t rows = (int64_t)p.T_total * H;
+  if (row0 >= rows) return;
+  const bool act = E * lane < dv;
+  const int col = act ? E * lane : 0;
   const T *gate = static_cast<const T *>(f.gate);
-  float v[kRmsRows][4], gt[kRmsRows][4];
-  int ok[kRmsRows];
+  V v[kRmsRows], gt[kRmsRows];
+#pragma unroll
+  for (int r = 0; r < kRmsRows; ++r) {
+    const int64_t row = row0 + r < rows ? row0 + r : rows - 1;
+    v[r] = *reinterpret_cast<const V *>(o + row * dv + col);
+    gt[r] = *reinterpret_cast<const V *>(gate + row * dv + col);
+  }
+  float nw[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) nw[e] = f.norm_w[col + e];
+  int b = seq_of(p.cu_seqlens, p.B, row0 / H);
 #pragma unroll
   for (int r = 0; r < kRmsRows; ++r) {
     const int64_t row = row0 + r;
-    ok[r] = row < rows;
+    if (row >= rows) break;
+    while (b + 1 < p.B && p.cu_seqlens[b + 1] <= row / H) ++b;
+    float x[E], ss = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int j = lane + 32 * e;
-      const bool in = ok[r] && j < dv;
-      v[r][e] = in ? to_f32(o[row * dv + j]) : 0.f;
-      gt[r][e] = in ? to_f32(gate[row * dv + j]) : 0.f;
+    for (int e = 0; e < E; ++e) {
+      x[e] = act ? to_f32(v[r].x[e]) : 0.f;
+      ss = fmaf(x[e], x[e], ss);
     }
-    if (ok[r]) ok[r] = p.meta[seq_of(p.cu_seqlens, p.B, row / H)].ok;
-  }
-#pragma unroll
-  for (int r = 0; r < kRmsRows; ++r) {
-    float ss = 0.f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) ss = fmaf(v[r][e], v[r][e], ss);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    if (!ok[r]) continue;
+    if (!act || !p.meta[b].ok) continue;
     const float rr = rsqrtf(ss / (float)dv + f.eps);
-    const int64_t row = row0 + r;
+    V y;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int j = lane + 32 * e;
-      if (j < dv) out[row * dv + j] = from_f32<T>(v[r][e] * rr * f.norm_w[j] * sigmoid_f(gt[r][e]));
-    }
+    for (int e = 0; e < E; ++e) y.x[e] = from_f32<T>(x[e] * rr * nw[e] * sigmoid_f(to_f32(gt[r].x[e])));
+    *reinterpret_cast<V *>(out + row * dv + col) = y;
   }
 }
 
 // ------------------------------------------------------------------ decode
 // One CTA of 256 threads per (sequence, head), dk = dv = 128; the state
 // layout of the 128 x 128 decode kernels (warp w: rows [16 w, +16), lane l:
-// columns [4 l, +4)), read once and written once.  Per token: the
-// convolution of the 384 raw channels (thread c and c + 256), the L2
+// columns [4 l, +4)), read once and written once.  The state loads are issued
+// first; everything else overlaps them.  Thread c owns raw channel c (q for
+// c < 128, k otherwise) and, for c < 128, channel 256 + c (v): its last three raw
+// inputs live in registers and go back to the slot's convolution state at the
+// end.  Per token: the convolution, the L2
 // normalisation of q and k, their rounding to the call's element type (the
-// type every call's recurrence takes them in), the recurrence step, the gated
-// RMSNorm of the output; the channel's last three raw inputs stay in shared memory and go
-// back to the slot's convolution state at the end.
+// type every call's recurrence takes them in), the recurrence step and the
+// gated RMSNorm of the output, with five block barriers.
 constexpr int kD = 128;
 constexpr int kDecThreads = 256;
 constexpr int kRows = kD / (kDecThreads / 32);  // 16
@@ -251,13 +265,12 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(DecodePlan
   const int H = p.H;
   const int n = blockIdx.x / H, h = blockIdx.x % H;
   __shared__ int s_slot;
-  __shared__ float hist[kC3][kConvW - 1];
-  __shared__ float cw[kC3][kConvW];
-  __shared__ __align__(16) float sq[kD], sk[kD], sv[kD], sa[kD], sg[kD];
+  __shared__ __align__(16) float sq[kD], sk[kD], sv[kD], sa[kD];
   __shared__ __align__(16) float su[kD], sy[kD];
   __shared__ __align__(16) float redx[kDecThreads / 32][kD], redy[kDecThreads / 32][kD];
-  __shared__ float red[kDecThreads / 32];
+  __shared__ float rn[kDecThreads / 32], rkq[4], ro[4];
   __shared__ float sbeta;
+  __shared__ float taps[kC3][kConvW];  // read only by the thread that wrote it
 
   if (tid == 0) {
     int slot = p.slot_ids[n];
@@ -274,68 +287,75 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(DecodePlan
   const int slot = s_slot;
   if (slot < 0) return;
 
-  T *cpool = static_cast<T *>(f.conv_pool) + ((int64_t)slot * H + h) * kC3 * (kConvW - 1);
-  for (int c = tid; c < kC3; c += kDecThreads) {
-#pragma unroll
-    for (int i = 0; i < kConvW - 1; ++i) hist[c][i] = to_f32(cpool[c * (kConvW - 1) + i]);
-#pragma unroll
-    for (int i = 0; i < kConvW; ++i) cw[c][i] = f.conv_w[((int64_t)h * kC3 + c) * kConvW + i];
-  }
   const int64_t kStateElems = (int64_t)kD * kD;
   float *state = p.pool + ((int64_t)slot * H + h) * kStateElems;
   float4 s[kRows];
 #pragma unroll
   for (int m = 0; m < kRows; ++m)
     s[m] = __ldcs(reinterpret_cast<const float4 *>(state + (w * kRows + m) * kD) + l);
+
+  const bool has_v = tid < kD;
+  const int c0 = tid, c1 = 2 * kD + tid;
+  T *cpool = static_cast<T *>(f.conv_pool) + ((int64_t)slot * H + h) * kC3 * (kConvW - 1);
+  const float *cw = f.conv_w + (int64_t)h * kC3 * kConvW;
+#pragma unroll
+  for (int i = 0; i < kConvW; ++i) {
+    taps[c0][i] = cw[c0 * kConvW + i];
+    if (has_v) taps[c1][i] = cw[c1 * kConvW + i];
+  }
+  float h0[kConvW - 1], h1[kConvW - 1];
+#pragma unroll
+  for (int i = 0; i < kConvW - 1; ++i) {
+    h0[i] = to_f32(cpool[c0 * (kConvW - 1) + i]);
+    h1[i] = has_v ? to_f32(cpool[c1 * (kConvW - 1) + i]) : 0.f;
+  }
   const T *g = (const T *)p.g, *beta = (const T *)p.beta, *gate = (const T *)f.gate;
   T *out = (T *)p.out;
-  const float nw = tid < kD ? f.norm_w[tid] : 0.f;
+  const float nw = has_v ? f.norm_w[tid] : 0.f;
   const float qscale = rsqrtf((float)kD);
-  __syncthreads();
 
   for (int j = 0; j < p.n_tok; ++j) {
     const int64_t t = (int64_t)n * p.n_tok + j, row = t * H + h;
-    // convolution of the 384 channels: thread tid takes channel tid (q or k)
-    // and, for tid < 128, channel 256 + tid (v)
-    float ysq = 0.f;
-    for (int c = tid; c < kC3; c += kDecThreads) {
-      const float x = raw_input<T>(f, t, H, h, kD, kD, c);
-      float acc = cw[c][kConvW - 1] * x;
-#pragma unroll
-      for (int i = 0; i < kConvW - 1; ++i) acc = fmaf(cw[c][i], hist[c][i], acc);
-#pragma unroll
-      for (int i = 0; i + 1 < kConvW - 1; ++i) hist[c][i] = hist[c][i + 1];
-      hist[c][kConvW - 2] = x;
-      const float y = act_f(acc, f.act);
-      if (c < kD) { sq[c] = y; ysq = y * y; }
-      else if (c < 2 * kD) { sk[c - kD] = y; ysq = y * y; }
-      else sv[c - 2 * kD] = y;
-    }
-    if (tid < kD) {
-      sa[tid] = expf(to_f32(g[row * kD + tid]));
-      sg[tid] = sigmoid_f(to_f32(gate[row * kD + tid]));
-    }
+    const float x0 = raw_input<T>(f, t, H, h, kD, kD, c0);
+    const float x1 = has_v ? raw_input<T>(f, t, H, h, kD, kD, c1) : 0.f;
+    const float gr = has_v ? to_f32(g[row * kD + tid]) : 0.f;
+    const float gt = has_v ? to_f32(gate[row * kD + tid]) : 0.f;
     if (tid == 0) sbeta = to_f32(beta[row]);
+    float y0 = taps[c0][kConvW - 1] * x0, y1 = has_v ? taps[c1][kConvW - 1] * x1 : 0.f;
+#pragma unroll
+    for (int i = 0; i < kConvW - 1; ++i) {
+      y0 = fmaf(taps[c0][i], h0[i], y0);
+      if (has_v) y1 = fmaf(taps[c1][i], h1[i], y1);
+    }
+#pragma unroll
+    for (int i = 0; i + 1 < kConvW - 1; ++i) { h0[i] = h0[i + 1]; h1[i] = h1[i + 1]; }
+    h0[kConvW - 2] = x0;
+    h1[kConvW - 2] = x1;
+    y0 = act_f(y0, f.act);
+    y1 = act_f(y1, f.act);
+    float ysq = y0 * y0;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ysq += __shfl_xor_sync(0xffffffffu, ysq, off);
-    if (l == 0) red[w] = ysq;  // warps 0-3: |q~|^2 partials, 4-7: |k~|^2
+    if (l == 0) rn[w] = ysq;  // warps 0-3: |q~|^2 partials, 4-7: |k~|^2
     __syncthreads();
-    {  // the recurrence takes q, k, v in the call's element type (as the prefill does)
-      const float qn = (red[0] + red[1]) + (red[2] + red[3]);
-      const float kn = (red[4] + red[5]) + (red[6] + red[7]);
-      if (tid < kD) {
-        sq[tid] = to_f32(from_f32<T>(sq[tid] * (qn > 0.f ? rsqrtf(qn) : 0.f) * qscale));
-        sv[tid] = to_f32(from_f32<T>(sv[tid]));
-      } else {
-        sk[tid - kD] = to_f32(from_f32<T>(sk[tid - kD] * (kn > 0.f ? rsqrtf(kn) : 0.f)));
-      }
+    // the recurrence takes q, k, v in the call's element type (as the prefill does)
+    if (has_v) {
+      const float qn = (rn[0] + rn[1]) + (rn[2] + rn[3]);
+      sq[tid] = to_f32(from_f32<T>(y0 * (qn > 0.f ? rsqrtf(qn) : 0.f) * qscale));
+      sv[tid] = to_f32(from_f32<T>(y1));
+      sa[tid] = expf(gr);
+    } else {
+      const float kn = (rn[4] + rn[5]) + (rn[6] + rn[7]);
+      sk[tid - kD] = to_f32(from_f32<T>(y0 * (kn > 0.f ? rsqrtf(kn) : 0.f)));
     }
     __syncthreads();
     // the recurrence step of the 128 x 128 decode kernels
-    float kq = 0.f;
-    if (tid < kD) kq = sq[tid] * sk[tid];
+    if (has_v) {
+      float kq = sq[tid] * sk[tid];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+      for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+      if (l == 0) rkq[w] = kq;
+    }
     float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f), y4 = x4;
 #pragma unroll
     for (int m = 0; m < kRows; ++m) {
@@ -349,9 +369,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(DecodePlan
     }
     *reinterpret_cast<float4 *>(&redx[w][4 * l]) = x4;
     *reinterpret_cast<float4 *>(&redy[w][4 * l]) = y4;
-    __syncthreads();  // (the q . k partials of warps 0-3 go through red as well)
-    if (l == 0 && w < 4) red[w] = kq;
-    if (tid < kD) {
+    __syncthreads();
+    if (has_v) {
       float xs = 0.f;
 #pragma unroll
       for (int ww = 0; ww < kDecThreads / 32; ++ww) xs += redx[ww][tid];
@@ -365,10 +384,13 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(DecodePlan
     __syncthreads();
     // output o = y + u (k . q), then its RMSNorm and gate
     float o = 0.f;
-    if (tid < kD) o = fmaf(su[tid], (red[0] + red[1]) + (red[2] + red[3]), sy[tid]);
-    float osq = o * o;
+    if (has_v) {
+      o = fmaf(su[tid], (rkq[0] + rkq[1]) + (rkq[2] + rkq[3]), sy[tid]);
+      float osq = o * o;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) osq += __shfl_xor_sync(0xffffffffu, osq, off);
+      for (int off = 16; off > 0; off >>= 1) osq += __shfl_xor_sync(0xffffffffu, osq, off);
+      if (l == 0) ro[w] = osq;
+    }
     const float4 u4 = *reinterpret_cast<const float4 *>(&su[4 * l]);
 #pragma unroll
     for (int m = 0; m < kRows; ++m) {
@@ -382,23 +404,30 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(DecodePlan
       for (int m = 0; m < kRows; ++m)
         __stcs(reinterpret_cast<float4 *>(pt + (w * kRows + m) * kD) + l, s[m]);
     }
-    __syncthreads();  // every read of red (k . q) is done
-    if (l == 0 && w < 4) red[w] = osq;
+    // past this barrier only ro is still read (just below); the next token
+    // writes ro four barriers later, so its staging can start at once
     __syncthreads();
-    if (tid < kD) {
-      const float r = rsqrtf(((red[0] + red[1]) + (red[2] + red[3])) / (float)kD + f.eps);
-      out[row * kD + tid] = from_f32<T>(o * r * nw * sg[tid]);
+    if (has_v) {
+      const float r = rsqrtf(((ro[0] + ro[1]) + (ro[2] + ro[3])) / (float)kD + f.eps);
+      out[row * kD + tid] = from_f32<T>(o * r * nw * sigmoid_f(gt));
     }
-    __syncthreads();  // the next token's staging overwrites sq, sk, red
   }
 
 #pragma unroll
   for (int m = 0; m < kRows; ++m)
     __stcs(reinterpret_cast<float4 *>(state + (w * kRows + m) * kD) + l, s[m]);
-  for (int c = tid; c < kC3; c += kDecThreads) {
 #pragma unroll
-    for (int i = 0; i < kConvW - 1; ++i) cpool[c * (kConvW - 1) + i] = from_f32<T>(hist[c][i]);
+  for (int i = 0; i < kConvW - 1; ++i) {
+    cpool[c0 * (kConvW - 1) + i] = from_f32<T>(h0[i]);
+    if (has_v) cpool[c1 * (kConvW - 1) + i] = from_f32<T>(h1[i]);
   }
+}
+
+template <typename T>
+void launch_rms_vec(const PrefillPlan &p, const FusedParams &f, const T *o, T *out, unsigned grid) {
+  if (p.dv == 128) rms_gate_kernel<T, 4><<<grid, 256, 0, p.stream>>>(p, f, o, out);
+  else if (p.dv == 64) rms_gate_kernel<T, 2><<<grid, 256, 0, p.stream>>>(p, f, o, out);
+  else rms_gate_kernel<T, 1><<<grid, 256, 0, p.stream>>>(p, f, o, out);
 }
 
 }  // namespace
@@ -406,7 +435,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_fused_kernel(DecodePlan
 cudaError_t launch_conv_prefill(const PrefillPlan &p, const FusedParams &f) {
   if (p.T_total == 0) return cudaSuccess;
   const int C = 2 * p.dk + p.dv;
-  dim3 grid((unsigned)((p.T_total + kConvTile - 1) / kConvTile), p.H);
+  const unsigned grid = (unsigned)((p.T_total + kConvTile - 1) / kConvTile * p.H);
   const int threads = (C + 31) / 32 * 32;
   if (p.dtype == KDA_BF16)
     conv_prefill_kernel<__nv_bfloat16><<<grid, threads, 0, p.stream>>>(p, f);
@@ -431,12 +460,13 @@ cudaError_t launch_rms_gate(const PrefillPlan &p, const FusedParams &f, const vo
   const int64_t rows = (int64_t)p.T_total * p.H;
   if (rows == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((rows + 8 * kRmsRows - 1) / (8 * kRmsRows));
+  // dv is 16, 32, 64 or 128 (checked by every entry point) and every pointer
+  // is 16-byte aligned: each lane's E elements are one aligned vector
+  using bf = __nv_bfloat16;
   if (p.dtype == KDA_BF16)
-    rms_gate_kernel<__nv_bfloat16><<<grid, 256, 0, p.stream>>>(
-        p, f, static_cast<const __nv_bfloat16 *>(o), static_cast<__nv_bfloat16 *>(out));
+    launch_rms_vec<bf>(p, f, static_cast<const bf *>(o), static_cast<bf *>(out), grid);
   else
-    rms_gate_kernel<float><<<grid, 256, 0, p.stream>>>(p, f, static_cast<const float *>(o),
-                                                       static_cast<float *>(out));
+    launch_rms_vec<float>(p, f, static_cast<const float *>(o), static_cast<float *>(out), grid);
   return cudaGetLastError();
 }
 

@@ -119,6 +119,25 @@ def test_fused_prefill_fp32_path():
     np.testing.assert_array_equal(cp.cpu().numpy()[touched], rconv[touched])
 
 
+@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (16, "f32")])
+def test_fused_prefill_narrow_heads(d, dtype):
+    """Heads of 64 and 16 channels: the gated RMSNorm's rows then take two
+    elements per lane, or one on half of the lanes."""
+    lens = [90, 1, 33]
+    slots = [[0, 0], [-1, 1], [2, 3]]
+    cu, sl, tt, ft, pool = _prefill_case(lens, 3, 5, slots, dtype=dtype, d=d)
+    out, p, cp, snaps, (st, bits) = _run_prefill(cu, sl, tt, ft, pool, 32, act="silu")
+    assert st == kda.KDA_OK and bits == 0
+    ro, rpool, rconv, rsn = _oracle_prefill(cu, sl, tt, ft, pool, 32, act="silu")
+    touched = _touched(sl)
+    tol = TOL[dtype]
+    assert rel(out, ro) <= tol, rel(out, ro)
+    assert worst_unit(out, ro, cu.numpy(), 3) <= 2 * tol
+    assert rel(p[touched], rpool[touched]) <= tol
+    assert rel(snaps, rsn) <= tol
+    np.testing.assert_array_equal(cp.float().cpu().numpy()[touched], rconv[touched])
+
+
 @pytest.mark.parametrize("n_tok,act,dtype", [(1, "none", "bf16"), (4, "silu", "bf16"),
                                              (3, "none", "f32")])
 def test_fused_decode_matches_oracle(n_tok, act, dtype):
