@@ -23,7 +23,6 @@
 namespace kda {
 namespace {
 
-constexpr int kConvTile = 16;     // tokens per CTA of the prefill convolution
 constexpr int kMaxConvC = 384;    // channels of a head: 2 dk + dv <= 384
 
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
@@ -50,112 +49,171 @@ __device__ __forceinline__ int seq_of(const int32_t *cu, int B, int64_t t) {
   return lo;
 }
 
-// One CTA: kConvTile packed tokens x one head; thread c: channel c of the
-// head's 2 dk + dv.  The tile's raw inputs are loaded together first; the
-// convolution then runs token by token with the channel's last inputs in
-// registers.  |q~| and |k~| of each token are reduced by one warp per (token,
-// part) in a fixed order (deterministic).  Writes q, k, v (the recurrence's
-// inputs) for tokens of sequences the plan accepted.
+// Four consecutive elements of T as one vector (8 bytes for bf16, 16 for
+// fp32), and their conversion to and from fp32 (round to nearest even).
+template <typename T> struct Quad;
+template <> struct Quad<__nv_bfloat16> { uint2 u; };
+template <> struct Quad<float> { uint4 u; };
+
 template <typename T>
-__global__ void __launch_bounds__(kMaxConvC) conv_prefill_kernel(PrefillPlan p, FusedParams f) {
-  // heads fastest: the CTAs resident together read whole token rows
-  const int c = threadIdx.x, H = p.H, h = (int)(blockIdx.x % (unsigned)H), dk = p.dk, dv = p.dv;
-  const int C = 2 * dk + dv;
-  const int64_t t0 = (int64_t)(blockIdx.x / (unsigned)H) * kConvTile;
-  const int n = (int)min((int64_t)kConvTile, (int64_t)p.T_total - t0);
-  __shared__ float ss[kConvTile][256];     // squares of the q and k channels
-  __shared__ float sinv[2][kConvTile];     // 1 / |q~|, 1 / |k~| per token
-  __shared__ int sb0;
-  if (c == 0) sb0 = seq_of(p.cu_seqlens, p.B, t0);
-  float xs[kConvTile];
-  if (c < C) {
-#pragma unroll
-    for (int tt = 0; tt < kConvTile; ++tt)
-      xs[tt] = tt < n ? raw_input<T>(f, t0 + tt, H, h, dk, dv, c) : 0.f;
-  }
-  __syncthreads();
-  float y[kConvTile];
-  int ok_mask = 0;  // bit tt: token t0 + tt belongs to an accepted sequence
-  if (c < C) {
-    float w[kConvW];
-#pragma unroll
-    for (int i = 0; i < kConvW; ++i) w[i] = f.conv_w[((int64_t)h * C + c) * kConvW + i];
-    int b = sb0;
-    int64_t start = p.cu_seqlens[b], end = p.cu_seqlens[b + 1];
-    int ok = p.meta[b].ok;
-    float hist[kConvW - 1];
-    // the kConvW - 1 raw inputs before token t of sequence b, from the
-    // sequence itself or from its starting convolution state
-    auto init_hist = [&](int64_t t) {
-      const int src = p.meta[b].src;
-      const T *cp = static_cast<const T *>(f.conv_pool);
-#pragma unroll
-      for (int i = 0; i < kConvW - 1; ++i) {
-        const int64_t pos = t - start - (kConvW - 1) + i;
-        if (pos >= 0)
-          hist[i] = raw_input<T>(f, start + pos, H, h, dk, dv, c);
-        else if (src >= 0)
-          hist[i] = to_f32(cp[(((int64_t)src * H + h) * C + c) * (kConvW - 1) +
-                              (kConvW - 1 + pos)]);
-        else
-          hist[i] = 0.f;
-      }
-    };
-    init_hist(t0);
-#pragma unroll
-    for (int tt = 0; tt < kConvTile; ++tt) {
-      y[tt] = 0.f;
-      if (tt >= n) continue;
-      const int64_t t = t0 + tt;
-      if (t >= end) {  // the next sequence (skipping empty ones) starts here
-        while (t >= end) {
-          ++b;
-          start = p.cu_seqlens[b];
-          end = p.cu_seqlens[b + 1];
-        }
-        ok = p.meta[b].ok;
-        init_hist(t);
-      }
-      float acc = w[kConvW - 1] * xs[tt];
-#pragma unroll
-      for (int i = 0; i < kConvW - 1; ++i) acc = fmaf(w[i], hist[i], acc);
-#pragma unroll
-      for (int i = 0; i + 1 < kConvW - 1; ++i) hist[i] = hist[i + 1];
-      hist[kConvW - 2] = xs[tt];
-      y[tt] = act_f(acc, f.act);
-      if (ok) ok_mask |= 1 << tt;
-      if (c < 2 * dk) ss[tt][c] = y[tt] * y[tt];
-    }
-  }
-  __syncthreads();
-  // |q~| and |k~| of each token: warp w takes (token, part) pairs w, w + warps,
-  // ...; lane i sums channels i, i + 32, ... of the part, then a fixed tree
+__device__ __forceinline__ Quad<T> load_quad(const T *p) {
+  Quad<T> q;
+  q.u = __ldcs(reinterpret_cast<const decltype(q.u) *>(p));
+  return q;
+}
+
+__device__ __forceinline__ void unpack_quad(const Quad<__nv_bfloat16> &q, float (&x)[4]) {
+  x[0] = __uint_as_float(q.u.x << 16);
+  x[1] = __uint_as_float(q.u.x & 0xffff0000u);
+  x[2] = __uint_as_float(q.u.y << 16);
+  x[3] = __uint_as_float(q.u.y & 0xffff0000u);
+}
+__device__ __forceinline__ void unpack_quad(const Quad<float> &q, float (&x)[4]) {
+  x[0] = __uint_as_float(q.u.x); x[1] = __uint_as_float(q.u.y);
+  x[2] = __uint_as_float(q.u.z); x[3] = __uint_as_float(q.u.w);
+}
+
+__device__ __forceinline__ void store_quad(__nv_bfloat16 *p, const float (&y)[4]) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]), hi = __floats2bfloat162_rn(y[2], y[3]);
+  *reinterpret_cast<uint2 *>(p) =
+      make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+}
+__device__ __forceinline__ void store_quad(float *p, const float (&y)[4]) {
+  *reinterpret_cast<float4 *>(p) = make_float4(y[0], y[1], y[2], y[3]);
+}
+
+// The prefill convolution.  A unit is (head h, run of kConvRun consecutive
+// packed tokens); a CTA takes kConvUnits units, heads fastest, so the CTAs
+// that run together read whole token rows.  Unit u has three warps, one per
+// part (q, k, v); lane i owns channels [4 i, 4 i + 4) of the part (one vector
+// load per token), so |q~| and |k~| of a token are a shuffle tree inside one
+// warp.  A lane keeps its taps and its channels' last three raw inputs in
+// registers and walks its run a batch of tokens at a time (64 bytes a lane),
+// the batch's loads issued together.  At a run start inside a sequence the
+// history is the three tokens before it; at a sequence start, the sequence's
+// starting convolution state (zeros without one).  Writes q, k, v (the
+// recurrence's inputs) for tokens of sequences the plan accepted.
+constexpr int kConvRun = 32;
+constexpr int kConvUnits = 2;
+constexpr int kConvThreads = 32 * 3 * kConvUnits;
+constexpr int kConvBatchBytes = 64;  // per lane in flight: 8 bf16 or 4 fp32 tokens
+
+template <typename T>
+__global__ void __launch_bounds__(kConvThreads, 4) conv_prefill_kernel(PrefillPlan p, FusedParams f) {
+  constexpr int kConvBatch = kConvBatchBytes / (int)sizeof(Quad<T>);
+  const int H = p.H, dk = p.dk, dv = p.dv, C = 2 * dk + dv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = warp / 3, part = warp % 3;  // part 0: q, 1: k, 2: v
+  const int dpart = part == 2 ? dv : dk;
+  const bool active = 4 * lane < dpart;
+  const int64_t u = (int64_t)blockIdx.x * kConvUnits + unit;
+  const int h = (int)(u % H);
+  if (u / H * kConvRun >= p.T_total) return;  // the whole warp (one unit)
+  const int tb = (int)(u / H) * kConvRun;      // token indices fit int32 (T_total does)
+  const int te = tb + min(kConvRun, p.T_total - tb);
+  const int q4 = active ? 4 * lane : 0;  // first channel of the lane within its part
+  const int c0 = part * dk + q4;         // ... within [q | k | v]
+  const T *x = static_cast<const T *>(part == 0 ? f.xq : part == 1 ? f.xk : f.xv);
+  T *y_out = static_cast<T *>(const_cast<void *>(part == 0 ? p.q : part == 1 ? p.k : p.v));
+  const int col = h * dpart + q4, row_stride = H * dpart;
+
+  float w[4][kConvW];
   {
-    const int warp = c >> 5, lane = c & 31, nwarps = blockDim.x >> 5;
-    for (int pr = warp; pr < 2 * n; pr += nwarps) {
-      const int tt = pr >> 1, part = pr & 1;
-      float sum = 0.f;
-      for (int i = lane; i < dk; i += 32) sum += ss[tt][part * dk + i];
+    const float *wp = f.conv_w + ((int64_t)h * C + c0) * kConvW;
+    if ((reinterpret_cast<uintptr_t>(f.conv_w) & 15u) == 0) {
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      if (lane == 0) sinv[part][tt] = sum > 0.f ? rsqrtf(sum) : 0.f;
+      for (int e = 0; e < 4; ++e) {
+        const float4 t4 = reinterpret_cast<const float4 *>(wp)[e];
+        w[e][0] = t4.x; w[e][1] = t4.y; w[e][2] = t4.z; w[e][3] = t4.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int i = 0; i < kConvW; ++i) w[e][i] = wp[e * kConvW + i];
     }
   }
-  __syncthreads();
-  if (c >= C) return;
-  const float qscale = rsqrtf((float)dk);
+
+  int b = seq_of(p.cu_seqlens, p.B, tb);
+  int start = p.cu_seqlens[b], end = p.cu_seqlens[b + 1];
+  int ok = p.meta[b].ok;
+  float hist[kConvW - 1][4];
+  // the kConvW - 1 raw inputs before token t of sequence b: tokens of the
+  // sequence, else its starting convolution state, else zeros
+  auto init_hist = [&](int t) {
+    const int src = p.meta[b].src;
+    const T *cp = static_cast<const T *>(f.conv_pool) +
+                  (((int64_t)(src >= 0 ? src : 0) * H + h) * C + c0) * (kConvW - 1);
 #pragma unroll
-  for (int tt = 0; tt < kConvTile; ++tt) {
-    if (!(ok_mask >> tt & 1)) continue;
-    const int64_t t = t0 + tt;
-    if (c < dk)
-      static_cast<T *>(const_cast<void *>(p.q))[(t * H + h) * dk + c] =
-          from_f32<T>(y[tt] * sinv[0][tt] * qscale);
-    else if (c < 2 * dk)
-      static_cast<T *>(const_cast<void *>(p.k))[(t * H + h) * dk + c - dk] =
-          from_f32<T>(y[tt] * sinv[1][tt]);
-    else
-      static_cast<T *>(const_cast<void *>(p.v))[(t * H + h) * dv + c - 2 * dk] = from_f32<T>(y[tt]);
+    for (int i = 0; i < kConvW - 1; ++i) {
+      const int pos = t - (kConvW - 1) + i;
+      if (pos >= start) {
+        unpack_quad(load_quad(x + (int64_t)pos * row_stride + col), hist[i]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          hist[i][e] = src >= 0 ? to_f32(cp[e * (kConvW - 1) + (kConvW - 1) + (pos - start)]) : 0.f;
+      }
+    }
+  };
+  init_hist(tb);
+  const float qscale = rsqrtf((float)dk);
+
+  // one token: convolution, |q~| or |k~| (a shuffle tree over the warp's
+  // active lanes; the others hold 0), scaling, store
+  auto step = [&](const Quad<T> &xq4, int t) {
+    float xv[4], y[4], ss = 0.f;
+    unpack_quad(xq4, xv);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float acc = w[e][kConvW - 1] * xv[e];
+#pragma unroll
+      for (int i = 0; i < kConvW - 1; ++i) acc = fmaf(w[e][i], hist[i][e], acc);
+      y[e] = act_f(acc, f.act);
+      ss = fmaf(y[e], y[e], ss);
+    }
+#pragma unroll
+    for (int i = 0; i + 1 < kConvW - 1; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) hist[i][e] = hist[i + 1][e];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) hist[kConvW - 2][e] = xv[e];
+    if (part < 2) {
+      if (!active) ss = 0.f;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      const float scale = ss > 0.f ? rsqrtf(ss) : 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) y[e] = part == 0 ? y[e] * scale * qscale : y[e] * scale;
+    }
+    if (active && ok) store_quad(y_out + (int64_t)t * row_stride + col, y);
+  };
+
+  // batches inside one sequence issue their loads together; a batch that
+  // reaches the run's end or a sequence start goes token by token
+  for (int t0 = tb; t0 < te; t0 += kConvBatch) {
+    if (t0 + kConvBatch <= te && t0 + kConvBatch <= end) {
+      Quad<T> xr[kConvBatch];
+#pragma unroll
+      for (int j = 0; j < kConvBatch; ++j) xr[j] = load_quad(x + (int64_t)(t0 + j) * row_stride + col);
+#pragma unroll
+      for (int j = 0; j < kConvBatch; ++j) step(xr[j], t0 + j);
+    } else {
+      const int t1 = min(t0 + kConvBatch, te);
+#pragma unroll 1
+      for (int t = t0; t < t1; ++t) {
+        if (t >= end) {  // the next sequence (skipping empty ones) starts here
+          while (t >= end) {
+            ++b;
+            start = p.cu_seqlens[b];
+            end = p.cu_seqlens[b + 1];
+          }
+          ok = p.meta[b].ok;
+          init_hist(t);
+        }
+        step(load_quad(x + (int64_t)t * row_stride + col), t);
+      }
+    }
   }
 }
 
@@ -434,13 +492,12 @@ void launch_rms_vec(const PrefillPlan &p, const FusedParams &f, const T *o, T *o
 
 cudaError_t launch_conv_prefill(const PrefillPlan &p, const FusedParams &f) {
   if (p.T_total == 0) return cudaSuccess;
-  const int C = 2 * p.dk + p.dv;
-  const unsigned grid = (unsigned)((p.T_total + kConvTile - 1) / kConvTile * p.H);
-  const int threads = (C + 31) / 32 * 32;
+  const int64_t units = (p.T_total + kConvRun - 1) / kConvRun * p.H;
+  const unsigned grid = (unsigned)((units + kConvUnits - 1) / kConvUnits);
   if (p.dtype == KDA_BF16)
-    conv_prefill_kernel<__nv_bfloat16><<<grid, threads, 0, p.stream>>>(p, f);
+    conv_prefill_kernel<__nv_bfloat16><<<grid, kConvThreads, 0, p.stream>>>(p, f);
   else
-    conv_prefill_kernel<float><<<grid, threads, 0, p.stream>>>(p, f);
+    conv_prefill_kernel<float><<<grid, kConvThreads, 0, p.stream>>>(p, f);
   return cudaGetLastError();
 }
 
