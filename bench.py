@@ -550,6 +550,9 @@ def main():
                     help="skip the other prefill workloads (reported under \"prefill\")")
     ap.add_argument("--no-prefill", action="store_true", help="decode only (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
+    ap.add_argument("--fused", action="store_true",
+                    help="run the step's prefill through the layer around the recurrence "
+                         "(convolution, prefill, gated RMSNorm); profiling captures, no e2e leg")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -571,7 +574,8 @@ def main():
     P = peaks()
     if not args.no_prefill:
         pre = bench_prefill(args, torch, kda, inputs, world, rank, args.workload,
-                            retain=args.retain, e2e=not args.no_e2e)
+                            retain=args.retain, e2e=not (args.no_e2e or args.fused),
+                            fused=args.fused)
         step_s = statistics.mean(pre["call_ms"]) / 1e3
         kern_s = statistics.mean(pre["kern_ms"]) / 1e3
         e2e_s = statistics.mean(pre["e2e_ms"]) / 1e3 if pre["e2e_ms"] else float("nan")
@@ -622,8 +626,10 @@ def main():
                          "state_GBps": gbs, "algorithmic_bytes": r["nbytes"],
                          "roofline": {"bound": "hbm", "achieved": gbs, "peak": P["hbm_gbs"],
                                       "unit": "GB/s", "frac": gbs / P["hbm_gbs"],
-                                      "traffic": ncu_traffic("decode128_" + name,
-                                                             ["kda_decode.cu"]),
+                                      "traffic": ncu_traffic(
+                                          "decode128_" + name,
+                                          ["kda_fused.cu" if name.startswith("decode_fused")
+                                           else "kda_decode.cu"]),
                                       "kernel": DECODE_KERNEL[name],
                                       "peak_source": P["source"]}}
 
@@ -663,10 +669,10 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "l2": "flushed between timed steps (256 MiB write); inputs exceed L2"},
         "roofline": prefill_roofline(pre, kern_s, P,
-                                     None if (args.retain or args.tokens or args.seqs)
+                                     None if (args.retain or args.tokens or args.seqs or args.fused)
                                      else "prefill_" + args.workload),
         "cpu_baseline": cpu,
-        "e2e": None if args.no_e2e else {"value": job_throughput(pre["T"], world, e2e_s),
+        "e2e": None if (args.no_e2e or args.fused) else {"value": job_throughput(pre["T"], world, e2e_s),
                                          "unit": "tokens/s",
                                          "h2d_bytes_per_step": pre["h2d"],
                                          "d2h_bytes_per_step": pre["d2h"]},
