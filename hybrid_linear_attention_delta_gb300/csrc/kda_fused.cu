@@ -26,6 +26,10 @@ namespace {
 constexpr int kMaxConvC = 384;    // channels of a head: 2 dk + dv <= 384
 
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+// the gate of the prefill's output norm, one per output element: the fast
+// exponential and division intrinsics (relative error a few ulp, far inside
+// the output's bf16 rounding); 0 for x below about -88, where e^-x overflows
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 __device__ __forceinline__ float act_f(float y, int act) {
   return act == 1 ? y / (1.f + expf(-y)) : y;
 }
@@ -278,12 +282,18 @@ __global__ void __launch_bounds__(256) rms_gate_kernel(PrefillPlan p, FusedParam
   float nw[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) nw[e] = f.norm_w[col + e];
-  int b = seq_of(p.cu_seqlens, p.B, row0 / H);
+  // token and head of the first row (one division a warp), then stepped
+  int t = (int)(row0 / H), hh = (int)(row0 - (int64_t)t * H);
+  int b = seq_of(p.cu_seqlens, p.B, t);
 #pragma unroll
   for (int r = 0; r < kRmsRows; ++r) {
     const int64_t row = row0 + r;
     if (row >= rows) break;
-    while (b + 1 < p.B && p.cu_seqlens[b + 1] <= row / H) ++b;
+    if (r > 0 && ++hh == H) {
+      hh = 0;
+      ++t;
+    }
+    while (b + 1 < p.B && p.cu_seqlens[b + 1] <= t) ++b;
     float x[E], ss = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -296,7 +306,7 @@ __global__ void __launch_bounds__(256) rms_gate_kernel(PrefillPlan p, FusedParam
     const float rr = rsqrtf(ss / (float)dv + f.eps);
     V y;
 #pragma unroll
-    for (int e = 0; e < E; ++e) y.x[e] = from_f32<T>(x[e] * rr * nw[e] * sigmoid_f(to_f32(gt[r].x[e])));
+    for (int e = 0; e < E; ++e) y.x[e] = from_f32<T>(x[e] * rr * nw[e] * sigmoid_fast(to_f32(gt[r].x[e])));
     *reinterpret_cast<V *>(out + row * dv + col) = y;
   }
 }
