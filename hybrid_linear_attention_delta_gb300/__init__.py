@@ -20,7 +20,7 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_DEVICE_C
     KDA_ERR_TIMEOUT = range(6)
 KDA_F32, KDA_BF16 = 0, 1
 KDA_ALGO_AUTO, KDA_ALGO_RECURRENT, KDA_ALGO_CHUNKED, KDA_ALGO_CHUNKED_PER_STATE, \
-    KDA_ALGO_CHUNKED_COOP = range(5)
+    KDA_ALGO_CHUNKED_COOP, KDA_ALGO_CHUNKED_COOP_HALVES = range(6)
 
 EXPORTS = ("kda_prefill_varlen", "kda_prefill_varlen_retain", "kda_decode", "kda_decode_spec",
            "kda_prefill_varlen_fused", "kda_decode_fused", "kda_fused_scratch_bytes",

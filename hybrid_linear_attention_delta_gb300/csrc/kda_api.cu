@@ -167,7 +167,7 @@ kda_status prefill(const void *q, const void *k, const void *v, const void *g, c
   if (snap_interval == 0 && target) return KDA_ERR_INVALID_ARG;
   if (snap_interval > 0 && !target && a->snaps_capacity > 0) return KDA_ERR_INVALID_ARG;
   if (snaps && !aligned16(snaps)) return KDA_ERR_INVALID_ARG;
-  if (a->algo < KDA_ALGO_AUTO || a->algo > KDA_ALGO_CHUNKED_COOP) return KDA_ERR_INVALID_ARG;
+  if (a->algo < KDA_ALGO_AUTO || a->algo > KDA_ALGO_CHUNKED_COOP_HALVES) return KDA_ERR_INVALID_ARG;
   if (a->B == 0) return a->T_total == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
   if (!cu_seqlens || !init_slots || !state_pool || !aligned16(state_pool))
     return KDA_ERR_INVALID_ARG;
@@ -216,6 +216,10 @@ kda_status prefill(const void *q, const void *k, const void *v, const void *g, c
   if (a->algo == KDA_ALGO_CHUNKED_COOP) {
     if (!kda::coop_supported(p)) return KDA_ERR_UNSUPPORTED;
     mode = kda::kChunkCoop;
+  }
+  if (a->algo == KDA_ALGO_CHUNKED_COOP_HALVES) {
+    if (!kda::coop_halves_supported(p)) return KDA_ERR_UNSUPPORTED;
+    mode = kda::kChunkCoopHalves;
   }
   if (a->algo >= KDA_ALGO_CHUNKED && !chunked) return KDA_ERR_UNSUPPORTED;
   if (a->algo == KDA_ALGO_RECURRENT) chunked = false;

@@ -916,9 +916,11 @@ constexpr uint32_t kCoopSmem =
 struct CoopArgs {
   ChunkArgs c;
   uint8_t *ring;                       // [units][kCoopRing][kCoopPkgBytes]
-  unsigned long long *ready, *consumed;  // [units][kCoopRing]
+  unsigned long long *ready;           // [units][kCoopRing]
+  unsigned long long *consumed;        // [split][units][kCoopRing], one per chain CTA
   uint32_t *hdr;                       // [0] ticket, [1] abort, [2] max chunks per sequence
-  int units;                           // (sequence, head) pairs = chain CTAs
+  int units;                           // (sequence, head) pairs
+  int split;                           // chain CTAs per pair: 1 (whole state) or 2 (column halves)
   uint32_t epoch;
 };
 
@@ -1148,9 +1150,13 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       mma_commit(bar_mma);
       s_item[2] = next >= 0 ? take_from(raw_ticket) : -1;
     }
-    if (tid == kPub)  // peek at this chunk's ring slot early; it is waited for only if the
-      // pair's chain CTA had not yet copied out the chunk that used it before
-      slot_seen = n >= kCoopRing ? ld_relaxed_u64(a.consumed + u * kCoopRing + n % kCoopRing) : 0;
+    if (tid == kPub && n >= kCoopRing) {  // peek at this chunk's ring slot early; it is waited
+      // for only if a chain CTA of the pair had not yet copied out the chunk that used it before
+      slot_seen = ld_relaxed_u64(a.consumed + u * kCoopRing + n % kCoopRing);
+      for (int hv = 1; hv < a.split; ++hv)
+        slot_seen = min(slot_seen,
+                        ld_relaxed_u64(a.consumed + ((size_t)hv * units + u) * kCoopRing + n % kCoopRing));
+    }
     mma_pending = true;
     if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
     mma_phase ^= 1;
@@ -1206,8 +1212,9 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       beta_r = beta_of(next);
       if (tid == kPub && after >= 0) issue_q(after, st);  // before the stores, on the same engine
       if (tid == kPub && n >= kCoopRing && slot_seen < coop_tag(a.epoch, n - kCoopRing))
-        ok = coop_flag_wait(a.consumed + u * kCoopRing + slot, coop_tag(a.epoch, n - kCoopRing),
-                            a.hdr + 1);
+        for (int hv = 0; hv < a.split && ok; ++hv)
+          ok = coop_flag_wait(a.consumed + ((size_t)hv * units + u) * kCoopRing + slot,
+                              coop_tag(a.epoch, n - kCoopRing), a.hdr + 1);
       // the package, piece by piece from where it was staged (W, S0 region,
       // U, M, e^{G_C}); these are first overwritten after
       // the next chunk's first MMA, where thread kPub waits for the stores
@@ -1276,7 +1283,172 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
-__device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u) {
+// State warps of a half chain: value columns [64 hv, 64 hv + 64) of pair u.
+// The chain's MMAs then have M = 64, whose rows m sit in TMEM lane
+// 32 (m / 16) + m % 16: warp w owns rows 16 w .. 16 w + 15 in the first 16
+// lanes of its quarter and reaches them with the 16-lane shapes, so every
+// thread works.  Thread t (g = t / 4, q = t % 4) holds value columns
+// j0 = 64 hv + 16 w + g and j0 + 8 and, of each, channels 8 r + 2 q + {0, 1},
+// r = 0..15: 64 state elements, half of a whole-column thread's 128.  The
+// 16x256b loads of X^T and acc^T hand it exactly the tokens or channels that
+// its 16x128b stores of U^T and S^T pack into one bf16 pair (column 4 r + q
+// holds K-positions 8 r + 2 q, 8 r + 2 q + 1), so no value changes thread.
+// Returns false when a wait gave up.
+__device__ bool chain_state_half(uint8_t *smem, const CoopArgs &a, int u, int hv, const SeqMeta &m,
+                                 int N, uint32_t tmem, uint32_t bars) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const uint32_t sbase = smem_u32(smem);
+  const int H = a.c.H, h = u % H, dv = a.c.dv;
+  const uint32_t full0 = bars, empty0 = bars + 24, sready0 = bars + 48, accf = bars + 64,
+                 xf = bars + 72, of0 = bars + 80, oe0 = bars + 96, uready = bars + 120;
+  const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+  const int j0 = 64 * hv + 16 * warp + g;
+  float S[2][32];  // S[s][2 r + e]: channel 8 r + 2 q + e of value column j0 + 8 s
+  if (m.ok && m.src >= 0) {
+    const float *s0 = a.c.pool + ((int64_t)m.src * H + h) * kDK * dv + j0;
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+      for (int i = 0; i < 32; ++i) S[s][i] = s0[(int64_t)(8 * (i >> 1) + 2 * q + (i & 1)) * dv + 8 * s];
+  } else {
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+      for (int i = 0; i < 32; ++i) S[s][i] = 0.f;
+  }
+  // outputs of chunk n, half hf (tokens 32 hf .. 32 hf + 31), from O^T buffer
+  // n & 1 with the 16x64b shape: register r is token 2 r + c of value column
+  // 64 hv + 16 w + orow, so per store the warp writes 16 consecutive outputs
+  // (32 bytes) of each of two tokens
+  const int orow = g + 8 * (lane & 1), oc = (lane >> 1) & 1;
+  auto retire = [&](int n, int hf) -> bool {
+    const int b = n & 1;
+    if (hf == 0 && !warp_wait(of0 + 8 * b, (n >> 1) & 1)) return false;
+    tc_fence_after();
+    uint32_t v[16];
+    tmem_ld16x64_x16(lane_base + 128 + 64 * b + 32 * hf, v);
+    tmem_wait_ld();
+    reg_fence16(v);
+    if (hf == 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(oe0 + 8 * b);
+    }
+    const int cl = min(kC, m.len - n * kC) - 32 * hf;
+    const int64_t ts = (int64_t)H * dv;
+    __nv_bfloat16 *o = a.c.out + ((int64_t)(m.tok0 + n * kC + 32 * hf + oc) * H + h) * dv +
+                       64 * hv + 16 * warp + orow;
+    if (cl >= 32) {
+#pragma unroll
+      for (int r = 0; r < 16; ++r) o[2 * r * ts] = __float2bfloat16_rn(__uint_as_float(v[r]));
+    } else {
+#pragma unroll
+      for (int r = 0; r < 16; ++r)
+        if (2 * r + oc < cl) o[2 * r * ts] = __float2bfloat16_rn(__uint_as_float(v[r]));
+    }
+    return true;
+  };
+  auto store_state = [&](float *base) {  // a whole state's [dk][dv] fp32 layout
+    float *d = base + j0;
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+      for (int i = 0; i < 32; ++i) d[(int64_t)(8 * (i >> 1) + 2 * q + (i & 1)) * dv + 8 * s] = S[s][i];
+  };
+  const int snap_every = a.c.snap_interval > 0 ? a.c.snap_interval / kC : 0;
+  int snap_left = snap_every;
+  int64_t snap_next = m.snap_off;
+  for (int n = 0; n < N; ++n) {
+    const int b = n & 1, st = n % kChStages;
+    {  // bf16(S^T) -> S^T[b]
+      uint32_t r[32];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        r[2 * i] = pack_bf16x2(S[0][2 * i], S[0][2 * i + 1]);
+        r[2 * i + 1] = pack_bf16x2(S[1][2 * i], S[1][2 * i + 1]);
+      }
+      tmem_st16x128_x16(lane_base + 256 + 64 * b, r);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sready0 + 8 * b);
+    if (n > 0 && !retire(n - 1, 0)) return false;
+    if (!warp_wait(full0 + 8 * st, (n / kChStages) & 1) || !warp_wait(xf, n & 1)) return false;
+    tc_fence_after();
+    const uint32_t sp = sbase + st * (uint32_t)kCoopPkgBytes;
+    {  // U^T = U~^T - X^T: tokens 8 r + 2 q + {0, 1} of value columns j0, j0 + 8
+      uint32_t x[32], w0[8], w1[8];
+      tmem_ld16x256_x8(lane_base + 384, x);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        w0[r] = ld_shared_u32(sp + kPkU + sw128_chunk(j0, r) + 4 * q);
+        w1[r] = ld_shared_u32(sp + kPkU + sw128_chunk(j0 + 8, r) + 4 * q);
+      }
+      tmem_wait_ld();
+      reg_fence(x);
+      uint32_t ur[16];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        ur[2 * r] = pack_bf16x2(bf16lo(w0[r]) - __uint_as_float(x[4 * r]),
+                                bf16hi(w0[r]) - __uint_as_float(x[4 * r + 1]));
+        ur[2 * r + 1] = pack_bf16x2(bf16lo(w1[r]) - __uint_as_float(x[4 * r + 2]),
+                                    bf16hi(w1[r]) - __uint_as_float(x[4 * r + 3]));
+      }
+      tmem_st16x128_x8(lane_base + 448, ur);
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(uready);
+    if (n > 0) retire(n - 1, 1);
+    if (!warp_wait(accf, n & 1)) return false;
+    tc_fence_after();
+    {  // S = Diag(e^{G_C}) S + acc: channels 8 r + 2 q + {0, 1}
+      const uint32_t egc = sp + kPkDec + 8 * q;
+      uint32_t v[2][32];
+      tmem_ld16x256_x8(lane_base, v[0]);
+      tmem_ld16x256_x8(lane_base + 64, v[1]);
+      tmem_wait_ld();
+      reg_fence(v[0]);
+      reg_fence(v[1]);
+#pragma unroll
+      for (int p = 0; p < 2; ++p)
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) {
+          const int r = 8 * p + rr;
+          const float2 e = ld_shared_f2(egc + 32 * r);
+          S[0][2 * r] = fmaf(e.x, S[0][2 * r], __uint_as_float(v[p][4 * rr]));
+          S[0][2 * r + 1] = fmaf(e.y, S[0][2 * r + 1], __uint_as_float(v[p][4 * rr + 1]));
+          S[1][2 * r] = fmaf(e.x, S[1][2 * r], __uint_as_float(v[p][4 * rr + 2]));
+          S[1][2 * r + 1] = fmaf(e.y, S[1][2 * r + 1], __uint_as_float(v[p][4 * rr + 3]));
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * st);
+    const int cl = min(kC, m.len - n * kC);
+    if (snap_every > 0 && --snap_left == 0 && cl == kC) {
+      snap_left = snap_every;
+      const int64_t s = snap_next++;
+      if (s < a.c.snaps_capacity) {
+        float *base = snapshot_base(a.c.snaps, a.c.snap_slots, a.c.pool, s, H, h, (int64_t)kDK * dv);
+        if (base) store_state(base);
+      } else if (tid == 0 && hv == 0) {
+        raise_error(a.c.err, ERR_SNAP_CAPACITY);
+      }
+    }
+  }
+  if (N > 0 && !(retire(N - 1, 0) && retire(N - 1, 1))) return false;
+  // a unit flagged by a producer keeps its source for the exact recomputation
+  const bool flagged = atomicAdd(a.c.rerun + u, 0u) == a.epoch;
+  if (m.ok && !flagged) store_state(a.c.pool + ((int64_t)m.dst * H + h) * kDK * dv);
+  return true;
+}
+
+template <bool kHalf>
+__device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u, int hv) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_u32(smem);
   const int H = a.c.H, h = u % H, dv = a.c.dv;
@@ -1312,7 +1484,9 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u) {
   const int N = m.ok ? (m.len + kC - 1) / kC : 0;
   bool failed = false;
 
-  if (warp < 4) {
+  if (warp < 4 && kHalf) {
+    failed = !chain_state_half(smem, a, u, hv, m, N, tmem, bars);
+  } else if (warp < 4) {
     const int j = tid;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     const int64_t cs = dv;  // stride between channels (rows) of a state
@@ -1459,7 +1633,8 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u) {
       for (int c = 0; c < kDK; ++c) d[c * cs] = S[c];
     }
   } else if (warp == 4 && lane == 0) {
-    unsigned long long *consumed = a.consumed + u * kCoopRing;
+    unsigned long long *consumed = a.consumed + ((size_t)hv * a.units + u) * kCoopRing;
+    constexpr int kM = kHalf ? 64 : 128;  // value columns this CTA carries
     bool issued = false;
     for (int n = 0; n < N; ++n) {
       const int b = n & 1, st = n % kChStages;
@@ -1485,23 +1660,23 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u) {
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)  // X^T = S^T W^^T
         mma_bf16_ts(xt, sa + kk * 8, sw128_desc(sp + kPkW + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
-                    idesc_bf16(128, 64, 0, 0), kk > 0);
+                    idesc_bf16(kM, 64, 0, 0), kk > 0);
       mma_commit(xf);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)  // O^T = S^T Q+'^T
         mma_bf16_ts(o, sa + kk * 8, sw128_desc(sp + kPkQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
-                    idesc_bf16(128, 64, 0, 0), kk > 0);
+                    idesc_bf16(kM, 64, 0, 0), kk > 0);
       if (!mbar_wait(uready, n & 1)) { failed = true; break; }
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)  // acc^T = U^T K^
         mma_bf16_ts(tmem, ut + kk * 8, sw128_desc(sp + kPkKm + kk * 2048, 8192, 1024),
-                    idesc_bf16(128, 128, 0, 1), kk > 0);
+                    idesc_bf16(kM, 128, 0, 1), kk > 0);
       mma_commit(accf);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)  // O^T += U^T M^T
         mma_bf16_ts(o, ut + kk * 8, sw128_desc(sp + kPkM + kk * 32, 16, 1024),
-                    idesc_bf16(128, 64, 0, 0), 1);
+                    idesc_bf16(kM, 64, 0, 0), 1);
       mma_commit(of0 + 8 * b);
       mma_commit(empty0 + 8 * st);
     }
@@ -1559,10 +1734,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) coop_abort(a);
     return;
   }
-  if ((int)blockIdx.x < a.units)
-    coop_chain(smem, a, blockIdx.x);
-  else
+  if ((int)blockIdx.x < a.units * a.split) {
+    if (a.split == 2)
+      coop_chain<true>(smem, a, blockIdx.x % a.units, blockIdx.x / a.units);
+    else
+      coop_chain<false>(smem, a, blockIdx.x, 0);
+  } else {
     coop_producer(smem, &tm_q, &tm_k, &tm_v, &tm_g, a);
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1643,8 +1822,9 @@ cudaError_t launch_dv(const PrefillPlan &p, const CUtensorMap &mq, const CUtenso
 }
 
 // Grid of the cooperative kernel on the current device (0 when it cannot run
-// there: no cooperative launch, or fewer than 16 producer CTAs would remain).
-int coop_grid(int units) {
+// there: no cooperative launch, or fewer than 16 producer CTAs would remain
+// beside `chains` chain CTAs).
+int coop_grid(int chains) {
   if (set_smem_limit_once(reinterpret_cast<const void *>(coop_kernel), kCoopSmem) != cudaSuccess)
     return 0;
   int dev = 0, sms = 0, coop = 0, per_sm = 0;
@@ -1655,10 +1835,22 @@ int coop_grid(int units) {
           cudaSuccess)
     return 0;
   const int grid = sms * per_sm;
-  return grid >= units + 16 ? grid : 0;
+  return grid >= chains + 16 ? grid : 0;
 }
 
-cudaError_t launch_coop(const PrefillPlan &p, int grid, const CUtensorMap &mq,
+// Chunks per cycle the cooperative grid sustains with `split` chain CTAs per
+// pair: its producers prepare a chunk each in about kProducerCycles, a chain
+// CTA takes kChainCycles (whole columns) or kHalfChainCycles (column halves)
+// per chunk of its pair, and the slower side sets the pace (cycle counts
+// measured on GB300).
+constexpr double kProducerCycles = 15000, kChainCycles = 2900, kHalfChainCycles = 1900;
+double coop_rate(int grid, int units, int split) {
+  const double producers = grid - units * split;
+  return fmin(producers / kProducerCycles,
+              units / (split == 2 ? kHalfChainCycles : kChainCycles));
+}
+
+cudaError_t launch_coop(const PrefillPlan &p, int grid, int split, const CUtensorMap &mq,
                         const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mg) {
   CoopArgs a;
   a.c.beta = static_cast<const __nv_bfloat16 *>(p.beta);
@@ -1678,6 +1870,7 @@ cudaError_t launch_coop(const PrefillPlan &p, int grid, const CUtensorMap &mq,
   a.c.epoch = p.epoch;
   a.c.snap_tma = 0;  // the chain CTAs store snapshots directly (coalesced columns)
   a.units = p.B * p.H;
+  a.split = split;
   a.ring = p.coop_ring;
   a.ready = p.coop_flags;
   a.consumed = p.coop_flags + (size_t)a.units * kCoopRing;
@@ -1701,6 +1894,10 @@ bool coop_supported(const PrefillPlan &p) {
          (int64_t)p.B * p.H <= kCoopMaxUnits && coop_grid(p.B * p.H) > 0;
 }
 
+bool coop_halves_supported(const PrefillPlan &p) {
+  return coop_supported(p) && coop_grid(2 * p.B * p.H) > 0;
+}
+
 cudaError_t launch_chunked_prefill(const PrefillPlan &p, int mode) {
   CUtensorMap mq, mk, mv, mg;
   const uint64_t T = (uint64_t)p.T_total;
@@ -1709,8 +1906,14 @@ cudaError_t launch_chunked_prefill(const PrefillPlan &p, int mode) {
     return cudaErrorInvalidValue;
   // cooperative producer/chain grid when few (sequence, head) pairs would
   // leave most SMs idle; otherwise one CTA per (sequence, head, dv block)
-  if (mode == kChunkCoop || (mode == kChunkAuto && coop_supported(p)))
-    return launch_coop(p, coop_grid(p.B * p.H), mq, mk, mv, mg);
+  if (mode == kChunkCoop) return launch_coop(p, coop_grid(p.B * p.H), 1, mq, mk, mv, mg);
+  if (mode == kChunkCoopHalves) return launch_coop(p, coop_grid(2 * p.B * p.H), 2, mq, mk, mv, mg);
+  if (mode == kChunkAuto && coop_supported(p)) {
+    // column halves when their faster chains outweigh the producers they take
+    const int units = p.B * p.H, g1 = coop_grid(units), g2 = coop_grid(2 * units);
+    const bool halves = g2 > 0 && coop_rate(g2, units, 2) > coop_rate(g1, units, 1);
+    return launch_coop(p, halves ? g2 : g1, halves ? 2 : 1, mq, mk, mv, mg);
+  }
   // Two 64-column dv blocks per (sequence, head) only while they all fit in
   // one wave (one CTA per SM): a 64-column CTA is about 13% faster than a
   // 128-column one on the same chunks, so a second wave costs more than the

@@ -14,7 +14,8 @@
 //                            kernel then recomputes the unit in the same call
 //   when B*H <= kCoopMaxUnits, the cooperative prefill's section:
 //   [.., +256)               uint32 ticket, abort word, longest sequence in chunks
-//   [.., +align(B*H*R*16))   u64 ready[B*H][R], consumed[B*H][R] flags (R = kCoopRing)
+//   [.., +align(B*H*R*24))   u64 ready[B*H][R] and consumed[2][B*H][R] flags (R =
+//                            kCoopRing; one consumed flag per chain CTA of a pair)
 //   [.., +B*H*R*74752)       package ring, R chunk packages per (sequence, head)
 #pragma once
 
@@ -73,7 +74,7 @@ struct WorkspaceLayout {
     coop_units = (B * H <= kCoopMaxUnits) ? B * H : 0;
     // header (ticket, abort, max chunks) | ready[u][ring] | consumed[u][ring] | ring
     coop_flags_off = coop_off + 256;
-    coop_ring_off = coop_flags_off + align256((size_t)coop_units * kCoopRing * 16);
+    coop_ring_off = coop_flags_off + align256((size_t)coop_units * kCoopRing * 24);
     total = coop_units ? coop_ring_off + (size_t)coop_units * kCoopRing * kCoopPkgBytes
                        : coop_off;
   }
@@ -197,12 +198,15 @@ cudaError_t launch_recurrent_decode(const DecodePlan &p);
 cudaError_t launch_decode128(const DecodePlan &p);
 // The chunked tensor-core prefill: whether it applies to these shapes, whether
 // its cooperative mode can run, and the launch (mode: which variant).
-enum ChunkMode { kChunkAuto = 0, kChunkPerState = 1, kChunkCoop = 2 };
+enum ChunkMode { kChunkAuto = 0, kChunkPerState = 1, kChunkCoop = 2, kChunkCoopHalves = 3 };
 bool chunked_supported(const PrefillPlan &p);
 // cudaFuncSetAttribute(func, MaxDynamicSharedMemorySize, bytes) once per
 // (function, device) in this process (thread-safe)
 cudaError_t set_smem_limit_once(const void *func, int bytes);
 bool coop_supported(const PrefillPlan &p);
+// the cooperative mode with two chain CTAs per (sequence, head), one per half
+// of the value columns
+bool coop_halves_supported(const PrefillPlan &p);
 cudaError_t launch_chunked_prefill(const PrefillPlan &p, int mode);
 
 }  // namespace kda

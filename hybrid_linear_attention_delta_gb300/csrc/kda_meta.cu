@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kMetaThreads) meta_kernel(PrefillPlan p) {
   // chunks; ready / consumed flags cleared (the workspace may have held other
   // data at their place in a call with other sizes)
   if (p.coop_hdr) {
-    const int nflags = 2 * p.B * p.H * kCoopRing;
+    const int nflags = 3 * p.B * p.H * kCoopRing;  // ready, consumed x 2
     for (int i = tid; i < nflags; i += kMetaThreads) p.coop_flags[i] = 0ull;
     int mx = 0;
     for (int b = tid; b < B; b += kMetaThreads) {

@@ -67,10 +67,14 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
  * supported shape).  The chunked prefill has two variants: one CTA per
  * (sequence, head, dv block), and, when a batch has at most 64 (sequence,
  * head) pairs with dv = 128 and the workspace was sized for it, a cooperative
- * grid in which the other SMs prepare chunks for the per-pair CTAs.  CHUNKED
- * lets the library choose the variant; CHUNKED_PER_STATE and CHUNKED_COOP
- * force one.  A forced choice that does not apply returns
- * KDA_ERR_UNSUPPORTED.
+ * grid in which the other SMs prepare chunks for the per-pair CTAs.  The
+ * cooperative grid carries each pair's state in one CTA, or in two that hold
+ * one half of the value columns each (faster per chunk, at the cost of a
+ * producer SM per pair: the library takes the halves when that raises the
+ * grid's sustained chunk rate, i.e. for the few pairs of long single
+ * sequences).  CHUNKED lets the library choose; CHUNKED_PER_STATE,
+ * CHUNKED_COOP (one CTA per pair) and CHUNKED_COOP_HALVES (two) force one.
+ * A forced choice that does not apply returns KDA_ERR_UNSUPPORTED.
  *
  * The chunked algorithm scales its operands by exp(+-(G_r - a)), G_r the
  * in-chunk cumulative log-decay and a its value at mid-chunk, which stays
@@ -84,7 +88,8 @@ typedef enum {
   KDA_ALGO_RECURRENT = 1,
   KDA_ALGO_CHUNKED = 2,
   KDA_ALGO_CHUNKED_PER_STATE = 3,
-  KDA_ALGO_CHUNKED_COOP = 4
+  KDA_ALGO_CHUNKED_COOP = 4,
+  KDA_ALGO_CHUNKED_COOP_HALVES = 5
 } kda_algo;
 
 typedef struct {

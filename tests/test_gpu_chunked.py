@@ -16,7 +16,8 @@ pytestmark = pytest.mark.gpu
 CH = kda.KDA_ALGO_CHUNKED
 PER = kda.KDA_ALGO_CHUNKED_PER_STATE
 COOP = kda.KDA_ALGO_CHUNKED_COOP
-MODES = pytest.mark.parametrize("mode", [PER, COOP], ids=["per_state", "coop"])
+HALVES = kda.KDA_ALGO_CHUNKED_COOP_HALVES
+MODES = pytest.mark.parametrize("mode", [PER, COOP, HALVES], ids=["per_state", "coop", "halves"])
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -156,8 +157,11 @@ def test_auto_selects_chunked_for_bf16_128():
     o_auto, _, _, _ = gpu_prefill(b, 0)
     o_ch, _, _, _ = gpu_prefill(b, 0, algo=CH)
     o_coop, _, _, _ = gpu_prefill(b, 0, algo=COOP)
+    o_half, _, _, _ = gpu_prefill(b, 0, algo=HALVES)
     assert torch.equal(o_auto.cpu(), o_ch.cpu())
-    assert torch.equal(o_auto.cpu(), o_coop.cpu())  # few (sequence, head) pairs: cooperative
+    # few (sequence, head) pairs: cooperative, here with two chain CTAs per pair
+    assert torch.equal(o_auto.cpu(), o_half.cpu())
+    assert rel(o_half, o_coop.float().cpu().numpy()) <= TOL["bf16"]
 
 
 def test_coop_and_per_state_agree_with_resume():
@@ -168,20 +172,32 @@ def test_coop_and_per_state_agree_with_resume():
     b = _case(lens, 8, 8, [[5, 0], [-1, 1], [6, 2]])
     o1, p1, s1, st1 = gpu_prefill(b, 128, algo=PER)
     o2, p2, s2, st2 = gpu_prefill(b, 128, algo=COOP)
-    assert st1 == (0, 0) and st2 == (0, 0)
-    assert rel(o2, o1.float().cpu().numpy()) <= TOL["bf16"]
-    assert rel(s2, s1.cpu().numpy()) <= TOL["bf16"]
-    assert rel(p2[:3], p1[:3].cpu().numpy()) <= TOL["bf16"]
-    _check(b, 128, o2, p2, s2)
+    o3, p3, s3, st3 = gpu_prefill(b, 128, algo=HALVES)
+    assert st1 == (0, 0) and st2 == (0, 0) and st3 == (0, 0)
+    for o, p, sn in ((o2, p2, s2), (o3, p3, s3)):
+        assert rel(o, o1.float().cpu().numpy()) <= TOL["bf16"]
+        assert rel(sn, s1.cpu().numpy()) <= TOL["bf16"]
+        assert rel(p[:3], p1[:3].cpu().numpy()) <= TOL["bf16"]
+        _check(b, 128, o, p, sn)
 
 
 def test_coop_refused_for_many_pairs():
     """More than 64 (sequence, head) pairs: the cooperative variant does not
     apply and forcing it is refused up front."""
     b = _case([64] * 5, 16, 6, [[-1, i] for i in range(5)])
-    with pytest.raises(kda.KdaError) as e:
-        gpu_prefill(b, 0, algo=COOP)
-    assert e.value.status == kda.KDA_ERR_UNSUPPORTED
+    for algo in (COOP, HALVES):
+        with pytest.raises(kda.KdaError) as e:
+            gpu_prefill(b, 0, algo=algo)
+        assert e.value.status == kda.KDA_ERR_UNSUPPORTED
+
+
+def test_halves_with_most_pairs():
+    """64 pairs, the most the cooperative grid serves, with two chain CTAs
+    each: 128 chain CTAs and the remaining SMs as producers."""
+    b = _case([64, 130, 1, 200], 16, 5, [[-1, 0], [4, 1], [-1, 2], [3, 3]])
+    out, pool, snaps, st = gpu_prefill(b, 64, algo=HALVES)
+    assert st == (0, 0)
+    _check(b, 64, out, pool, snaps)
 
 
 # ------------------------------------------------------------ full-size workloads

@@ -22,6 +22,7 @@ from kda_cases import TOL, assert_untouched, rel, worst_state, worst_unit
 pytestmark = pytest.mark.gpu
 PER = kda.KDA_ALGO_CHUNKED_PER_STATE
 COOP = kda.KDA_ALGO_CHUNKED_COOP
+HALVES = kda.KDA_ALGO_CHUNKED_COOP_HALVES
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -76,9 +77,9 @@ def _touched(slots):
     return sorted(set(int(s) for s in slots[:, 1].tolist()))
 
 
-@pytest.mark.parametrize("algo,act", [(PER, "none"), (COOP, "none"), (PER, "silu"),
-                                      (COOP, "silu")], ids=["per_state", "coop", "per_state_silu",
-                                                            "coop_silu"])
+@pytest.mark.parametrize("algo,act", [(PER, "none"), (COOP, "none"), (HALVES, "none"),
+                                      (PER, "silu"), (COOP, "silu")],
+                         ids=["per_state", "coop", "halves", "per_state_silu", "coop_silu"])
 def test_fused_prefill_matches_oracle(algo, act):
     """A varlen batch with ragged tails, a short sequence (shorter than the
     convolution), resumed and fresh sequences, one extended in place: outputs,

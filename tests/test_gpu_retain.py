@@ -63,6 +63,7 @@ CASES = [
     (kda.KDA_ALGO_RECURRENT, "f32", 32, 3, 16),
     (kda.KDA_ALGO_CHUNKED_PER_STATE, "bf16", 128, 2, 64),
     (kda.KDA_ALGO_CHUNKED_COOP, "bf16", 128, 2, 64),
+    (kda.KDA_ALGO_CHUNKED_COOP_HALVES, "bf16", 128, 2, 64),
     (kda.KDA_ALGO_CHUNKED_PER_STATE, "bf16", 64, 2, 128),   # dk = 128, dv = 64 below
 ]
 
