@@ -901,7 +901,7 @@ constexpr uint32_t kPkM = 65536;    // M [64 tok][64 tok] bf16, K-major, 8 KiB
 constexpr uint32_t kPkDec = 73728;  // f32 e^{G_C}[128]
 static_assert(kPkDec + 512 <= kCoopPkgBytes && kCoopPkgBytes % 1024 == 0, "package layout");
 // a package is fetched as kPkPieces bulk copies of kPkPiece bytes (8 measured
-// 0.3-0.6% faster than 4 in a same-box A/B)
+// 0.3-0.6% faster than 4, measured back to back on one GPU)
 constexpr uint32_t kPkPieces = 8, kPkPiece = (uint32_t)kCoopPkgBytes / kPkPieces;
 static_assert(kPkPiece % 16 == 0 && kPkPiece * kPkPieces == kCoopPkgBytes, "bulk copy pieces");
 // chain CTA shared memory: three package stages (a package copy from L2
@@ -1268,11 +1268,12 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
 //     (commit: X ready) and O^T = S^T Q+'^T (it runs while the state warps
 //     form U^T); once they stored U^T = U~^T - X^T, acc^T = U^T K^ (commit:
 //     acc ready) and O^T += U^T M^T (commit: outputs ready, stage free).
-//     (Same-box A/B on the 2^20-token prefill: 23.2 ms in this order, 24.6 ms
+//     (Back to back on one GPU, 2^20-token prefill: 23.2 ms in this order, 24.6 ms
 //     with acc^T ahead of O^T = S^T Q+'^T.)
-//   warp 5, one lane (loader): waits until package n is in the ring and its
-//     stage n % 3 is free, and requests it with bulk copies; the next
-//     package's ready flag is read (acquire) while this one is in flight.
+//   warps 5-7, one lane each (loaders): warp 5 + k waits until package n =
+//     k (mod 3) is in the ring and stage k is free, and requests it with bulk
+//     copies; its next package's ready flag is read (acquire) while this one
+//     is in flight.
 // TMEM columns: acc^T [0, 128); O^T[b] [128 + 64 b, +64); S^T[b] as bf16
 // pairs [256 + 64 b, +64); X^T [384, 448); U^T as bf16 pairs [448, 480).
 // Every wait is bounded; a role that gives up raises the abort word and
@@ -1684,16 +1685,21 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u, int hv) {
       mma_commit(drain);
       if (!mbar_wait(drain, 0)) failed = true;
     }
-  } else if (warp == 5 && lane == 0) {
+  } else if (warp >= 5 && lane == 0) {
+    // one loader per package stage: warp 5 + k requests the chunks n = k (mod
+    // 3).  A loader's acquire read of its next ready flag stalls it for about
+    // the length of a chunk step, so a single loader serialised the chain
+    // (2^20-token prefill, measured back to back on one GPU: 21.8 ms with one
+    // loader, 19.4 with two; on another GPU 21.1 with two, 19.6 with three).
+    // The ready flag of the loader's next package is read (acquire) as soon
+    // as this one's copy is requested, so that L2 round trip overlaps the
+    // wait for the stage.
+    const int k = warp - 5, st = k;
     const unsigned long long *ready = a.ready + u * kCoopRing;
     const uint8_t *ring_u = a.ring + (size_t)u * kCoopRing * kCoopPkgBytes;
-    // The ready flag of the next package is read (acquire) as soon as this
-    // one's copy is requested: that L2 round trip, often to the other die,
-    // then overlaps the wait for the next stage.
-    unsigned long long seen = N > 0 ? ld_acquire_u64(ready) : 0ull;
-    int issued = -1;  // last chunk whose copy was requested
-    for (int n = 0; n < N; ++n) {
-      const int st = n % kChStages;
+    unsigned long long seen = N > k ? ld_acquire_u64(ready + k) : 0ull;
+    int issued = -1;  // last chunk whose copy this loader requested
+    for (int n = k; n < N; n += kChStages) {
       const unsigned long long want = coop_tag(a.epoch, n);
       if (seen < want && !coop_flag_wait(ready + n % kCoopRing, want, a.hdr + 1)) {
         failed = true;
@@ -1709,12 +1715,11 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u, int hv) {
       mbar_expect_tx(bar, (uint32_t)kCoopPkgBytes);
       for (uint32_t q = 0; q < kPkPieces; ++q) bulk_g2s(dst + q * kPkPiece, src + q * kPkPiece, kPkPiece, bar);
       issued = n;
-      if (n + 1 < N) seen = ld_acquire_u64(ready + (n + 1) % kCoopRing);
+      if (n + kChStages < N) seen = ld_acquire_u64(ready + (n + kChStages) % kCoopRing);
     }
-    // copies still writing this CTA's shared memory finish before it exits
-    // (the last copy into each stage: earlier ones landed before it was reused)
-    for (int c = issued - kChStages + 1; c <= issued; ++c)
-      if (c >= 0) mbar_wait(full0 + 8 * (c % kChStages), (c / kChStages) & 1);
+    // its last copy lands before the CTA exits (earlier ones landed before
+    // their stage was reused)
+    if (issued >= 0) mbar_wait(full0 + 8 * st, (issued / kChStages) & 1);
   }
   if (failed) coop_abort(a);
   tc_fence_before();
@@ -1918,7 +1923,7 @@ cudaError_t launch_chunked_prefill(const PrefillPlan &p, int mode) {
   // one wave (one CTA per SM): a 64-column CTA is about 13% faster than a
   // 128-column one on the same chunks, so a second wave costs more than the
   // narrower blocks gain (3 x 32768 tokens x 32 heads: 6.78 ms with 192
-  // narrow CTAs, 3.90 ms with 96 wide ones, same box).
+  // narrow CTAs, 3.90 ms with 96 wide ones, back to back on one GPU).
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)

@@ -54,8 +54,10 @@ constexpr int kClaimsPerState = 4;  // one claim word per (slot, head, column bl
 // packages handed from producer CTAs to the pair's state-carrying CTA.
 constexpr int kCoopMaxUnits = 64;      // (sequence, head) pairs it serves at most
 // packages in flight per pair: 6 measured 1% faster than 8 and 8% faster than 16 on
-// the 8k-token prefill (same box; a deeper ring lets the producers run ahead of all
-// pairs together, and its packages go cold in L2)
+// the 8k-token prefill with one loader per chain CTA (back to back on one GPU; a
+// deeper ring lets the producers run ahead of all pairs together, and its packages
+// go cold in L2); with a loader per stage, 12 and 24 gained nothing on the
+// 2^20-token prefill
 constexpr int kCoopRing = 6;
 constexpr size_t kCoopPkgBytes = 74752;
 
