@@ -66,8 +66,8 @@ struct Layout {
   static constexpr uint32_t kG = kV + (DV / 64) * 8192;
   static constexpr uint32_t kStage = kG + 16384;
   static constexpr uint32_t kTM = 2 * kStage;          // [T; M]: 128 rows x 64 tokens
-  static constexpr uint32_t kW = kTM + 16384;          // W halves; fp32 L during the solve
-  static constexpr uint32_t kU = kW + 16384;           // U halves; fp32 X during the solve
+  static constexpr uint32_t kW = kTM + 16384;          // W halves
+  static constexpr uint32_t kU = kW + 16384;           // U halves; X_00^T, A_10 during the solve
   static constexpr uint32_t kScr = kU + 16384;         // solve scratch (16 KiB)
   static constexpr uint32_t kS0 = kScr + 16384;        // S0' halves (128 rows each)
   static constexpr uint32_t kMisc = kS0 + (DV / 64) * 16384;
@@ -83,8 +83,9 @@ struct Layout {
   // prep scratch: per 4-row group decay sums f32[16][128], in the T rows of
   // [T; M] (8 KiB; the solve rewrites them and zeroes T's upper blocks)
   static constexpr uint32_t kGpart = kTM;
-  // solve scratch (fp32): L (swizzled 64x64) in the W buffer, X_00^T in the U
-  // buffer; X_11, Y^T and the transposed diagonal blocks of A in kScr
+  // solve scratch (fp32): X_00^T (rows 0..31 of 64 read by its product) and
+  // A_10 in the U buffer; X_11, Y^T (X_11's padding rows) and the transposed
+  // diagonal blocks of A in kScr
   static constexpr uint32_t kXd = kScr;                 // f32[32][32]
   static constexpr uint32_t kYt = kScr + 4096;          // f32[32][32]
   static constexpr uint32_t kLT = kScr + 8192;          // f32[2][32][32]
@@ -125,54 +126,44 @@ __device__ __forceinline__ void st_bf(uint8_t *base, uint32_t off, float x) {
   *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(x);
 }
 
-// 64x64 fp32 matrices in shared memory: row r holds 16 float4 chunks, chunk c
-// stored at position c ^ (r & 15).  A warp writing one row per lane, or
-// reading the same chunk of 16 different rows, touches distinct banks, and any
-// 4 aligned consecutive entries of a row are one float4.
-__device__ __forceinline__ int fidx(int r, int i) {
-  return r * 64 + ((((i >> 2) ^ (r & 15)) << 2) | (i & 3));
-}
-__device__ __forceinline__ float4 ld4(const float *M, int r, int i) {
-  return *reinterpret_cast<const float4 *>(M + fidx(r, i));
-}
-__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
-  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
-}
-
-// A 32 x 32 fp32 matrix stored by rows of 8 float4 chunks, chunk c of row r
-// at position c ^ (r & 7) (rows that differ in their low bits hit different
-// banks).
+// A 32-column fp32 matrix stored by rows of 8 float4 chunks, chunk c of row r
+// at position c ^ (r & 7): the 128-byte swizzled K-major layout of a tf32
+// tensor-core operand (rows that differ in their low bits hit different banks).
 __device__ __forceinline__ int sidx(int r, int i) {
   return r * 32 + ((((i >> 2) ^ (r & 7)) << 2) | (i & 3));
 }
-__device__ __forceinline__ float4 ld4s(const float *M, int r, int i) {
-  return *reinterpret_cast<const float4 *>(M + sidx(r, i));
-}
 
-// T = (I + A)^{-1} Diag(beta) for the 64x64 strictly lower A held in L
-// (fidx layout, fp32, zero on and above the diagonal).  X = (I + A)^{-1} is
-// built from 32 x 32 blocks:
+// T = (I + A)^{-1} Diag(beta) for the 64x64 strictly lower A.  X = (I + A)^{-1}
+// is built from 32 x 32 blocks:
 //  * the diagonal blocks X_00, X_11 by forward substitution, each column
 //    shared by two lanes of a warp (rows 0..15 and 16..31; threads 128..255,
 //    so that thread 0 can issue tensor-core work just before the solve);
 //  * the block below them, X_10 = -X_11 (A_10 X_00), as two 32 x 32 x 32
-//    products, each thread owning rows {p, p + 16} x columns {q, q + 16}
-//    (p = tid / 16, q = tid % 16).
-// Scratch: X_00^T in XT (fidx rows 0..31), X_11 row-major in Xd and
-// Y^T = (A_10 X_00)^T in YT (sidx layout, 4 KiB each).  LT holds the two
-// diagonal blocks of A transposed (LT[b][m][i] = A[32b + i][32b + m],
-// written by extract_am), so the substitution runs column by column: once
-// x[m] is known it is folded into the running sums of every later row, and
-// x[m + 1] is one multiply-add away.  T is written as bf16
+//    products on the tensor cores in tf32 (fp32 accumulation; the operands'
+//    11-bit significands keep their rounding under the bf16 rounding T then
+//    takes): Y^T = X_00^T A_10^T, then X_10 = -X_11 Y, each 4 MMAs of M = 64
+//    (rows 32..63 of A are padding whose results are not read) into TMEM
+//    columns [0, 32) and [32, 64), which no chunk phase holds during the solve.
+// Operands, fp32 rows of 32 in the 128-byte swizzled K-major layout (sidx):
+// X_00^T at XT (64 rows read, 32 written), A_10 at A10 (written by
+// extract_am), X_11 at Xd followed by Y^T at YT (X_11's padding rows are
+// Y^T's).  LT holds the two diagonal blocks of A transposed (LT[b][m][i] =
+// A[32b + i][32b + m], written by extract_am), so the substitution runs column
+// by column: once x[m] is known it is folded into the running sums of every
+// later row, and x[m + 1] is one multiply-add away.  T is written as bf16
 // into rows 0..63 of the K-major [T; M] operand at tm; the threads without a
 // diagonal column (0..127) zero its upper block (the rows also hold the decay
 // prefix scratch of the chunk's preparation) and then run side(tid), work of
-// the caller that does not touch the solve's buffers.  Ends with T fenced
-// for the tensor cores and a barrier.
+// the caller that does not touch the solve's buffers.  bar / phase: the
+// chunk's MMA barrier and the parity of its next completion (advanced twice).
+// Ends with T fenced for the tensor cores and a barrier; false when a wait
+// gave up (pending then says whether an MMA is still in flight).
 template <class Side>
-__device__ __forceinline__ void solve_T(const float *L, const float *LT, float *XT, float *Xd,
-                                        float *YT, const float *beta, uint8_t *tm, int tid,
+__device__ __forceinline__ bool solve_T(const float *LT, float *XT, const float *A10, float *Xd,
+                                        float *YT, const float *beta, uint8_t *tm, uint32_t tmem,
+                                        uint32_t bar, uint32_t &phase, bool &pending, int tid,
                                         const Side &side) {
+  fence_async_smem();  // A10 (extract_am) for the tensor cores
   if (tid < 128) {  // T's upper block: rows 0..31, 16-byte chunks 4..7
     const int e = tid;
     *reinterpret_cast<uint4 *>(tm + sw128_chunk(e >> 2, 4 + (e & 3))) = make_uint4(0, 0, 0, 0);
@@ -226,10 +217,10 @@ __device__ __forceinline__ void solve_T(const float *L, const float *LT, float *
     }
     const float bj = beta[base + j];
     const int r0 = 16 * half;
-    if (b == 0) {
+    if (b == 0) {  // row j of X_00^T: entries r0 .. r0 + 15
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<float4 *>(XT + fidx(j, r0 + 4 * q)) =
+        *reinterpret_cast<float4 *>(XT + sidx(j, r0 + 4 * q)) =
             make_float4(xo[4 * q], xo[4 * q + 1], xo[4 * q + 2], xo[4 * q + 3]);
     } else {
 #pragma unroll
@@ -238,49 +229,71 @@ __device__ __forceinline__ void solve_T(const float *L, const float *LT, float *
 #pragma unroll
     for (int e = 0; e < 16; ++e) st_bf(tm, sw128_offset(base + r0 + e, base + j), xo[e] * bj);
   }
+  fence_async_smem();  // X_00^T, X_11 for the tensor cores
   __syncthreads();
-  const int pr = tid >> 4, qc = tid & 15;
-  {  // Y = A_10 X_00: Y[i][j] = sum_k A[32 + i][k] X_00^T[j][k]
-    float acc[2][2][4] = {};
+  const int warp = tid >> 5, lane = tid & 31;
+  const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+  const uint32_t xt = smem_u32(XT), a10 = smem_u32(A10), xd = smem_u32(Xd), yt = smem_u32(YT);
+  if (tid == 0) {  // Y^T = X_00^T A_10^T
+    tc_fence_after();
 #pragma unroll
-    for (int k4 = 0; k4 < 8; ++k4) {
-      const float4 a0 = ld4(L, 32 + pr, 4 * k4), a1 = ld4(L, 48 + pr, 4 * k4);
-      const float4 x0 = ld4(XT, qc, 4 * k4), x1 = ld4(XT, qc + 16, 4 * k4);
-      acc[0][0][k4 & 3] = dot4(a0, x0, acc[0][0][k4 & 3]);
-      acc[0][1][k4 & 3] = dot4(a0, x1, acc[0][1][k4 & 3]);
-      acc[1][0][k4 & 3] = dot4(a1, x0, acc[1][0][k4 & 3]);
-      acc[1][1][k4 & 3] = dot4(a1, x1, acc[1][1][k4 & 3]);
-    }
-#pragma unroll
-    for (int ii = 0; ii < 2; ++ii)
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj)
-        YT[sidx(qc + 16 * jj, pr + 16 * ii)] =
-            (acc[ii][jj][0] + acc[ii][jj][1]) + (acc[ii][jj][2] + acc[ii][jj][3]);
+    for (int kk = 0; kk < 4; ++kk)
+      mma_tf32(tmem, sw128_desc(xt + kk * 32, 16, 1024), sw128_desc(a10 + kk * 32, 16, 1024),
+               idesc_tf32(64, 32), kk > 0);
+    mma_commit(bar);
   }
-  __syncthreads();
-  {  // X_10 = -X_11 Y: X_10[i][j] = -sum_k X_11[i][k] Y^T[j][k]
-    float acc[2][2][4] = {};
+  pending = true;
+  if (!cta_wait(bar, phase)) return false;
+  phase ^= 1;
+  pending = false;
+  tc_fence_after();
+  if (warp < 2) {  // M = 64 rows 0..31 sit in lanes 0..15 of quarters 0 and 1
+    float v[32];
+    tmem_ld32(lane_base, v);
+    if (lane < 16) {
+      const int jr = 16 * warp + lane;
 #pragma unroll
-    for (int k4 = 0; k4 < 8; ++k4) {
-      const float4 a0 = ld4s(Xd, pr, 4 * k4), a1 = ld4s(Xd, pr + 16, 4 * k4);
-      const float4 y0 = ld4s(YT, qc, 4 * k4), y1 = ld4s(YT, qc + 16, 4 * k4);
-      acc[0][0][k4 & 3] = dot4(a0, y0, acc[0][0][k4 & 3]);
-      acc[0][1][k4 & 3] = dot4(a0, y1, acc[0][1][k4 & 3]);
-      acc[1][0][k4 & 3] = dot4(a1, y0, acc[1][0][k4 & 3]);
-      acc[1][1][k4 & 3] = dot4(a1, y1, acc[1][1][k4 & 3]);
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<float4 *>(YT + sidx(jr, 4 * q)) =
+            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     }
-#pragma unroll
-    for (int ii = 0; ii < 2; ++ii)
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const int i = pr + 16 * ii, j = qc + 16 * jj;
-        const float v = -((acc[ii][jj][0] + acc[ii][jj][1]) + (acc[ii][jj][2] + acc[ii][jj][3]));
-        st_bf(tm, sw128_offset(32 + i, j), v * beta[j]);
-      }
   }
   fence_async_smem();
+  tc_fence_before();
   __syncthreads();
+  if (tid == 0) {  // X_10 = -X_11 Y
+    tc_fence_after();
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_tf32(tmem + 32, sw128_desc(xd + kk * 32, 16, 1024), sw128_desc(yt + kk * 32, 16, 1024),
+               idesc_tf32(64, 32, 1), kk > 0);
+    mma_commit(bar);
+  }
+  pending = true;
+  if (!cta_wait(bar, phase)) return false;
+  phase ^= 1;
+  pending = false;
+  tc_fence_after();
+  if (warp < 2) {  // rows 32 + i of T, columns 0..31: X_10 Diag(beta)
+    float v[32];
+    tmem_ld32(lane_base + 32, v);
+    if (lane < 16) {
+      const int i = 16 * warp + lane;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float *bc = beta + 8 * c;
+        *reinterpret_cast<uint4 *>(tm + sw128_chunk(32 + i, c)) =
+            make_uint4(pack_bf16x2(v[8 * c] * bc[0], v[8 * c + 1] * bc[1]),
+                       pack_bf16x2(v[8 * c + 2] * bc[2], v[8 * c + 3] * bc[3]),
+                       pack_bf16x2(v[8 * c + 4] * bc[4], v[8 * c + 5] * bc[5]),
+                       pack_bf16x2(v[8 * c + 6] * bc[6], v[8 * c + 7] * bc[7]));
+      }
+    }
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  return true;
 }
 
 // ------------------------------------------------------------------ chunk phases
@@ -398,30 +411,34 @@ __device__ __forceinline__ void issue_mma1(uint32_t d, uint32_t sb) {
              idesc_bf16(128, 64, 0, 0), kk > 0);
 }
 
-// A (rows 0..63 of the MMA1 result at taddr) into the fp32 system L (fidx
-// layout, Diag(beta) strict_lower, zero elsewhere), and its two diagonal
-// 32 x 32 blocks transposed into LT (LT[b][m][i] = A[32b + i][32b + m]);
-// M = lower_incl(Q+ K-^T) (rows 64..127) as bf16 into rows 64..127 of [T; M]
-// at tm.
+// A = Diag(beta) strict_lower(rows 0..63 of the MMA1 result at taddr): its
+// two diagonal 32 x 32 blocks transposed into LT (LT[b][m][i] = A[32b + i][32b
+// + m]) and the block below them, A_10, as fp32 rows of 32 in the 128-byte
+// swizzled K-major layout at A10 (the solve's tensor-core operand); M =
+// lower_incl(Q+ K-^T) (rows 64..127) as bf16 into rows 64..127 of [T; M] at tm.
 __device__ __forceinline__ void extract_am(uint32_t taddr, int quarter, int colhalf, int lane,
-                                           const float *s_beta, float *Lm, float *LT, uint32_t tm) {
-  float v[32];
-  tmem_ld32(taddr + colhalf * 32, v);
+                                           const float *s_beta, float *A10, float *LT, uint32_t tm) {
   const int rr = quarter * 32 + lane;
   if (quarter < 2) {
+    if (quarter < colhalf) return;  // above the diagonal blocks: zero, not needed
+    float v[32];
+    tmem_ld32(taddr + colhalf * 32, v);
     const float br = s_beta[rr];
     float a[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) a[e] = colhalf * 32 + e < rr ? br * v[e] : 0.f;
-#pragma unroll
-    for (int q4 = 0; q4 < 8; ++q4)
-      *reinterpret_cast<float4 *>(Lm + fidx(rr, colhalf * 32 + q4 * 4)) =
-          make_float4(a[q4 * 4], a[q4 * 4 + 1], a[q4 * 4 + 2], a[q4 * 4 + 3]);
     if (quarter == colhalf) {  // a diagonal block: lane = row within it
 #pragma unroll
       for (int e = 0; e < 32; ++e) LT[quarter * 1024 + e * 32 + lane] = a[e];
+    } else {  // A_10: row lane
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4)
+        *reinterpret_cast<float4 *>(A10 + sidx(lane, 4 * q4)) =
+            make_float4(a[q4 * 4], a[q4 * 4 + 1], a[q4 * 4 + 2], a[q4 * 4 + 3]);
     }
   } else {
+    float v[32];
+    tmem_ld32(taddr + colhalf * 32, v);
     const int r = rr - 64;
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
@@ -653,17 +670,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_async_smem();
     }
-    // the previous chunk's outputs were stored from the W buffer, which the
-    // system L overwrites next
+    // the previous chunk's outputs were stored from the W buffer, which this
+    // chunk's W overwrites after MMA2
     if (tid == 0) bulk_wait_read<0>();
     if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
     mma_phase ^= 1;
     mma_pending = false;
     tc_fence_after();
 
-    // A (rows 0..63) into the fp32 system; M (rows 64..127) into [T; M]
-    float *Lm = reinterpret_cast<float *>(smem + Ly::kW);
-    extract_am(lane_base + 256, quarter, colhalf, lane, s_beta, Lm,
+    // A (rows 0..63) into the solve's operands; M (rows 64..127) into [T; M]
+    float *A10 = reinterpret_cast<float *>(smem + Ly::kU + 8192);
+    extract_am(lane_base + 256, quarter, colhalf, lane, s_beta, A10,
                reinterpret_cast<float *>(smem + Ly::kLT), sbase + Ly::kTM);
     tc_fence_before();
     __syncthreads();
@@ -685,9 +702,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto next_tiles = [&](int e) {
       if (e == 0 && n + 1 < nchunks) issue_tma(n + 1);
     };
-    solve_T(Lm, reinterpret_cast<const float *>(smem + Ly::kLT), reinterpret_cast<float *>(smem + Ly::kU),
-            reinterpret_cast<float *>(smem + Ly::kXd),
-            reinterpret_cast<float *>(smem + Ly::kYt), s_beta, smem + Ly::kTM, tid, next_tiles);
+    if (!solve_T(reinterpret_cast<const float *>(smem + Ly::kLT),
+                 reinterpret_cast<float *>(smem + Ly::kU), A10,
+                 reinterpret_cast<float *>(smem + Ly::kXd), reinterpret_cast<float *>(smem + Ly::kYt),
+                 s_beta, smem + Ly::kTM, tmem, bar_mma, mma_phase, mma_pending, tid, next_tiles)) {
+      aborted = true;
+      break;
+    }
     if (n + 1 < nchunks) {
       tma_pending[(n + 1) & 1] = true;
       tma_parity[(n + 1) & 1] = ((n + 1) >> 1) & 1;
@@ -1107,8 +1128,8 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       s_ea[tid] = expf(s_anc[tid]);
       s_cke[tid] = expf(s_tot[tid] - s_anc[tid]);
     }
-    float *Lm = reinterpret_cast<float *>(smem + Ly::kW);
-    extract_am(lane_base + 256, quarter, colhalf, lane, s_beta, Lm,
+    float *A10 = reinterpret_cast<float *>(smem + Ly::kU + 8192);
+    extract_am(lane_base + 256, quarter, colhalf, lane, s_beta, A10,
                reinterpret_cast<float *>(smem + Ly::kLT), sbase + Ly::kTM);
     tc_fence_before();
     __syncthreads();
@@ -1142,9 +1163,13 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
                      pack_bf16x2(bf16lo(w.w) * f1.z, bf16hi(w.w) * f1.w));
       }
     };
-    solve_T(Lm, reinterpret_cast<const float *>(smem + Ly::kLT), reinterpret_cast<float *>(smem + Ly::kU),
-            reinterpret_cast<float *>(smem + Ly::kXd),
-            reinterpret_cast<float *>(smem + Ly::kYt), s_beta, smem + Ly::kTM, tid, stage_kq);
+    if (!solve_T(reinterpret_cast<const float *>(smem + Ly::kLT),
+                 reinterpret_cast<float *>(smem + Ly::kU), A10,
+                 reinterpret_cast<float *>(smem + Ly::kXd), reinterpret_cast<float *>(smem + Ly::kYt),
+                 s_beta, smem + Ly::kTM, tmem, bar_mma, mma_phase, mma_pending, tid, stage_kq)) {
+      aborted = true;
+      break;
+    }
     if (tid == 0) {
       issue_mma2_coop<Ly>(tmem, sbase + Ly::kTM, sb);
       mma_commit(bar_mma);

@@ -371,6 +371,28 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
          | ((uint32_t)(M >> 4) << 24);  // M / 16
 }
 
+// kind::tf32: A and B are fp32 containers read as tf32 (both operands TF32,
+// format code 2), D fp32.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, int neg_a = 0) {
+  return (1u << 4)                      // D: f32
+         | (2u << 7)                    // A: tf32
+         | (2u << 10)                   // B: tf32
+         | ((uint32_t)neg_a << 13)      // negate A
+         | ((uint32_t)(N >> 3) << 17)   // N / 8
+         | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+// D[tmem] (+)= A[smem] * B[smem] in tf32, one instruction of K = 8 (32 bytes
+// of a K-major fp32 row, as K = 16 is for bf16).
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem], one instruction of K = 16.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accumulate) {
