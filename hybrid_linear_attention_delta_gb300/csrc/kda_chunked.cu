@@ -1327,7 +1327,8 @@ __device__ bool chain_state_half(uint8_t *smem, const CoopArgs &a, int u, int hv
   const uint32_t sbase = smem_u32(smem);
   const int H = a.c.H, h = u % H, dv = a.c.dv;
   const uint32_t full0 = bars, empty0 = bars + 24, sready0 = bars + 48, accf = bars + 64,
-                 xf = bars + 72, of0 = bars + 80, oe0 = bars + 96, uready = bars + 120;
+                 xf = bars + 72, of0 = bars + 80, oe0 = bars + 96, uready = bars + 120,
+                 sreadyhi0 = bars + 136;
   const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
   const int j0 = 64 * hv + 16 * warp + g;
   float S[2][32];  // S[s][2 r + e]: channel 8 r + 2 q + e of value column j0 + 8 s
@@ -1382,24 +1383,31 @@ __device__ bool chain_state_half(uint8_t *smem, const CoopArgs &a, int u, int hv
 #pragma unroll
       for (int i = 0; i < 32; ++i) d[(int64_t)(8 * (i >> 1) + 2 * q + (i & 1)) * dv + 8 * s] = S[s][i];
   };
-  const int snap_every = a.c.snap_interval > 0 ? a.c.snap_interval / kC : 0;
-  int snap_left = snap_every;
-  int64_t snap_next = m.snap_off;
-  for (int n = 0; n < N; ++n) {
-    const int b = n & 1, st = n % kChStages;
-    {  // bf16(S^T) -> S^T[b]
-      uint32_t r[32];
+  // bf16(S^T) channels [64 p, 64 p + 64) -> S^T buffer buf, then its half-p
+  // barrier: X^T's first four MMAs (K = channels 0..63) start while the second
+  // half of the state is still being updated
+  auto store_st = [&](int buf, int p) {
+    uint32_t r[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        r[2 * i] = pack_bf16x2(S[0][2 * i], S[0][2 * i + 1]);
-        r[2 * i + 1] = pack_bf16x2(S[1][2 * i], S[1][2 * i + 1]);
-      }
-      tmem_st16x128_x16(lane_base + 256 + 64 * b, r);
+    for (int i = 0; i < 8; ++i) {
+      r[2 * i] = pack_bf16x2(S[0][16 * p + 2 * i], S[0][16 * p + 2 * i + 1]);
+      r[2 * i + 1] = pack_bf16x2(S[1][16 * p + 2 * i], S[1][16 * p + 2 * i + 1]);
     }
+    tmem_st16x128_x8(lane_base + 256 + 64 * buf + 32 * p, r);
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(sready0 + 8 * b);
+    if (lane == 0) mbar_arrive((p ? sreadyhi0 : sready0) + 8 * buf);
+  };
+  const int snap_every = a.c.snap_interval > 0 ? a.c.snap_interval / kC : 0;
+  int snap_left = snap_every;
+  int64_t snap_next = m.snap_off;
+  if (N > 0) {
+    store_st(0, 0);
+    store_st(0, 1);
+  }
+  for (int n = 0; n < N; ++n) {
+    const int b = n & 1, st = n % kChStages;
     if (n > 0 && !retire(n - 1, 0)) return false;
     if (!warp_wait(full0 + 8 * st, (n / kChStages) & 1) || !warp_wait(xf, n & 1)) return false;
     tc_fence_after();
@@ -1431,7 +1439,9 @@ __device__ bool chain_state_half(uint8_t *smem, const CoopArgs &a, int u, int hv
     if (n > 0) retire(n - 1, 1);
     if (!warp_wait(accf, n & 1)) return false;
     tc_fence_after();
-    {  // S = Diag(e^{G_C}) S + acc: channels 8 r + 2 q + {0, 1}
+    {  // S = Diag(e^{G_C}) S + acc: channels 8 r + 2 q + {0, 1}, then S^T of the
+       // next chunk into the other buffer (last read by chunk n - 1's MMAs, done
+       // before X^T of chunk n completed), one channel half at a time
       const uint32_t egc = sp + kPkDec + 8 * q;
       uint32_t v[2][32];
       tmem_ld16x256_x8(lane_base, v[0]);
@@ -1440,7 +1450,7 @@ __device__ bool chain_state_half(uint8_t *smem, const CoopArgs &a, int u, int hv
       reg_fence(v[0]);
       reg_fence(v[1]);
 #pragma unroll
-      for (int p = 0; p < 2; ++p)
+      for (int p = 0; p < 2; ++p) {
 #pragma unroll
         for (int rr = 0; rr < 8; ++rr) {
           const int r = 8 * p + rr;
@@ -1450,6 +1460,8 @@ __device__ bool chain_state_half(uint8_t *smem, const CoopArgs &a, int u, int hv
           S[1][2 * r] = fmaf(e.x, S[1][2 * r], __uint_as_float(v[p][4 * rr + 2]));
           S[1][2 * r + 1] = fmaf(e.y, S[1][2 * r + 1], __uint_as_float(v[p][4 * rr + 3]));
         }
+        if (n + 1 < N) store_st(b ^ 1, p);
+      }
     }
     tc_fence_before();
     __syncwarp();
@@ -1494,6 +1506,7 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u, int hv) {
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(sready0 + 8 * s, 4);
+      mbar_init(sready0 + 88 + 8 * s, 4);  // second channel half (column halves)
       mbar_init(of0 + 8 * s, 1);
       mbar_init(oe0 + 8 * s, 4);
     }
@@ -1684,9 +1697,15 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u, int hv) {
       const uint32_t o = tmem + 128 + 64 * b, sa = tmem + 256 + 64 * b, xt = tmem + 384,
                      ut = tmem + 448;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // X^T = S^T W^^T
+      for (int kk = 0; kk < 8; ++kk) {  // X^T = S^T W^^T
+        if (kHalf && kk == 4) {  // column halves store S^T a channel half at a time
+          if (!mbar_wait(sready0 + 88 + 8 * b, (n >> 1) & 1)) { failed = true; break; }
+          tc_fence_after();
+        }
         mma_bf16_ts(xt, sa + kk * 8, sw128_desc(sp + kPkW + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
                     idesc_bf16(kM, 64, 0, 0), kk > 0);
+      }
+      if (failed) break;
       mma_commit(xf);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)  // O^T = S^T Q+'^T
