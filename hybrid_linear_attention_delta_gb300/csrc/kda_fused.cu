@@ -97,7 +97,7 @@ __device__ __forceinline__ void store_quad(float *p, const float (&y)[4]) {
 // history is the three tokens before it; at a sequence start, the sequence's
 // starting convolution state (zeros without one).  Writes q, k, v (the
 // recurrence's inputs) for tokens of sequences the plan accepted.
-constexpr int kConvRun = 32;
+constexpr int kConvRun = 64;
 constexpr int kConvUnits = 2;
 constexpr int kConvThreads = 32 * 3 * kConvUnits;
 constexpr int kConvBatchBytes = 64;  // per lane in flight: 8 bf16 or 4 fp32 tokens
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kConvThreads, 4) conv_prefill_kernel(PrefillPl
 
   // one token: convolution, |q~| or |k~| (a shuffle tree over the warp's
   // active lanes; the others hold 0), scaling, store
-  auto step = [&](const Quad<T> &xq4, int t) {
+  auto step = [&](const Quad<T> &xq4, T *dst) {
     float xv[4], y[4], ss = 0.f;
     unpack_quad(xq4, xv);
 #pragma unroll
@@ -190,18 +190,19 @@ __global__ void __launch_bounds__(kConvThreads, 4) conv_prefill_kernel(PrefillPl
 #pragma unroll
       for (int e = 0; e < 4; ++e) y[e] = part == 0 ? y[e] * scale * qscale : y[e] * scale;
     }
-    if (active && ok) store_quad(y_out + (int64_t)t * row_stride + col, y);
+    if (active && ok) store_quad(dst, y);
   };
 
   // batches inside one sequence issue their loads together; a batch that
   // reaches the run's end or a sequence start goes token by token
   for (int t0 = tb; t0 < te; t0 += kConvBatch) {
     if (t0 + kConvBatch <= te && t0 + kConvBatch <= end) {
+      const int64_t off = (int64_t)t0 * row_stride + col;
       Quad<T> xr[kConvBatch];
 #pragma unroll
-      for (int j = 0; j < kConvBatch; ++j) xr[j] = load_quad(x + (int64_t)(t0 + j) * row_stride + col);
+      for (int j = 0; j < kConvBatch; ++j) xr[j] = load_quad(x + off + j * row_stride);
 #pragma unroll
-      for (int j = 0; j < kConvBatch; ++j) step(xr[j], t0 + j);
+      for (int j = 0; j < kConvBatch; ++j) step(xr[j], y_out + off + j * row_stride);
     } else {
       const int t1 = min(t0 + kConvBatch, te);
 #pragma unroll 1
@@ -215,7 +216,8 @@ __global__ void __launch_bounds__(kConvThreads, 4) conv_prefill_kernel(PrefillPl
           ok = p.meta[b].ok;
           init_hist(t);
         }
-        step(load_quad(x + (int64_t)t * row_stride + col), t);
+        const int64_t off = (int64_t)t * row_stride + col;
+        step(load_quad(x + off), y_out + off);
       }
     }
   }

@@ -231,3 +231,32 @@ def test_fused_decode_full_size_256x32():
     assert rel(pool_d[sl], rpool) <= TOL["bf16"]
     assert worst_state(pool_d[sl], rpool) <= 2 * TOL["bf16"]
     np.testing.assert_array_equal(f["conv_pool"][sl].float().cpu().numpy(), rconv)
+
+
+@pytest.mark.slow
+def test_fused_prefill_8k_full():
+    """The 8k-token workload (B=1, T=8192, H=32, snapshots every 1024) through
+    the fused prefill, the raw inputs drawn as the workload's q, k, v: every
+    output, snapshot and final state against the oracle, and the new
+    convolution state bit for bit."""
+    w = inputs.WORKLOADS["prefill_8k"]
+    b = inputs.make_batch(w)
+    T, H = b.q.shape[:2]
+    ft = inputs.fused_tensors(T, H, w.dk, w.dv, torch.bfloat16, w.index, b.pool.shape[0])
+    tt = {n: getattr(b, n) for n in ("q", "k", "v", "g", "beta")}
+    out, p, cp, snaps, (st, bits) = _run_prefill(b.cu_seqlens, b.init_slots, tt, ft, b.pool,
+                                                  w.snap_interval)
+    assert st == kda.KDA_OK and bits == 0
+    ro, rpool, rconv, rsn = _oracle_prefill(b.cu_seqlens, b.init_slots, tt, ft, b.pool,
+                                            w.snap_interval)
+    touched = _touched(b.init_slots)
+    tol = TOL["bf16"]
+    e = rel(out, ro)
+    print(f"fused prefill 8k: out {e:.2e}")
+    assert e <= tol
+    assert worst_unit(out, ro, b.cu_seqlens.numpy(), H) <= 2 * tol
+    assert rel(p[touched], rpool[touched]) <= tol
+    assert worst_state(p[touched], rpool[touched]) <= 2 * tol
+    assert rel(snaps, rsn) <= tol
+    assert worst_state(snaps, rsn) <= 2 * tol
+    np.testing.assert_array_equal(cp.float().cpu().numpy()[touched], rconv[touched])
