@@ -77,7 +77,7 @@ struct Layout {
   static constexpr uint32_t kTot = kBeta + 256;        // f32[128] G_C (chunk decay)
   static constexpr uint32_t kAnc = kTot + 512;         // f32[128] a (anchor decay)
   static constexpr uint32_t kEa = kAnc + 512;          // f32[128] e^{a} (cooperative producer)
-  static constexpr uint32_t kCke = kEa + 512;          // f32[128] e^{G_C - a} (cooperative producer)
+  static constexpr uint32_t kCke = kEa + 512;          // f32[128] e^{G_C} (cooperative producer)
   static constexpr uint32_t kSeqs = kCke + 512;        // int2[64] (tok0, len) per sequence
   static constexpr uint32_t kBytes = kMisc + kSeqs + 512;
   // prep scratch: per 4-row group decay sums f32[16][128], in the T rows of
@@ -987,6 +987,8 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
   float *s_tot = reinterpret_cast<float *>(misc + Ly::kTot);
   float *s_anc = reinterpret_cast<float *>(misc + Ly::kAnc);
   float *s_ea = reinterpret_cast<float *>(misc + Ly::kEa);
+  // e^{G_C - a}: in the solve scratch, which is free while the first MMA runs
+  float *s_cka = reinterpret_cast<float *>(smem + Ly::kScr);
   float *s_cke = reinterpret_cast<float *>(misc + Ly::kCke);
   float *s_gpart = reinterpret_cast<float *>(smem + Ly::kGpart);
   int2 *s_seq = reinterpret_cast<int2 *>(misc + Ly::kSeqs);  // (tok0, len or 0) per sequence
@@ -1111,37 +1113,34 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       mma_commit(bar_mma);
       raw_ticket = next >= 0 ? (int)atomicAdd(a.hdr, 1u) : total;  // used at MMA2
     }
-    if (tid == kPub) {  // the previous package is complete (its sources are free): publish it
-      bulk_wait<0>();
-      if (pend) {
-        fence_proxy_async_all();
-        st_release_u64(pend_flag, pend_tag);
-        pend = false;
-      }
-    }
-    mma_pending = true;
-    if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
-    mma_phase ^= 1;
-    mma_pending = false;
-    tc_fence_after();
     if (tid < 128) {
       s_ea[tid] = expf(s_anc[tid]);
-      s_cke[tid] = expf(s_tot[tid] - s_anc[tid]);
+      s_cka[tid] = expf(s_tot[tid] - s_anc[tid]);
     }
-    float *A10 = reinterpret_cast<float *>(smem + Ly::kU + 8192);
-    extract_am(lane_base + 256, quarter, colhalf, lane, s_beta, A10,
-               reinterpret_cast<float *>(smem + Ly::kLT), sbase + Ly::kTM);
-    tc_fence_before();
-    __syncthreads();
-    // while threads 128..255 solve for T, threads 0..127 stage the package
-    // operands that need only the prepared tiles: K^ = K- Diag(e^{G_C - a})
-    // into the upper half of the S0 region and Q+' = Q+ Diag(e^{a}) into its
-    // lower half (the previous package's stores finished before MMA1's wait)
-    auto stage_kq = [&](int e0) {
-      for (int e = e0; e < 1024; e += 128) {
+    // While the first MMA runs, every warp but thread kPub's stages K^ = K-
+    // Diag(e^{G_C - a}), which needs only the prepared tiles, into the upper
+    // half of the S0 region.  That warp lets the others start (named barrier
+    // 1) once the previous package's bulk stores have read their sources,
+    // then waits until those stores are complete and publishes the package.
+    constexpr int kStagers = kThreads - 32;
+    if (warp == kPub / 32) {
+      if (tid == kPub) bulk_wait_read<0>();
+      __syncwarp();
+      named_bar_arrive(1, kThreads);
+      if (tid == kPub) {
+        bulk_wait<0>();
+        if (pend) {
+          fence_proxy_async_all();
+          st_release_u64(pend_flag, pend_tag);
+          pend = false;
+        }
+      }
+    } else {
+      named_bar_sync(1, kThreads);
+      for (int e = tid - (warp > kPub / 32 ? 32 : 0); e < 1024; e += kStagers) {
         const int half = e >> 9, r = (e >> 3) & 63, q = e & 7;
         const uint32_t off = r * 128 + q * 16;
-        const float4 *f = reinterpret_cast<const float4 *>(s_cke + half * 64 + 8 * (q ^ (r & 7)));
+        const float4 *f = reinterpret_cast<const float4 *>(s_cka + half * 64 + 8 * (q ^ (r & 7)));
         const float4 f0 = f[0], f1 = f[1];
         const uint4 w = ld_shared_v4(sb + Ly::kG + half * 8192 + off);
         st_shared_v4(sbase + Ly::kS0 + 16384 + half * 8192 + off,
@@ -1150,6 +1149,20 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
                      pack_bf16x2(bf16lo(w.z) * f1.x, bf16hi(w.z) * f1.y),
                      pack_bf16x2(bf16lo(w.w) * f1.z, bf16hi(w.w) * f1.w));
       }
+    }
+    mma_pending = true;
+    if (!cta_wait(bar_mma, mma_phase)) { aborted = true; break; }
+    mma_phase ^= 1;
+    mma_pending = false;
+    tc_fence_after();
+    float *A10 = reinterpret_cast<float *>(smem + Ly::kU + 8192);
+    extract_am(lane_base + 256, quarter, colhalf, lane, s_beta, A10,
+               reinterpret_cast<float *>(smem + Ly::kLT), sbase + Ly::kTM);
+    tc_fence_before();
+    __syncthreads();
+    // while threads 128..255 solve for T, threads 0..127 stage Q+' = Q+
+    // Diag(e^{a}) into the lower half of the S0 region
+    auto stage_q = [&](int e0) {
       for (int e = e0; e < 1024; e += 128) {
         const int half = e >> 9, r = (e >> 3) & 63, q = e & 7;
         const uint32_t off = r * 128 + q * 16;
@@ -1166,7 +1179,7 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     if (!solve_T(reinterpret_cast<const float *>(smem + Ly::kLT),
                  reinterpret_cast<float *>(smem + Ly::kU), A10,
                  reinterpret_cast<float *>(smem + Ly::kXd), reinterpret_cast<float *>(smem + Ly::kYt),
-                 s_beta, smem + Ly::kTM, tmem, bar_mma, mma_phase, mma_pending, tid, stage_kq)) {
+                 s_beta, smem + Ly::kTM, tmem, bar_mma, mma_phase, mma_pending, tid, stage_q)) {
       aborted = true;
       break;
     }
@@ -1191,7 +1204,7 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     // The package is staged in shared memory in its final layout, outside
     // both input stages, then written out with bulk copies: W^ = W Diag(e^{a})
     // in the W buffer, U~^T in the U buffer, K^ and Q+' in the S0 region (staged
-    // during the solve), M where the solve left it and e^{G_C} in the
+    // during the first MMA), M where the solve left it and e^{G_C} in the
     // e^{G_C - a} vector.
     // the chunk two ahead goes to this chunk's stage: its k, v and g tiles are
     // dead now (q is read once more, below), and thread kPub's warp has no

@@ -34,6 +34,17 @@ __device__ __forceinline__ uint32_t sw128_chunk(int row, int c) {
   return (uint32_t)(row * 128 + ((c ^ (row & 7)) << 4));
 }
 
+// ------------------------------------------------------------------ named CTA barriers
+// Barrier id (1..15; 0 is __syncthreads) over count threads, a multiple of 32;
+// whole warps execute these.  named_bar_arrive signals without waiting (its
+// writes are visible after the matching named_bar_sync), named_bar_sync waits.
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
