@@ -1333,8 +1333,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
 // its 16x128b stores of U^T and S^T pack into one bf16 pair (column 4 r + q
 // holds K-positions 8 r + 2 q, 8 r + 2 q + 1), so no value changes thread.
 // Returns false when a wait gave up.
-__device__ bool chain_state_half(uint8_t *smem, const CoopArgs &a, int u, int hv, const SeqMeta &m,
-                                 int N, uint32_t tmem, uint32_t bars) {
+__device__ bool chain_state_half(uint8_t *smem, const CoopArgs &a, const CUtensorMap *tm_o, int u,
+                                 int hv, const SeqMeta &m, int N, uint32_t tmem, uint32_t bars) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, q = lane & 3;
   const uint32_t sbase = smem_u32(smem);
@@ -1358,10 +1358,16 @@ __device__ bool chain_state_half(uint8_t *smem, const CoopArgs &a, int u, int hv
       for (int i = 0; i < 32; ++i) S[s][i] = 0.f;
   }
   // outputs of chunk n, half hf (tokens 32 hf .. 32 hf + 31), from O^T buffer
-  // n & 1 with the 16x64b shape: register r is token 2 r + c of value column
-  // 64 hv + 16 w + orow, so per store the warp writes 16 consecutive outputs
-  // (32 bytes) of each of two tokens
+  // n & 1 with the 16x64b shape: register r is token 2 r + oc of value column
+  // 64 hv + 16 w + orow.  A full half leaves through a TMA store per warp: its
+  // 16 columns x 32 tokens as bf16 rows of 32 bytes (conflict-free 2-byte
+  // shared stores, two tokens per instruction) in 1 KiB of package stage n % 3
+  // that the loaders leave alone (the other column half's rows of U~^T), where
+  // chunk n + 3 writes next once lane 0 saw the stores read it.  A ragged half
+  // is stored element by element (rows past the sequence end belong to the
+  // next sequence).
   const int orow = g + 8 * (lane & 1), oc = (lane >> 1) & 1;
+  const uint32_t obuf = kPkU + 8192u * (1 - hv) + 2048u * warp;
   auto retire = [&](int n, int hf) -> bool {
     const int b = n & 1;
     if (hf == 0 && !warp_wait(of0 + 8 * b, (n >> 1) & 1)) return false;
@@ -1376,13 +1382,24 @@ __device__ bool chain_state_half(uint8_t *smem, const CoopArgs &a, int u, int hv
       if (lane == 0) mbar_arrive(oe0 + 8 * b);
     }
     const int cl = min(kC, m.len - n * kC) - 32 * hf;
-    const int64_t ts = (int64_t)H * dv;
-    __nv_bfloat16 *o = a.c.out + ((int64_t)(m.tok0 + n * kC + 32 * hf + oc) * H + h) * dv +
-                       64 * hv + 16 * warp + orow;
     if (cl >= 32) {
+      const uint32_t buf = (uint32_t)(n % kChStages) * (uint32_t)kCoopPkgBytes + obuf + 1024u * hf;
+      if (lane == 0) bulk_wait_read<4>();  // (chunk n - 3's stores of this buffer)
+      __syncwarp();
 #pragma unroll
-      for (int r = 0; r < 16; ++r) o[2 * r * ts] = __float2bfloat16_rn(__uint_as_float(v[r]));
+      for (int r = 0; r < 16; ++r)
+        *reinterpret_cast<__nv_bfloat16 *>(smem + buf + (2 * r + oc) * 32 + 2 * orow) =
+            __float2bfloat16_rn(__uint_as_float(v[r]));
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tm_o, sbase + buf, h * dv + 64 * hv + 16 * warp, m.tok0 + n * kC + 32 * hf);
+        bulk_commit();
+      }
     } else {
+      const int64_t ts = (int64_t)H * dv;
+      __nv_bfloat16 *o = a.c.out + ((int64_t)(m.tok0 + n * kC + 32 * hf + oc) * H + h) * dv +
+                         64 * hv + 16 * warp + orow;
 #pragma unroll
       for (int r = 0; r < 16; ++r)
         if (2 * r + oc < cl) o[2 * r * ts] = __float2bfloat16_rn(__uint_as_float(v[r]));
@@ -1499,7 +1516,7 @@ __device__ bool chain_state_half(uint8_t *smem, const CoopArgs &a, int u, int hv
 }
 
 template <bool kHalf>
-__device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u, int hv) {
+__device__ void coop_chain(uint8_t *smem, const CoopArgs &a, const CUtensorMap *tm_o, int u, int hv) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_u32(smem);
   const int H = a.c.H, h = u % H, dv = a.c.dv;
@@ -1529,6 +1546,7 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u, int hv) {
     mbar_init(drain, 1);
     fence_mbar_init();
   }
+  if (kHalf && tid == 0) prefetch_tmap(tm_o);
   if (warp == 0) tmem_alloc(bars + 128, 512);
   __syncthreads();
   tc_fence_after();
@@ -1537,7 +1555,8 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u, int hv) {
   bool failed = false;
 
   if (warp < 4 && kHalf) {
-    failed = !chain_state_half(smem, a, u, hv, m, N, tmem, bars);
+    failed = !chain_state_half(smem, a, tm_o, u, hv, m, N, tmem, bars);
+    if (lane == 0) bulk_wait<0>();  // the output stores are complete before the CTA exits
   } else if (warp < 4) {
     const int j = tid;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
@@ -1769,8 +1788,17 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u, int hv) {
       fence_proxy_async_all();  // the package was written by another SM
       const uint8_t *src = ring_u + (size_t)(n % kCoopRing) * kCoopPkgBytes;
       const uint32_t dst = sbase + st * (uint32_t)kCoopPkgBytes, bar = full0 + 8 * st;
-      mbar_expect_tx(bar, (uint32_t)kCoopPkgBytes);
-      for (uint32_t q = 0; q < kPkPieces; ++q) bulk_g2s(dst + q * kPkPiece, src + q * kPkPiece, kPkPiece, bar);
+      if (kHalf) {  // all but the other column half's rows of U~^T (8 KiB pieces, 1 KiB tail)
+        const uint32_t skip = kPkU + 8192u * (1 - hv);
+        mbar_expect_tx(bar, (uint32_t)kCoopPkgBytes - 8192u);
+        for (uint32_t o = 0; o < (uint32_t)kCoopPkgBytes; o += 8192u)
+          if (o != skip)
+            bulk_g2s(dst + o, src + o, min(8192u, (uint32_t)kCoopPkgBytes - o), bar);
+      } else {
+        mbar_expect_tx(bar, (uint32_t)kCoopPkgBytes);
+        for (uint32_t q = 0; q < kPkPieces; ++q)
+          bulk_g2s(dst + q * kPkPiece, src + q * kPkPiece, kPkPiece, bar);
+      }
       issued = n;
       if (n + kChStages < N) seen = ld_acquire_u64(ready + (n + kChStages) % kCoopRing);
     }
@@ -1790,7 +1818,7 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, int u, int hv) {
 __global__ void __launch_bounds__(kThreads, 1)
     coop_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                const CoopArgs a) {
+                const __grid_constant__ CUtensorMap tm_o, const CoopArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023) {  // the swizzled layouts need a 1024-byte aligned base
     if (threadIdx.x == 0) coop_abort(a);
@@ -1798,9 +1826,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if ((int)blockIdx.x < a.units * a.split) {
     if (a.split == 2)
-      coop_chain<true>(smem, a, blockIdx.x % a.units, blockIdx.x / a.units);
+      coop_chain<true>(smem, a, &tm_o, blockIdx.x % a.units, blockIdx.x / a.units);
     else
-      coop_chain<false>(smem, a, blockIdx.x, 0);
+      coop_chain<false>(smem, a, &tm_o, blockIdx.x, 0);
   } else {
     coop_producer(smem, &tm_q, &tm_k, &tm_v, &tm_g, a);
   }
@@ -1830,6 +1858,20 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows)
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 [rows][inner] with unswizzled boxes of 16 columns x 32 rows (one
+// warp's outputs of half a chunk in a cooperative chain CTA)
+bool make_map_o16(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {16, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // fp32 [rows][inner] with 128-byte swizzled boxes of 32 columns x 128 rows
@@ -1938,8 +1980,9 @@ cudaError_t launch_coop(const PrefillPlan &p, int grid, int split, const CUtenso
   a.consumed = p.coop_flags + (size_t)a.units * kCoopRing;
   a.hdr = p.coop_hdr;
   a.epoch = p.epoch;
-  CUtensorMap q = mq, k = mk, v = mv, g = mg;
-  void *args[] = {&q, &k, &v, &g, &a};
+  CUtensorMap q = mq, k = mk, v = mv, g = mg, o;
+  if (!make_map_o16(&o, p.out, (uint64_t)p.H * p.dv, (uint64_t)p.T_total)) return cudaErrorInvalidValue;
+  void *args[] = {&q, &k, &v, &g, &o, &a};
   return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(coop_kernel), dim3(grid),
                                      dim3(kThreads), args, kCoopSmem, p.stream);
 }

@@ -53,12 +53,13 @@ constexpr int kClaimsPerState = 4;  // one claim word per (slot, head, column bl
 // Cooperative prefill (few (sequence, head) pairs): per pair a ring of chunk
 // packages handed from producer CTAs to the pair's state-carrying CTA.
 constexpr int kCoopMaxUnits = 64;      // (sequence, head) pairs it serves at most
-// packages in flight per pair: 6 measured 1% faster than 8 and 8% faster than 16 on
-// the 8k-token prefill with one loader per chain CTA (back to back on one GPU; a
-// deeper ring lets the producers run ahead of all pairs together, and its packages
-// go cold in L2); with a loader per stage, 12 and 24 gained nothing on the
-// 2^20-token prefill
-constexpr int kCoopRing = 6;
+// packages in flight per pair.  With the half chains' outputs leaving through TMA
+// stores, 12 measured 4% faster than 6 on the 2^20-token prefill (20.71 -> 19.85 ms
+// back to back on one GPU; 9 and 24 within 0.1% of 12) and the same on the 8k-token
+// one.  (With one loader per chain CTA, 6 had been 1% faster than 8 and 8% faster
+// than 16 on the 8k-token prefill: a deeper ring lets the producers run ahead of
+// all pairs together, and its packages go cold in L2.)
+constexpr int kCoopRing = 12;
 constexpr size_t kCoopPkgBytes = 74752;
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
