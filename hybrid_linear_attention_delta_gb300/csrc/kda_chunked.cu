@@ -360,15 +360,20 @@ __device__ __forceinline__ bool prep_chunk(uint32_t sb, int cl, float beta_r, fl
     s_tot[tid] = run;                  // G_C: decay through the chunk
   }
   __syncthreads();
-  float pre[8];  // G before this thread's rows, minus the anchor
+  // (G - a) log2(e) before this thread's rows: each scale factor is then one
+  // base-2 exponential of a multiply-add
+  constexpr float kLog2e = 1.44269504088896341f;
+  float pre[8];
   {
     const float4 *pp = reinterpret_cast<const float4 *>(s_gpart + rg * 128 + 8 * cq);
     const float4 *pa = reinterpret_cast<const float4 *>(s_anc + 8 * cq);
     const float4 p0 = pp[0], p1 = pp[1], a0 = pa[0], a1 = pa[1];
-    pre[0] = p0.x - a0.x; pre[1] = p0.y - a0.y; pre[2] = p0.z - a0.z; pre[3] = p0.w - a0.w;
-    pre[4] = p1.x - a1.x; pre[5] = p1.y - a1.y; pre[6] = p1.z - a1.z; pre[7] = p1.w - a1.w;
+    pre[0] = (p0.x - a0.x) * kLog2e; pre[1] = (p0.y - a0.y) * kLog2e;
+    pre[2] = (p0.z - a0.z) * kLog2e; pre[3] = (p0.w - a0.w) * kLog2e;
+    pre[4] = (p1.x - a1.x) * kLog2e; pre[5] = (p1.y - a1.y) * kLog2e;
+    pre[6] = (p1.z - a1.z) * kLog2e; pre[7] = (p1.w - a1.w) * kLog2e;
   }
-  int out_of_range = 0;
+  float xmax = 0.f;  // largest |G_r - a| log2(e) of the chunk's rows
 #pragma unroll
   for (int rr = 0; rr < 4; ++rr) {
     const int r = 4 * rg + rr;
@@ -380,11 +385,11 @@ __device__ __forceinline__ bool prep_chunk(uint32_t sb, int cl, float beta_r, fl
       const uint32_t kv[4] = {kw.x, kw.y, kw.z, kw.w}, qv[4] = {qw.x, qw.y, qw.z, qw.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float x0 = pre[2 * j] + gl[rr][2 * j];  // G_r - a
-        const float x1 = pre[2 * j + 1] + gl[rr][2 * j + 1];
-        out_of_range |= fabsf(x0) > kMaxHalfDecay || fabsf(x1) > kMaxHalfDecay;
-        const float e0 = __expf(x0), e1 = __expf(x1);
-        const float f0 = __expf(-x0), f1 = __expf(-x1);
+        const float x0 = fmaf(gl[rr][2 * j], kLog2e, pre[2 * j]);  // (G_r - a) log2(e)
+        const float x1 = fmaf(gl[rr][2 * j + 1], kLog2e, pre[2 * j + 1]);
+        xmax = fmaxf(xmax, fmaxf(fabsf(x0), fabsf(x1)));
+        const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+        const float f0 = ex2_approx(-x0), f1 = ex2_approx(-x1);
         const float k0 = bf16lo(kv[j]), k1 = bf16hi(kv[j]);
         const float q0 = bf16lo(qv[j]), q1 = bf16hi(qv[j]);
         kp[j] = pack_bf16x2(k0 * e0, k1 * e1);
@@ -397,7 +402,7 @@ __device__ __forceinline__ bool prep_chunk(uint32_t sb, int cl, float beta_r, fl
     st_shared_v4(sb + og + ck, km[0], km[1], km[2], km[3]);
   }
   fence_async_smem();
-  return __syncthreads_or(out_of_range) != 0;
+  return __syncthreads_or(xmax > kMaxHalfDecay * kLog2e) != 0;
 }
 
 // MMA1: [K+; Q+] K-^T -> d (64 columns: rows 0..63 A-raw, rows 64..127 Q+K-^T).

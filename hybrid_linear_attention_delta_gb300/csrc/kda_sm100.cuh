@@ -34,6 +34,15 @@ __device__ __forceinline__ uint32_t sw128_chunk(int row, int c) {
   return (uint32_t)(row * 128 + ((c ^ (row & 7)) << 4));
 }
 
+// ------------------------------------------------------------------ arithmetic
+// 2^x by the hardware's approximate base-2 exponential (subnormal results flush
+// to zero)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------------------ named CTA barriers
 // Barrier id (1..15; 0 is __syncthreads) over count threads, a multiple of 32;
 // whole warps execute these.  named_bar_arrive signals without waiting (its
