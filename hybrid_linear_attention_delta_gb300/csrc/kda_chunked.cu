@@ -135,9 +135,9 @@ __device__ __forceinline__ int sidx(int r, int i) {
 
 // T = (I + A)^{-1} Diag(beta) for the 64x64 strictly lower A.  X = (I + A)^{-1}
 // is built from 32 x 32 blocks:
-//  * the diagonal blocks X_00, X_11 by forward substitution, each column
-//    shared by two lanes of a warp (rows 0..15 and 16..31; threads 128..255,
-//    so that thread 0 can issue tensor-core work just before the solve);
+//  * the diagonal blocks X_00, X_11 by forward substitution, warps 0-3 on
+//    X_00 and warps 4-7 on X_11, each column shared by four lanes of a warp
+//    (rows 0..7, 8..15, 16..23, 24..31);
 //  * the block below them, X_10 = -X_11 (A_10 X_00), as two 32 x 32 x 32
 //    products on the tensor cores in tf32 (fp32 accumulation; the operands'
 //    11-bit significands keep their rounding under the bf16 rounding T then
@@ -151,10 +151,10 @@ __device__ __forceinline__ int sidx(int r, int i) {
 // A[32b + i][32b + m], written by extract_am), so the substitution runs column
 // by column: once x[m] is known it is folded into the running sums of every
 // later row, and x[m + 1] is one multiply-add away.  T is written as bf16
-// into rows 0..63 of the K-major [T; M] operand at tm; the threads without a
-// diagonal column (0..127) zero its upper block (the rows also hold the decay
-// prefix scratch of the chunk's preparation) and then run side(tid), work of
-// the caller that does not touch the solve's buffers.  bar / phase: the
+// into rows 0..63 of the K-major [T; M] operand at tm, whose upper block
+// threads 0..127 first zero (the rows also hold the decay prefix scratch of
+// the chunk's preparation) after running side(tid), brief work of the caller
+// that does not touch the solve's buffers.  bar / phase: the
 // chunk's MMA barrier and the parity of its next completion (advanced twice).
 // Ends with T fenced for the tensor cores and a barrier; false when a wait
 // gave up (pending then says whether an MMA is still in flight).
@@ -165,29 +165,27 @@ __device__ __forceinline__ bool solve_T(const float *LT, float *XT, const float 
                                         const Side &side) {
   fence_async_smem();  // A10 (extract_am) for the tensor cores
   if (tid < 128) {  // T's upper block: rows 0..31, 16-byte chunks 4..7
-    const int e = tid;
-    *reinterpret_cast<uint4 *>(tm + sw128_chunk(e >> 2, 4 + (e & 3))) = make_uint4(0, 0, 0, 0);
-    side(e);
-  } else {
-    // warp w (of warps 4..7, counted from 0): block b = w / 2, columns
-    // 16 (w % 2) .. +15 of it; a column's rows 0..15 belong to lane c, rows
-    // 16..31 to lane c + 16 (c = lane % 16)
-    const int dt = tid - 128;
-    const int lane = dt & 31, w = dt >> 5, b = w >> 1, half = lane >> 4;
-    const int j = 16 * (w & 1) + (lane & 15), base = 32 * b;
-    const float *lt = LT + b * 1024 + 16 * half;
-    float t[16], xo[16];  // running sums and values of this lane's rows 16 half + e
+    side(tid);
+    *reinterpret_cast<uint4 *>(tm + sw128_chunk(tid >> 2, 4 + (tid & 3))) = make_uint4(0, 0, 0, 0);
+  }
+  {
+    // warp w: block b = w / 4, columns j = 8 (w % 4) .. +7 of it (lane % 8);
+    // lane / 8 picks the column's rows 8 (lane / 8) .. +7
+    const int lane = tid & 31, w = tid >> 5, b = w >> 2, rq = lane >> 3;
+    const int j = 8 * (w & 3) + (lane & 7), base = 32 * b, r0 = 8 * rq;
+    const float *lt = LT + b * 1024 + r0;
+    float t[8], xo[8];  // running sums and values of this lane's rows r0 + e
 #pragma unroll
-    for (int e = 0; e < 16; ++e) t[e] = 0.f;
+    for (int e = 0; e < 8; ++e) t[e] = 0.f;
     auto sel = [&](int m, float v) { return m < j ? 0.f : (m == j ? 1.f : v); };
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {  // columns m0 .. m0 + 3, owned by the lanes of half g / 4
+    for (int g = 0; g < 8; ++g) {  // columns m0 .. m0 + 3, owned by the lanes of rows quarter g / 2
       const int m0 = 4 * g;
-      float l[4][16];  // column m0 + k of A at this lane's rows
+      float l[4][8];  // column m0 + k of A at this lane's rows
 #pragma unroll
       for (int k = 0; k < 4; ++k)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
           const float4 v = *reinterpret_cast<const float4 *>(lt + (m0 + k) * 32 + 4 * q);
           l[k][4 * q] = v.x;
           l[k][4 * q + 1] = v.y;
@@ -195,39 +193,38 @@ __device__ __forceinline__ bool solve_T(const float *LT, float *XT, const float 
           l[k][4 * q + 3] = v.w;
         }
       // the 4 x 4 triangle, on every lane (meaningful on the owner of rows m0..m0+3)
-      const int e0 = m0 & 15;
+      const int e0 = m0 & 7;
       const float y0 = sel(m0, t[e0]);
       const float y1 = sel(m0 + 1, fmaf(-l[0][e0 + 1], y0, t[e0 + 1]));
       const float y2 = sel(m0 + 2, fmaf(-l[1][e0 + 2], y1, fmaf(-l[0][e0 + 2], y0, t[e0 + 2])));
       const float y3 =
           sel(m0 + 3, fmaf(-l[2][e0 + 3], y2,
                            fmaf(-l[1][e0 + 3], y1, fmaf(-l[0][e0 + 3], y0, t[e0 + 3]))));
-      const int src = (lane & 15) + 16 * (g >> 2);
+      const int src = (lane & 7) + 8 * (g >> 1);
       const float x0 = __shfl_sync(0xffffffffu, y0, src), x1 = __shfl_sync(0xffffffffu, y1, src);
       const float x2 = __shfl_sync(0xffffffffu, y2, src), x3 = __shfl_sync(0xffffffffu, y3, src);
-      if (half == (g >> 2)) {
+      if (rq == (g >> 1)) {
         xo[e0] = x0;
         xo[e0 + 1] = x1;
         xo[e0 + 2] = x2;
         xo[e0 + 3] = x3;
       }
 #pragma unroll
-      for (int e = 0; e < 16; ++e)  // columns m0.. of A are zero at rows <= their index
+      for (int e = 0; e < 8; ++e)  // columns m0.. of A are zero at rows <= their index
         t[e] = fmaf(-l[3][e], x3, fmaf(-l[2][e], x2, fmaf(-l[1][e], x1, fmaf(-l[0][e], x0, t[e]))));
     }
     const float bj = beta[base + j];
-    const int r0 = 16 * half;
-    if (b == 0) {  // row j of X_00^T: entries r0 .. r0 + 15
+    if (b == 0) {  // row j of X_00^T: entries r0 .. r0 + 7
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
+      for (int q = 0; q < 2; ++q)
         *reinterpret_cast<float4 *>(XT + sidx(j, r0 + 4 * q)) =
             make_float4(xo[4 * q], xo[4 * q + 1], xo[4 * q + 2], xo[4 * q + 3]);
     } else {
 #pragma unroll
-      for (int e = 0; e < 16; ++e) Xd[sidx(r0 + e, j)] = xo[e];
+      for (int e = 0; e < 8; ++e) Xd[sidx(r0 + e, j)] = xo[e];
     }
 #pragma unroll
-    for (int e = 0; e < 16; ++e) st_bf(tm, sw128_offset(base + r0 + e, base + j), xo[e] * bj);
+    for (int e = 0; e < 8; ++e) st_bf(tm, sw128_offset(base + r0 + e, base + j), xo[e] * bj);
   }
   fence_async_smem();  // X_00^T, X_11 for the tensor cores
   __syncthreads();
@@ -1165,34 +1162,32 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
                reinterpret_cast<float *>(smem + Ly::kLT), sbase + Ly::kTM);
     tc_fence_before();
     __syncthreads();
-    // while threads 128..255 solve for T, threads 0..127 stage Q+' = Q+
-    // Diag(e^{a}) into the lower half of the S0 region
-    auto stage_q = [&](int e0) {
-      for (int e = e0; e < 1024; e += 128) {
-        const int half = e >> 9, r = (e >> 3) & 63, q = e & 7;
-        const uint32_t off = r * 128 + q * 16;
-        const float4 *f = reinterpret_cast<const float4 *>(s_ea + half * 64 + 8 * (q ^ (r & 7)));
-        const float4 f0 = f[0], f1 = f[1];
-        const uint4 w = ld_shared_v4(sb + Ly::kQ + half * 16384 + off);
-        st_shared_v4(sbase + Ly::kS0 + half * 8192 + off,
-                     pack_bf16x2(bf16lo(w.x) * f0.x, bf16hi(w.x) * f0.y),
-                     pack_bf16x2(bf16lo(w.y) * f0.z, bf16hi(w.y) * f0.w),
-                     pack_bf16x2(bf16lo(w.z) * f1.x, bf16hi(w.z) * f1.y),
-                     pack_bf16x2(bf16lo(w.w) * f1.z, bf16hi(w.w) * f1.w));
-      }
-    };
     if (!solve_T(reinterpret_cast<const float *>(smem + Ly::kLT),
                  reinterpret_cast<float *>(smem + Ly::kU), A10,
                  reinterpret_cast<float *>(smem + Ly::kXd), reinterpret_cast<float *>(smem + Ly::kYt),
-                 s_beta, smem + Ly::kTM, tmem, bar_mma, mma_phase, mma_pending, tid, stage_q)) {
+                 s_beta, smem + Ly::kTM, tmem, bar_mma, mma_phase, mma_pending, tid, [](int) {})) {
       aborted = true;
       break;
     }
     if (tid == 0) {
       issue_mma2_coop<Ly>(tmem, sbase + Ly::kTM, sb);
       mma_commit(bar_mma);
-      s_item[2] = next >= 0 ? take_from(raw_ticket) : -1;
     }
+    // while the second MMA runs, Q+' = Q+ Diag(e^{a}) into the lower half of
+    // the S0 region
+    for (int e = tid; e < 1024; e += kThreads) {
+      const int half = e >> 9, r = (e >> 3) & 63, q = e & 7;
+      const uint32_t off = r * 128 + q * 16;
+      const float4 *f = reinterpret_cast<const float4 *>(s_ea + half * 64 + 8 * (q ^ (r & 7)));
+      const float4 f0 = f[0], f1 = f[1];
+      const uint4 w = ld_shared_v4(sb + Ly::kQ + half * 16384 + off);
+      st_shared_v4(sbase + Ly::kS0 + half * 8192 + off,
+                   pack_bf16x2(bf16lo(w.x) * f0.x, bf16hi(w.x) * f0.y),
+                   pack_bf16x2(bf16lo(w.y) * f0.z, bf16hi(w.y) * f0.w),
+                   pack_bf16x2(bf16lo(w.z) * f1.x, bf16hi(w.z) * f1.y),
+                   pack_bf16x2(bf16lo(w.w) * f1.z, bf16hi(w.w) * f1.w));
+    }
+    if (tid == 0) s_item[2] = next >= 0 ? take_from(raw_ticket) : -1;
     if (tid == kPub && n >= kCoopRing) {  // peek at this chunk's ring slot early; it is waited
       // for only if a chain CTA of the pair had not yet copied out the chunk that used it before
       slot_seen = ld_relaxed_u64(a.consumed + u * kCoopRing + n % kCoopRing);
@@ -1209,11 +1204,11 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     // The package is staged in shared memory in its final layout, outside
     // both input stages, then written out with bulk copies: W^ = W Diag(e^{a})
     // in the W buffer, U~^T in the U buffer, K^ and Q+' in the S0 region (staged
-    // during the first MMA), M where the solve left it and e^{G_C} in the
-    // e^{G_C - a} vector.
+    // beside the first and the second MMA), M where the solve left it and
+    // e^{G_C} in its own vector.
     // the chunk two ahead goes to this chunk's stage: its k, v and g tiles are
-    // dead now (q is read once more, below), and thread kPub's warp has no
-    // rows to stage
+    // dead now (its q tiles are requested last, just before the package
+    // stores), and thread kPub's warp has no rows to stage
     if (tid == kPub && after >= 0) issue_kvg(after, st);
     if (after >= 0) tma_pending[st] = true;
     {  // U~^T: TMEM lane = value column c, this warp's 32 tokens -> row c of kU
