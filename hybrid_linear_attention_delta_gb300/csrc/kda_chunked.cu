@@ -1083,14 +1083,14 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
   float beta_r = beta_of(cur);
   uint32_t uses[2] = {0, 0}, mma_phase = 0;
   bool tma_pending[2] = {cur >= 0, next >= 0}, mma_pending = false, aborted = false;
-  // Thread kPub owns the copy engine: at the end of a chunk it requests the
-  // tiles of the chunk two ahead, waits for the ring slot and stores the
-  // package with bulk copies (shared -> global bulk writes run at about
-  // 29 B/cycle per SM, so the loads go first).  At the next chunk's first MMA
-  // it waits until the stores are complete (their sources are then free) and
-  // publishes the package (ready flag).  Thread 0 issues the MMAs and takes
-  // tickets.
-  constexpr int kPub = 64;
+  // Thread kLoad requests the tiles of the chunk two ahead at the end of a
+  // chunk; thread kPub then waits for the ring slot and stores the package
+  // with bulk copies (shared -> global bulk writes run at about 29 B/cycle per
+  // SM, so the loads go first).  At the next chunk's first MMA kPub waits
+  // until the stores are complete (their sources are then free) and publishes
+  // the package (ready flag): its proxy fence then has no tile loads of its
+  // own in flight to order.  Thread 0 issues the MMAs and takes tickets.
+  constexpr int kPub = 64, kLoad = 96;
   bool pend = false;
   unsigned long long *pend_flag = nullptr, pend_tag = 0, slot_seen = 0;
   int raw_ticket = 0;  // thread 0: drawn at a chunk's first MMA, validated at its second
@@ -1209,7 +1209,7 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
     // the chunk two ahead goes to this chunk's stage: its k, v and g tiles are
     // dead now (its q tiles are requested last, just before the package
     // stores), and thread kPub's warp has no rows to stage
-    if (tid == kPub && after >= 0) issue_kvg(after, st);
+    if (tid == kLoad && after >= 0) issue_kvg(after, st);
     if (after >= 0) tma_pending[st] = true;
     {  // U~^T: TMEM lane = value column c, this warp's 32 tokens -> row c of kU
       const int c = quarter * 32 + lane;
@@ -1248,7 +1248,7 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       int ok = 1;
       __syncthreads();
       beta_r = beta_of(next);
-      if (tid == kPub && after >= 0) issue_q(after, st);  // before the stores, on the same engine
+      if (tid == kLoad && after >= 0) issue_q(after, st);  // before the stores
       if (tid == kPub && n >= kCoopRing && slot_seen < coop_tag(a.epoch, n - kCoopRing))
         for (int hv = 0; hv < a.split && ok; ++hv)
           ok = coop_flag_wait(a.consumed + ((size_t)hv * units + u) * kCoopRing + slot,
