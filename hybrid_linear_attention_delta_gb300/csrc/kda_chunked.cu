@@ -910,16 +910,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 // so that with the state itself as the bf16 operand
 //     U = U~ - W^ S,   S_next = Diag(e^{G_C}) S + K^^T U,   O = Q+' S + M U,
 // and the chain CTA works on the transposed state: S^T (bf16, in TMEM) is the
-// A operand of X^T = S^T W^^T and of O^T = S^T Q+'^T; the state warps form
+// A operand of [X^T | O^T] = S^T [W^; Q+']^T (one product of N = 128: a
+// tensor-core instruction with N <= 128 costs about 94 cycles whatever its M
+// and N, measured on GB300, so two products of N = 64 cost twice as much);
+// the state warps form
 // U^T = U~^T - X^T (bf16, in TMEM), the A operand of acc^T = U^T K^ and of
 // O^T += U^T M^T.
 
 // package layout (bytes); each operand in the shared-memory layout the chain
 // CTA feeds to its MMAs (U~ is read by its state warps), copied verbatim
-constexpr uint32_t kPkW = 0;        // W^ [64 tok][128 ch] bf16, K-major, 2 halves x 8 KiB
-constexpr uint32_t kPkKm = 16384;   // K^ [64 tok][128 ch] bf16, 2 halves x 8 KiB
-constexpr uint32_t kPkU = 32768;    // U~^T [128 dv][64 tok] bf16, 128-byte swizzled rows
-constexpr uint32_t kPkQ = 49152;    // Q+' [64 tok][128 ch] bf16, K-major, 2 halves x 8 KiB
+// per channel half h: W^ [64 tok][64 ch] at 16384 h and Q+' [64 tok][64 ch] at
+// 16384 h + 8192 (bf16, K-major), i.e. the 128 rows of one B operand [W^; Q+']
+constexpr uint32_t kPkWQ = 0;
+constexpr uint32_t kPkKm = 32768;   // K^ [64 tok][128 ch] bf16, 2 halves x 8 KiB
+constexpr uint32_t kPkU = 49152;    // U~^T [128 dv][64 tok] bf16, 128-byte swizzled rows
 constexpr uint32_t kPkM = 65536;    // M [64 tok][64 tok] bf16, K-major, 8 KiB
 constexpr uint32_t kPkDec = 73728;  // f32 e^{G_C}[128]
 static_assert(kPkDec + 512 <= kCoopPkgBytes && kCoopPkgBytes % 1024 == 0, "package layout");
@@ -1258,10 +1262,12 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
       // the next chunk's first MMA, where thread kPub waits for the stores
       if (tid == kPub && ok) {
         uint8_t *pk = a.ring + ((size_t)u * kCoopRing + slot) * kCoopPkgBytes;
-        bulk_s2g(pk + kPkW, sbase + Ly::kW, 16384);
+        bulk_s2g(pk + kPkWQ, sbase + Ly::kW, 8192);
+        bulk_s2g(pk + kPkWQ + 8192, sbase + Ly::kS0, 8192);
+        bulk_s2g(pk + kPkWQ + 16384, sbase + Ly::kW + 8192, 8192);
+        bulk_s2g(pk + kPkWQ + 24576, sbase + Ly::kS0 + 8192, 8192);
         bulk_s2g(pk + kPkKm, sbase + Ly::kS0 + 16384, 16384);
         bulk_s2g(pk + kPkU, sbase + Ly::kU, 16384);
-        bulk_s2g(pk + kPkQ, sbase + Ly::kS0, 16384);
         bulk_s2g(pk + kPkM, sbase + Ly::kTM + 8192, 8192);
         bulk_s2g(pk + kPkDec, sbase + Ly::kMisc + Ly::kCke, 512);
         bulk_commit();
@@ -1297,23 +1303,22 @@ __device__ void coop_producer(uint8_t *smem, const CUtensorMap *tm_q, const CUte
 // specialised:
 //   warps 0-3 (state): thread j holds column j of S (row j of S^T) for all 128
 //     channels in fp32 registers.  Per chunk n it stores bf16(S^T) into TMEM
-//     buffer n & 1 (the A operand of the chunk's state-dependent MMAs),
+//     (the A operand of the chunk's state-dependent product; the previous
+//     chunk's, which read it, completed before that chunk's acc^T),
 //     retires chunk n-1's outputs in two halves while X^T and acc^T run, forms
 //     U^T = U~^T - X^T (bf16, into TMEM), then applies
 //     S <- Diag(e^{G_C}) S + acc and writes snapshots.
 //   warp 4, one lane (MMA): per chunk, once package n has landed it hands its
-//     ring slot back to the producers; once S^T is stored, X^T = S^T W^^T
-//     (commit: X ready) and O^T = S^T Q+'^T (it runs while the state warps
-//     form U^T); once they stored U^T = U~^T - X^T, acc^T = U^T K^ (commit:
-//     acc ready) and O^T += U^T M^T (commit: outputs ready, stage free).
-//     (Back to back on one GPU, 2^20-token prefill: 23.2 ms in this order, 24.6 ms
-//     with acc^T ahead of O^T = S^T Q+'^T.)
+//     ring slot back to the producers; once S^T is stored, [X^T | O^T] =
+//     S^T [W^; Q+']^T into buffer n & 1 (commit: X ready); once the state
+//     warps stored U^T = U~^T - X^T, acc^T = U^T K^ (commit: acc ready) and
+//     O^T += U^T M^T (commit: outputs ready, stage free).
 //   warps 5-7, one lane each (loaders): warp 5 + k waits until package n =
 //     k (mod 3) is in the ring and stage k is free, and requests it with bulk
 //     copies; its next package's ready flag is read (acquire) while this one
 //     is in flight.
-// TMEM columns: acc^T [0, 128); O^T[b] [128 + 64 b, +64); S^T[b] as bf16
-// pairs [256 + 64 b, +64); X^T [384, 448); U^T as bf16 pairs [448, 480).
+// TMEM columns: acc^T [0, 128); [X^T | O^T][b] [128 + 128 b, +128); S^T as
+// bf16 pairs [384, 448); U^T as bf16 pairs [448, 480).
 // Every wait is bounded; a role that gives up raises the abort word and
 // leaves its loop, and the others then time out.
 // Warp-uniform bounded wait: every lane polls, and all lanes give up together
@@ -1373,7 +1378,7 @@ __device__ bool chain_state_half(uint8_t *smem, const CoopArgs &a, const CUtenso
     if (hf == 0 && !warp_wait(of0 + 8 * b, (n >> 1) & 1)) return false;
     tc_fence_after();
     uint32_t v[16];
-    tmem_ld16x64_x16(lane_base + 128 + 64 * b + 32 * hf, v);
+    tmem_ld16x64_x16(lane_base + 192 + 128 * b + 32 * hf, v);
     tmem_wait_ld();
     reg_fence16(v);
     if (hf == 1) {
@@ -1413,9 +1418,9 @@ __device__ bool chain_state_half(uint8_t *smem, const CoopArgs &a, const CUtenso
 #pragma unroll
       for (int i = 0; i < 32; ++i) d[(int64_t)(8 * (i >> 1) + 2 * q + (i & 1)) * dv + 8 * s] = S[s][i];
   };
-  // bf16(S^T) channels [64 p, 64 p + 64) -> S^T buffer buf, then its half-p
-  // barrier: X^T's first four MMAs (K = channels 0..63) start while the second
-  // half of the state is still being updated
+  // bf16(S^T) channels [64 p, 64 p + 64) -> TMEM, then the half-p barrier of
+  // chunk parity buf: the first product's first four MMAs (K = channels
+  // 0..63) start while the second half of the state is still being updated
   auto store_st = [&](int buf, int p) {
     uint32_t r[16];
 #pragma unroll
@@ -1423,7 +1428,7 @@ __device__ bool chain_state_half(uint8_t *smem, const CoopArgs &a, const CUtenso
       r[2 * i] = pack_bf16x2(S[0][16 * p + 2 * i], S[0][16 * p + 2 * i + 1]);
       r[2 * i + 1] = pack_bf16x2(S[1][16 * p + 2 * i], S[1][16 * p + 2 * i + 1]);
     }
-    tmem_st16x128_x8(lane_base + 256 + 64 * buf + 32 * p, r);
+    tmem_st16x128_x8(lane_base + 384 + 32 * p, r);
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -1444,7 +1449,7 @@ __device__ bool chain_state_half(uint8_t *smem, const CoopArgs &a, const CUtenso
     const uint32_t sp = sbase + st * (uint32_t)kCoopPkgBytes;
     {  // U^T = U~^T - X^T: tokens 8 r + 2 q + {0, 1} of value columns j0, j0 + 8
       uint32_t x[32], w0[8], w1[8];
-      tmem_ld16x256_x8(lane_base + 384, x);
+      tmem_ld16x256_x8(lane_base + 128 + 128 * b, x);
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
         w0[r] = ld_shared_u32(sp + kPkU + sw128_chunk(j0, r) + 4 * q);
@@ -1581,7 +1586,7 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, const CUtensorMap *
       if (hf == 0 && !warp_wait(of0 + 8 * b, (n >> 1) & 1)) return false;
       tc_fence_after();
       uint32_t v[32];
-      tmem_ld32_async(lane_base + 128 + 64 * b + 32 * hf, v);
+      tmem_ld32_async(lane_base + 192 + 128 * b + 32 * hf, v);
       tmem_wait_ld();
       reg_fence(v);
       if (hf == 1) {
@@ -1607,14 +1612,15 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, const CUtensorMap *
     int64_t snap_next = m.snap_off;
     for (int n = 0; n < N; ++n) {
       const int b = n & 1, st = n % kChStages;
-      // bf16(S^T) -> S^T[b]: column q holds channels 2q (low half) and 2q + 1.
-      // Buffer b was last read by chunk n-2's MMAs, which retire(n-2) waited for.
+      // bf16(S^T) -> TMEM: column q holds channels 2q (low half) and 2q + 1.
+      // The last product to read it, chunk n-1's, completed before that
+      // chunk's acc^T, which the update of chunk n-1 waited for.
 #pragma unroll
       for (int p = 0; p < 2; ++p) {
         uint32_t r[32];
 #pragma unroll
         for (int q = 0; q < 32; ++q) r[q] = pack_bf16x2(S[64 * p + 2 * q], S[64 * p + 2 * q + 1]);
-        tmem_st32(lane_base + 256 + 64 * b + 32 * p, r);
+        tmem_st32(lane_base + 384 + 32 * p, r);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -1630,7 +1636,7 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, const CUtensorMap *
       {  // U^T = U~^T - X^T into tensor memory: column q holds tokens 2q (low half), 2q + 1;
          // row j of the package's U~^T holds this thread's 64 tokens
         float x[64];
-        tmem_ld64(lane_base + 384, x);
+        tmem_ld64(lane_base + 128 + 128 * b, x);
         uint32_t r[32];
 #pragma unroll
         for (int q8 = 0; q8 < 8; ++q8) {  // tokens 8 q8 .. 8 q8 + 7
@@ -1726,23 +1732,19 @@ __device__ void coop_chain(uint8_t *smem, const CoopArgs &a, const CUtensorMap *
       }
       tc_fence_after();
       issued = true;
-      const uint32_t o = tmem + 128 + 64 * b, sa = tmem + 256 + 64 * b, xt = tmem + 384,
-                     ut = tmem + 448;
+      const uint32_t xo = tmem + 128 + 128 * b, o = xo + 64, sa = tmem + 384, ut = tmem + 448;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {  // X^T = S^T W^^T
+      for (int kk = 0; kk < 8; ++kk) {  // [X^T | O^T] = S^T [W^; Q+']^T: one N = 128 product
         if (kHalf && kk == 4) {  // column halves store S^T a channel half at a time
           if (!mbar_wait(sready0 + 88 + 8 * b, (n >> 1) & 1)) { failed = true; break; }
           tc_fence_after();
         }
-        mma_bf16_ts(xt, sa + kk * 8, sw128_desc(sp + kPkW + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
-                    idesc_bf16(kM, 64, 0, 0), kk > 0);
+        mma_bf16_ts(xo, sa + kk * 8,
+                    sw128_desc(sp + kPkWQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                    idesc_bf16(kM, 128, 0, 0), kk > 0);
       }
       if (failed) break;
       mma_commit(xf);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // O^T = S^T Q+'^T
-        mma_bf16_ts(o, sa + kk * 8, sw128_desc(sp + kPkQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024),
-                    idesc_bf16(kM, 64, 0, 0), kk > 0);
       if (!mbar_wait(uready, n & 1)) { failed = true; break; }
       tc_fence_after();
 #pragma unroll
