@@ -1389,8 +1389,10 @@ __device__ bool chain_state_half(uint8_t *smem, const CoopArgs &a, const CUtenso
     const int cl = min(kC, m.len - n * kC) - 32 * hf;
     if (cl >= 32) {
       const uint32_t buf = (uint32_t)(n % kChStages) * (uint32_t)kCoopPkgBytes + obuf + 1024u * hf;
-      if (lane == 0) bulk_wait_read<4>();  // (chunk n - 3's stores of this buffer)
-      __syncwarp();
+      if (hf == 0) {  // chunk n - 3's two stores (four groups since) have read both halves
+        if (lane == 0) bulk_wait_read<4>();
+        __syncwarp();
+      }
 #pragma unroll
       for (int r = 0; r < 16; ++r)
         *reinterpret_cast<__nv_bfloat16 *>(smem + buf + (2 * r + oc) * 32 + 2 * orow) =
